@@ -1,0 +1,141 @@
+"""Seeded synthetic inputs and the named workload shapes.
+
+This module holds no attention arithmetic: it only draws i.i.d. N(0, 1)
+values (fp32 from a seeded CPU generator, rounded to bf16 with
+round-to-nearest-even) and KV lengths, with the shapes of the workloads the
+engine is measured on.  Both the CUDA path and the fp64 oracle are fed from
+here, so the two always see the same bf16 bits.
+
+Workloads (names used throughout the tests and the benchmark):
+
+* ``tiny_mha_causal``   B=1, Hq=Hkv=2, Sq=Skv=128, d=64, causal, scale 1/8, O fp32
+* ``gqa_prefill_3314``  B=1, Hq=28, Hkv=4, Sq=Skv=3314, d=128, causal, scale 1/sqrt(128), O bf16
+* ``gqa_decode_1641``   B=1, Hq=28, Hkv=4, one query token, KV length 1641, d=128,
+                        8 splits (min 1 row per split), merged to O bf16 + LSE fp32
+* ``mha_noncausal_4096_d{64,128,256}``  B=2, Hq=Hkv=16, S=4096, non-causal, scale 1/sqrt(d)
+* ``ragged_gqa_decode_b64`` B=64, Hq=32, Hkv=8, d=128, KV lengths ~ U[512, 8192],
+                        16 splits with at least 512 rows each, O bf16 + LSE fp32
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import torch
+
+
+@dataclass(frozen=True)
+class PrefillShape:
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    Sq: int
+    Skv: int
+    d: int
+    causal: bool
+    scale: float
+    out_dtype: str  # "f32" or "bf16"
+    seed: int
+
+
+@dataclass(frozen=True)
+class DecodeShape:
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    d: int
+    scale: float
+    n_splits: int
+    min_rows_per_split: int
+    seed: int
+    fixed_len: int | None = None          # every sequence this long, or
+    len_range: tuple[int, int] | None = None  # lengths ~ U[lo, hi] from the seed
+    out_dtype: str = "bf16"
+
+
+TINY = PrefillShape("tiny_mha_causal", 1, 2, 2, 128, 128, 64, True, 1.0 / 8.0, "f32", 1001)
+GQA_PREFILL = PrefillShape("gqa_prefill_3314", 1, 28, 4, 3314, 3314, 128, True,
+                           1.0 / math.sqrt(128.0), "bf16", 1002)
+GQA_DECODE = DecodeShape("gqa_decode_1641", 1, 28, 4, 128, 1.0 / math.sqrt(128.0), 8, 1, 1003,
+                         fixed_len=1641)
+
+
+def mha_sweep(d: int) -> PrefillShape:
+    return PrefillShape(f"mha_noncausal_4096_d{d}", 2, 16, 16, 4096, 4096, d, False,
+                        1.0 / math.sqrt(float(d)), "bf16", 1000 + 4 * 10 + d // 64)
+
+
+RAGGED_DECODE = DecodeShape("ragged_gqa_decode_b64", 64, 32, 8, 128, 1.0 / math.sqrt(128.0), 16,
+                            512, 1005, len_range=(512, 8192))
+
+
+def _gen(seed: int) -> torch.Generator:
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    return g
+
+
+def randn_bf16(shape, gen: torch.Generator) -> torch.Tensor:
+    """i.i.d. N(0,1) drawn in fp32, then rounded to bf16 (RNE)."""
+    return torch.randn(*shape, generator=gen, dtype=torch.float32).to(torch.bfloat16)
+
+
+def prefill_inputs(B, Hq, Hkv, Sq, Skv, d, seed):
+    """Q [B,Sq,Hq,d], K/V [B,Skv,Hkv,d] bf16 on the CPU."""
+    g = _gen(seed)
+    q = randn_bf16((B, Sq, Hq, d), g)
+    k = randn_bf16((B, Skv, Hkv, d), g)
+    v = randn_bf16((B, Skv, Hkv, d), g)
+    return q, k, v
+
+
+def prefill_inputs_for(shape: PrefillShape):
+    return prefill_inputs(shape.B, shape.Hq, shape.Hkv, shape.Sq, shape.Skv, shape.d, shape.seed)
+
+
+def kv_lengths(B, lo, hi, seed) -> torch.Tensor:
+    """Per-sequence KV lengths ~ U[lo, hi] (inclusive), int32."""
+    g = _gen(seed)
+    return torch.randint(lo, hi + 1, (B,), generator=g, dtype=torch.int64).to(torch.int32)
+
+
+def decode_inputs(B, Hq, Hkv, d, kv_lens: torch.Tensor, seed, Lmax: int | None = None):
+    """q [B,Hq,d], kcache/vcache [B,Lmax,Hkv,d] bf16 on the CPU."""
+    if Lmax is None:
+        Lmax = int(kv_lens.max().item()) if kv_lens.numel() else 0
+    g = _gen(seed + 7919)
+    q = randn_bf16((B, Hq, d), g)
+    kc = randn_bf16((B, Lmax, Hkv, d), g)
+    vc = randn_bf16((B, Lmax, Hkv, d), g)
+    return q, kc, vc
+
+
+def decode_inputs_for(shape: DecodeShape):
+    if shape.fixed_len is not None:
+        lens = torch.full((shape.B,), shape.fixed_len, dtype=torch.int32)
+    else:
+        lo, hi = shape.len_range
+        lens = kv_lengths(shape.B, lo, hi, shape.seed)
+    q, kc, vc = decode_inputs(shape.B, shape.Hq, shape.Hkv, shape.d, lens, shape.seed)
+    return q, kc, vc, lens
+
+
+def prefill_flops(B, Hq, Sq, Skv, d, causal) -> int:
+    """Algorithmic FLOPs: 4*d per admissible (query, key) pair (2*d for QK^T, 2*d for PV)."""
+    if causal:
+        off = Skv - Sq
+        pairs = 0
+        # admissible keys of query i: j in [0, min(Skv, i + off + 1))
+        for i in range(Sq):
+            pairs += max(0, min(Skv, i + off + 1))
+    else:
+        pairs = Sq * Skv
+    return 4 * d * B * Hq * pairs
+
+
+def decode_kv_bytes(kv_lens, Hkv, d, elem_bytes=2) -> int:
+    """Algorithmic K+V bytes: every cached row of every KV head read once."""
+    total = int(torch.as_tensor(kv_lens).to(torch.int64).sum().item())
+    return total * Hkv * d * elem_bytes * 2
