@@ -1,0 +1,214 @@
+"""ctypes binding of libattn.so (the C ABI in include/attn.h).
+
+Argument marshalling only: every step of the attention path runs in the
+library's CUDA kernels.  The raw entry points keep the C names and argument
+order; the torch helpers below allocate outputs with torch and pass device
+pointers and the current CUDA stream.  If the library is missing this module
+raises -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libattn.so")
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = -1
+ATTN_ERR_UNSUPPORTED = -2
+ATTN_ERR_CUDA = -3
+ATTN_ERR_DEVICE_TIMEOUT = -4
+ATTN_F32 = 0
+ATTN_BF16 = 1
+
+_lock = threading.Lock()
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: status {status} ({attn_strerror(status)})")
+
+
+def load(path: str | None = None):
+    """Load libattn.so (once).  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(
+                f"{p} is missing: build the CUDA library first "
+                "(python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(p)
+        vp, i, f, ull = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_ulonglong
+        lib.attn_prefill_fwd.argtypes = [vp, vp, vp, vp, vp] + [i] * 7 + [f, i, vp]
+        lib.attn_decode_split.argtypes = [vp, vp, vp, vp] + [i] * 5 + [f, i, i, vp, vp, vp]
+        lib.attn_merge.argtypes = [vp, vp, vp, vp] + [i] * 5 + [vp]
+        lib.attn_sync_check.argtypes = [vp]
+        lib.attn_strerror.argtypes = [i]
+        lib.attn_strerror.restype = ctypes.c_char_p
+        lib.attn_version.argtypes = []
+        lib.attn_debug_wait_timeout.argtypes = [ull, vp]
+        for name in ("attn_prefill_fwd", "attn_decode_split", "attn_merge", "attn_sync_check",
+                     "attn_version", "attn_debug_wait_timeout"):
+            getattr(lib, name).restype = i
+        _lib = lib
+        return lib
+
+
+# ------------------------------------------------------------------ raw C ABI
+def attn_prefill_fwd(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, d, causal, scale, o_dtype, stream) -> int:
+    return load().attn_prefill_fwd(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, d, int(causal),
+                                   float(scale), o_dtype, stream)
+
+
+def attn_decode_split(q, kcache, vcache, kv_lens, B, Hq, Hkv, d, max_kv, scale, n_splits,
+                      min_rows_per_split, part_o, part_lse, stream) -> int:
+    return load().attn_decode_split(q, kcache, vcache, kv_lens, B, Hq, Hkv, d, max_kv, float(scale),
+                                    n_splits, min_rows_per_split, part_o, part_lse, stream)
+
+
+def attn_merge(part_o, part_lse, o, lse, B, Hq, n_splits, d, o_dtype, stream) -> int:
+    return load().attn_merge(part_o, part_lse, o, lse, B, Hq, n_splits, d, o_dtype, stream)
+
+
+def attn_sync_check(stream) -> int:
+    return load().attn_sync_check(stream)
+
+
+def attn_strerror(status: int) -> str:
+    return load().attn_strerror(int(status)).decode()
+
+
+def attn_version() -> int:
+    return load().attn_version()
+
+
+def attn_debug_wait_timeout(limit_ns: int, stream) -> int:
+    return load().attn_debug_wait_timeout(int(limit_ns), stream)
+
+
+# ------------------------------------------------------------------ torch helpers
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_handle(stream=None):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check_tensor(t, name, dtype, ndim):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {ndim}-D tensor")
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _out_code(dtype):
+    torch = _torch()
+    if dtype == torch.float32:
+        return ATTN_F32
+    if dtype == torch.bfloat16:
+        return ATTN_BF16
+    raise TypeError(f"unsupported output dtype {dtype}")
+
+
+def prefill(q, k, v, causal: bool = True, scale: float | None = None, out_dtype=None, stream=None,
+            out=None):
+    """Exact attention forward.  q [B,Sq,Hq,d], k/v [B,Skv,Hkv,d] bf16 on the GPU.
+
+    Returns (o [B,Sq,Hq,d] in out_dtype (default bf16), lse [B,Hq,Sq] fp32)."""
+    torch = _torch()
+    out_dtype = out_dtype or torch.bfloat16
+    _check_tensor(q, "q", torch.bfloat16, 4)
+    _check_tensor(k, "k", torch.bfloat16, 4)
+    _check_tensor(v, "v", torch.bfloat16, 4)
+    B, Sq, Hq, d = q.shape
+    _, Skv, Hkv, _ = k.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        o = torch.empty((B, Sq, Hq, d), dtype=out_dtype, device=q.device)
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    else:
+        o, lse = out
+    rc = attn_prefill_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Skv, d,
+                          causal, scale, _out_code(o.dtype), _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_prefill_fwd")
+    return o, lse
+
+
+def decode_split(q, kcache, vcache, kv_lens, n_splits: int, min_rows_per_split: int = 1,
+                 scale: float | None = None, stream=None, out=None):
+    """Split-KV partials.  q [B,Hq,d], caches [B,max_kv,Hkv,d] bf16, kv_lens int32 [B].
+
+    Returns (part_o [B,Hq,n_splits,d] fp32, part_lse [B,Hq,n_splits] fp32)."""
+    torch = _torch()
+    _check_tensor(q, "q", torch.bfloat16, 3)
+    _check_tensor(kcache, "kcache", torch.bfloat16, 4)
+    _check_tensor(vcache, "vcache", torch.bfloat16, 4)
+    _check_tensor(kv_lens, "kv_lens", torch.int32, 1)
+    B, Hq, d = q.shape
+    _, max_kv, Hkv, _ = kcache.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        part_o = torch.empty((B, Hq, n_splits, d), dtype=torch.float32, device=q.device)
+        part_lse = torch.empty((B, Hq, n_splits), dtype=torch.float32, device=q.device)
+    else:
+        part_o, part_lse = out
+    rc = attn_decode_split(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(kv_lens), B, Hq, Hkv, d, max_kv,
+                           scale, n_splits, min_rows_per_split, _ptr(part_o), _ptr(part_lse),
+                           _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_decode_split")
+    return part_o, part_lse
+
+
+def merge(part_o, part_lse, out_dtype=None, stream=None, out=None):
+    """LSE-weighted merge.  Returns (o [B,Hq,d] in out_dtype (default bf16), lse [B,Hq] fp32)."""
+    torch = _torch()
+    out_dtype = out_dtype or torch.bfloat16
+    _check_tensor(part_o, "part_o", torch.float32, 4)
+    _check_tensor(part_lse, "part_lse", torch.float32, 3)
+    B, Hq, n_splits, d = part_o.shape
+    if out is None:
+        o = torch.empty((B, Hq, d), dtype=out_dtype, device=part_o.device)
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=part_o.device)
+    else:
+        o, lse = out
+    rc = attn_merge(_ptr(part_o), _ptr(part_lse), _ptr(o), _ptr(lse), B, Hq, n_splits, d,
+                    _out_code(o.dtype), _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_merge")
+    return o, lse
+
+
+def decode(q, kcache, vcache, kv_lens, n_splits: int, min_rows_per_split: int = 1,
+           scale: float | None = None, out_dtype=None, stream=None):
+    """Split-KV decode followed by the merge: (o [B,Hq,d], lse [B,Hq])."""
+    po, pl = decode_split(q, kcache, vcache, kv_lens, n_splits, min_rows_per_split, scale, stream)
+    return merge(po, pl, out_dtype, stream)
+
+
+def sync_check(stream=None) -> None:
+    rc = attn_sync_check(_stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_sync_check")

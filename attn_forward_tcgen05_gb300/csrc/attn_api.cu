@@ -1,0 +1,221 @@
+// attn_api.cu -- the C ABI declared in include/attn.h: argument validation,
+// TMA tensor-map encoding, kernel launches and device error reporting.
+//
+// The library keeps one static device word per device (g_attn_err) for
+// errors that only the device can see (a bounded pipeline wait that ran out).
+// Its device address is looked up once per device with cudaGetSymbolAddress
+// and handed to every kernel; attn_sync_check() reads and clears it.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/attn.h"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace {
+
+__device__ uint32_t g_attn_err;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+uint32_t* g_err_ptr[kMaxDevices] = {nullptr};
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+int current_device(int* dev) { return cudaGetDevice(dev) == cudaSuccess ? 0 : -1; }
+
+// Device address of this device's error word (looked up once per device).
+uint32_t* err_word() {
+  int dev = 0;
+  if (current_device(&dev) != 0 || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_err_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_attn_err) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<uint32_t*>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+EncodeTiledFn encoder() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  return g_encode;
+}
+
+// 4-D bf16 tensor map over a [n3][n2][n1][n0] row-major tensor (n0 innermost),
+// box {64, 1, box_rows, 1}, 128-byte swizzle, zero fill out of bounds.
+int encode_bf16_4d(CUtensorMap* map, const void* base, uint64_t n0, uint64_t n1, uint64_t n2,
+                   uint64_t n3, uint32_t box_rows) {
+  EncodeTiledFn enc = encoder();
+  if (enc == nullptr) return ATTN_ERR_CUDA;
+  const cuuint64_t dims[4] = {n0, n1, n2, n3};
+  const cuuint64_t strides[3] = {n0 * 2, n0 * n1 * 2, n0 * n1 * n2 * 2};
+  const cuuint32_t box[4] = {64, 1, box_rows, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool ok_dim(int d) { return d == 64 || d == 128 || d == 256; }
+bool ok_scale(float s) { return std::isfinite(s) && s > 0.f; }
+
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int attn_version(void) { return 10000; }
+
+const char* attn_strerror(int status) {
+  switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument (null/misaligned pointer, bad size or head ratio)";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported configuration (head dim or dtype code)";
+    case ATTN_ERR_CUDA: return "CUDA runtime or launch error";
+    case ATTN_ERR_DEVICE_TIMEOUT: return "a kernel's bounded pipeline wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int attn_prefill_fwd(const attn_bf16_t* q, const attn_bf16_t* k, const attn_bf16_t* v, void* o,
+                     float* lse, int B, int Hq, int Hkv, int Sq, int Skv, int d, int causal,
+                     float scale, int o_dtype, attn_stream_t stream) {
+  if (B < 0 || Sq < 0 || Skv < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (!ok_scale(scale)) return ATTN_ERR_INVALID_ARG;
+  if (!ok_dim(d) || (o_dtype != ATTN_F32 && o_dtype != ATTN_BF16)) return ATTN_ERR_UNSUPPORTED;
+  if (B == 0 || Sq == 0) return ATTN_OK;
+  if (!q || !o || !lse || !aligned16(q) || !aligned16(o) || !aligned16(lse))
+    return ATTN_ERR_INVALID_ARG;
+  if (Skv > 0 && (!k || !v || !aligned16(k) || !aligned16(v))) return ATTN_ERR_INVALID_ARG;
+  // row counts of every tensor must fit the kernels' 32-bit row indices
+  if ((long long)B * Sq * Hq >= (1LL << 31) || (long long)B * Skv * Hkv >= (1LL << 31))
+    return ATTN_ERR_INVALID_ARG;
+  attn::PrefillArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.o = o;
+  a.lse = lse;
+  a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.Sq = Sq; a.Skv = Skv; a.d = d;
+  a.causal = causal ? 1 : 0;
+  a.o_bf16 = o_dtype == ATTN_BF16 ? 1 : 0;
+  a.scale = scale;
+  a.err = err_word();
+  if (a.err == nullptr) return ATTN_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (Skv == 0) return from_cuda(attn::launch_prefill_empty_kv(a, s));
+  int rc = encode_bf16_4d(&a.tm_q, q, d, Hq, Sq, B, attn::kPrefillTileM);
+  if (rc == ATTN_OK) rc = encode_bf16_4d(&a.tm_k, k, d, Hkv, Skv, B, attn::kPrefillTileN);
+  if (rc == ATTN_OK) rc = encode_bf16_4d(&a.tm_v, v, d, Hkv, Skv, B, attn::kPrefillTileN);
+  if (rc != ATTN_OK) return rc;
+  return from_cuda(attn::launch_prefill(a, s));
+}
+
+int attn_decode_split(const attn_bf16_t* q, const attn_bf16_t* kcache, const attn_bf16_t* vcache,
+                      const int* kv_lens, int B, int Hq, int Hkv, int d, int max_kv, float scale,
+                      int n_splits, int min_rows_per_split, float* part_o, float* part_lse,
+                      attn_stream_t stream) {
+  if (B < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Hq / Hkv > 16 || max_kv < 1)
+    return ATTN_ERR_INVALID_ARG;
+  if (n_splits < 1 || n_splits > 1024 || min_rows_per_split < 0 || !ok_scale(scale))
+    return ATTN_ERR_INVALID_ARG;
+  if (B > 65535 || Hkv > 65535) return ATTN_ERR_INVALID_ARG;
+  if (!ok_dim(d)) return ATTN_ERR_UNSUPPORTED;
+  if (B == 0) return ATTN_OK;
+  if (!q || !kcache || !vcache || !kv_lens || !part_o || !part_lse) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(part_o) ||
+      (reinterpret_cast<uintptr_t>(kv_lens) & 3u) || (reinterpret_cast<uintptr_t>(part_lse) & 3u))
+    return ATTN_ERR_INVALID_ARG;
+  if ((long long)B * max_kv * Hkv >= (1LL << 31)) return ATTN_ERR_INVALID_ARG;
+  attn::DecodeArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.q = q; a.kv_lens = kv_lens; a.part_o = part_o; a.part_lse = part_lse;
+  a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.d = d; a.max_kv = max_kv;
+  a.n_splits = n_splits; a.min_rows = min_rows_per_split; a.scale = scale;
+  a.err = err_word();
+  if (a.err == nullptr) return ATTN_ERR_CUDA;
+  int rc = encode_bf16_4d(&a.tm_k, kcache, d, Hkv, max_kv, B, attn::kDecodeTileRows);
+  if (rc == ATTN_OK) rc = encode_bf16_4d(&a.tm_v, vcache, d, Hkv, max_kv, B, attn::kDecodeTileRows);
+  if (rc != ATTN_OK) return rc;
+  return from_cuda(attn::launch_decode_split(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int attn_merge(const float* part_o, const float* part_lse, void* o, float* lse, int B, int Hq,
+               int n_splits, int d, int o_dtype, attn_stream_t stream) {
+  if (B < 0 || Hq < 1 || n_splits < 1 || n_splits > 1024) return ATTN_ERR_INVALID_ARG;
+  if (!ok_dim(d) || (o_dtype != ATTN_F32 && o_dtype != ATTN_BF16)) return ATTN_ERR_UNSUPPORTED;
+  if (B == 0) return ATTN_OK;
+  if (!part_o || !part_lse || !o || !lse) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(part_o) || !aligned16(o) || (reinterpret_cast<uintptr_t>(part_lse) & 3u) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return ATTN_ERR_INVALID_ARG;
+  if ((long long)B * Hq >= (1LL << 31)) return ATTN_ERR_INVALID_ARG;
+  attn::MergeArgs a;
+  a.part_o = part_o; a.part_lse = part_lse; a.o = o; a.lse = lse;
+  a.B = B; a.Hq = Hq; a.n_splits = n_splits; a.d = d; a.o_bf16 = o_dtype == ATTN_BF16 ? 1 : 0;
+  return from_cuda(attn::launch_merge(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int attn_sync_check(attn_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return ATTN_ERR_CUDA;
+  uint32_t* e = err_word();
+  if (e == nullptr) return ATTN_ERR_CUDA;
+  uint32_t h = 0;
+  if (cudaMemcpy(&h, e, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (h != 0) {
+    const uint32_t zero = 0;
+    if (cudaMemcpy(e, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return ATTN_ERR_CUDA;
+    return ATTN_ERR_DEVICE_TIMEOUT;
+  }
+  return ATTN_OK;
+}
+
+int attn_debug_wait_timeout(unsigned long long limit_ns, attn_stream_t stream) {
+  if (limit_ns < 1000ull || limit_ns > 10000000000ull) return ATTN_ERR_INVALID_ARG;
+  uint32_t* e = err_word();
+  if (e == nullptr) return ATTN_ERR_CUDA;
+  return from_cuda(attn::launch_wait_timeout_probe(limit_ns, e, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"
+
+namespace attn {
+namespace {
+// One CTA waits on an mbarrier that nothing ever arrives on; the bounded wait
+// gives up after limit_ns, records the timeout and the kernel returns.
+__global__ void wait_timeout_probe_kernel(uint64_t limit_ns, uint32_t* err) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) (void)mbar_wait(&bar, 0, err, &abort_flag, limit_ns);
+}
+}  // namespace
+
+cudaError_t launch_wait_timeout_probe(uint64_t limit_ns, uint32_t* err, cudaStream_t stream) {
+  wait_timeout_probe_kernel<<<1, 32, 0, stream>>>(limit_ns, err);
+  return cudaGetLastError();
+}
+}  // namespace attn

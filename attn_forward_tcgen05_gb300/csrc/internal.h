@@ -1,0 +1,52 @@
+// internal.h -- launch interface between the C-ABI layer (attn_api.cu) and the
+// kernel translation units.  Not part of the public ABI.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace attn {
+
+// Prefill launch description (already validated by the C-ABI layer).
+struct PrefillArgs {
+  CUtensorMap tm_q, tm_k, tm_v;  // 4-D maps {d, H, S, B}, box {64, 1, 128, 1}, 128B swizzle
+  void* o;                       // [B][Sq][Hq][d], fp32 or bf16
+  float* lse;                    // [B][Hq][Sq]
+  int B, Hq, Hkv, Sq, Skv, d, causal, o_bf16;
+  float scale;
+  uint32_t* err;                 // device error word
+};
+
+// Decode-split launch description.
+struct DecodeArgs {
+  CUtensorMap tm_k, tm_v;  // 4-D maps {d, Hkv, max_kv, B}, box {64, 1, 32, 1}, 128B swizzle
+  const uint16_t* q;       // [B][Hq][d] bf16
+  const int* kv_lens;      // [B]
+  float* part_o;           // [B][Hq][n_splits][d]
+  float* part_lse;         // [B][Hq][n_splits]
+  int B, Hq, Hkv, d, max_kv, n_splits, min_rows;
+  float scale;
+  uint32_t* err;
+};
+
+struct MergeArgs {
+  const float* part_o;
+  const float* part_lse;
+  void* o;
+  float* lse;
+  int B, Hq, n_splits, d, o_bf16;
+};
+
+// Rows of a KV tile streamed by the decode producer per pipeline stage.
+constexpr int kDecodeTileRows = 32;
+// Rows of a Q tile / KV tile in the prefill kernel.
+constexpr int kPrefillTileM = 128;
+constexpr int kPrefillTileN = 128;
+
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
+cudaError_t launch_prefill_empty_kv(const PrefillArgs& a, cudaStream_t stream);
+cudaError_t launch_decode_split(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);
+cudaError_t launch_wait_timeout_probe(uint64_t limit_ns, uint32_t* err, cudaStream_t stream);
+
+}  // namespace attn

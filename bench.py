@@ -1,0 +1,464 @@
+#!/usr/bin/env python3
+"""Benchmark of the attention-forward hot path on one GB300 (or N replicas).
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  1. prefill FMHA on gqa_prefill_3314  (B=1, Hq=28, Hkv=4, S=3314, d=128, causal, O bf16)
+  2. split-KV decode + merge on gqa_decode_1641 (B=1, Hq=28, Hkv=4, KV 1641, 8 splits)
+  3. split-KV decode + merge on ragged_gqa_decode_b64 (B=64, Hq=32, Hkv=8, KV ~ U[512,8192])
+L2 is flushed (a 256 MiB device write) before every step, outside the kernel
+events.  `value` is the prefill throughput in TFLOP/s (algorithmic FLOPs:
+4*d per admissible (query, key) pair); the decode throughput (algorithmic K+V
+bytes, every cached row of every KV head read once) is reported beside it.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+With --gpus N > 1 the script expects torchrun (one process per GPU); every rank
+runs an independent replica (the path has no exchange step) and rank 0 prints
+one JSON line with the max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "prefill attn TFLOP/s (% BF16 TC peak); decode KV GB/s (% HBM peak)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, interval_ms: int = 20):
+        self.gpu_index = gpu_index
+        self.interval_ms = interval_ms
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", str(self.interval_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)  # let the sampler start before the timed region
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.05)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+        return False
+
+    def summary(self):
+        rows = []
+        for rec in csv.reader(io.StringIO(getattr(self, "out", "") or "")):
+            if len(rec) < 9:
+                continue
+            try:
+                rows.append({"sm": float(rec[1]), "max": float(rec[2]), "power": float(rec[3]),
+                             "hw": rec[5].strip(), "hw_thermal": rec[6].strip(),
+                             "sw_thermal": rec[7].strip(), "sw_power": rec[8].strip()})
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        busy = [r for r in rows if r["power"] > 0] or rows
+        reasons = set()
+        for r in busy:
+            for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                              ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in busy),
+                "sm_max_mhz": max(r["max"] for r in busy), "reasons": sorted(reasons),
+                "samples": len(busy), "power_w_max": max(r["power"] for r in busy)}
+
+
+# --------------------------------------------------------------------------- ours
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import attn_forward_tcgen05_gb300 as attn
+    from attn_forward_tcgen05_gb300 import workloads as W
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    attn.load()  # fails loudly if the CUDA library is missing
+    peaks, peak_src = load_peaks()
+
+    P = W.GQA_PREFILL
+    D3 = W.GQA_DECODE
+    D5 = W.RAGGED_DECODE
+    # inputs resident in HBM before the timed region
+    q, k, v = [t.to(dev) for t in W.prefill_inputs_for(P)]
+    o = torch.empty((P.B, P.Sq, P.Hq, P.d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((P.B, P.Hq, P.Sq), dtype=torch.float32, device=dev)
+    dec = {}
+    for sh in (D3, D5):
+        qd, kc, vc, lens = W.decode_inputs_for(sh)
+        dec[sh.name] = dict(
+            shape=sh, host=(qd, kc, vc, lens), dev=[t.to(dev) for t in (qd, kc, vc, lens)],
+            part=(torch.empty((sh.B, sh.Hq, sh.n_splits, sh.d), dtype=torch.float32, device=dev),
+                  torch.empty((sh.B, sh.Hq, sh.n_splits), dtype=torch.float32, device=dev)),
+            out=(torch.empty((sh.B, sh.Hq, sh.d), dtype=torch.bfloat16, device=dev),
+                 torch.empty((sh.B, sh.Hq), dtype=torch.float32, device=dev)),
+            kv_bytes=W.decode_kv_bytes(lens, sh.Hkv, sh.d))
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flops = W.prefill_flops(P.B, P.Hq, P.Sq, P.Skv, P.d, P.causal)
+    stream = torch.cuda.current_stream()
+
+    do_prefill = args.only in (None, "prefill")
+    do_decode = args.only in (None, "decode")
+
+    def step(ev=None):
+        flush.zero_()  # evict L2 (outside the kernel events)
+        if ev is not None:
+            ev[0].record(stream)
+        if do_prefill:
+            attn.prefill(q, k, v, causal=P.causal, scale=P.scale, out=(o, lse))
+        if ev is not None:
+            ev[1].record(stream)
+        i = 2
+        for name in ((D3.name, D5.name) if do_decode else ()):
+            dd = dec[name]
+            sh = dd["shape"]
+            qd, kc, vc, lens = dd["dev"]
+            attn.decode_split(qd, kc, vc, lens, sh.n_splits, sh.min_rows_per_split, sh.scale,
+                              out=dd["part"])
+            if ev is not None:
+                ev[i].record(stream)
+            attn.merge(dd["part"][0], dd["part"][1], torch.bfloat16, out=dd["out"])
+            if ev is not None:
+                ev[i + 1].record(stream)
+            i += 2
+        if not do_decode and ev is not None:
+            for e in ev[2:]:
+                e.record(stream)
+
+    # warm-up
+    for _ in range(args.warmup):
+        step()
+    attn.sync_check()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as sampler:
+        barrier()
+        torch.cuda.synchronize()
+        t_start.record(stream)
+        for s in range(args.steps):
+            step(evs[s])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    attn.sync_check()
+    clocks = sampler.summary()
+
+    # per-kernel device times (ms), averaged over the K timed steps
+    def avg(a, b):
+        return sum(evs[s][a].elapsed_time(evs[s][b]) for s in range(args.steps)) / args.steps
+
+    t_prefill = avg(0, 1)
+    t_split3 = avg(1, 2)
+    t_merge3 = avg(2, 3)
+    t_split5 = avg(3, 4)
+    t_merge5 = avg(4, 5)
+    ms_step = t_prefill + t_split3 + t_merge3 + t_split5 + t_merge5
+    wall_ms = t_start.elapsed_time(t_end)
+
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([ms_step, t_prefill, t_split5 + t_merge5, wall_ms], dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_step, t_prefill_max, t_dec5_max, wall_ms = [float(x) for x in tt]
+    else:
+        t_prefill_max, t_dec5_max = t_prefill, t_split5 + t_merge5
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = None if (args.no_e2e or args.only) else run_e2e(args, attn, W, dev, stream, P, dec, flops)
+
+    if rank != 0:
+        return None
+    prefill_tflops = world * flops / (max(t_prefill_max, 1e-9) * 1e-3) / 1e12
+    kv5 = dec[D5.name]["kv_bytes"]
+    kv3 = dec[D3.name]["kv_bytes"]
+    dec_gbs = world * kv5 / (max(t_dec5_max, 1e-9) * 1e-3) / 1e9
+    split_gbs = kv5 / (max(t_split5, 1e-9) * 1e-3) / 1e9
+    peak_tc = float(peaks["bf16_tflops"])
+    peak_hbm = float(peaks["hbm_gbs"])
+    traffic = load_traffic()
+    line = {
+        "metric": METRIC,
+        "value": round(prefill_tflops, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"{P.name} + {D3.name} + {D5.name}",
+                   "prefill": {"B": P.B, "Hq": P.Hq, "Hkv": P.Hkv, "Sq": P.Sq, "Skv": P.Skv,
+                               "d": P.d, "causal": P.causal, "o_dtype": "bf16"},
+                   "decode_1641": {"B": D3.B, "Hq": D3.Hq, "Hkv": D3.Hkv, "kv_len": D3.fixed_len,
+                                   "d": D3.d, "n_splits": D3.n_splits},
+                   "decode_ragged": {"B": D5.B, "Hq": D5.Hq, "Hkv": D5.Hkv, "d": D5.d,
+                                     "kv_len_range": list(D5.len_range), "n_splits": D5.n_splits,
+                                     "min_rows_per_split": D5.min_rows_per_split},
+                   "l2": "flushed before every step (256 MiB device write)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "tensor", "kernel": "fmha_fwd_kernel<128>",
+                     "achieved": round(prefill_tflops / world, 2), "peak": peak_tc,
+                     "unit": "TFLOP/s", "frac": round(prefill_tflops / world / peak_tc, 4),
+                     "traffic": traffic.get("fmha_fwd_kernel<128>"),
+                     "peak_source": f"bf16_tflops (burst) of {peak_src}"},
+        "decode": {"value": round(dec_gbs, 1), "unit": "GB/s", "workload": D5.name,
+                   "kv_bytes": kv5, "split_us": round(t_split5 * 1e3, 2),
+                   "merge_us": round(t_merge5 * 1e3, 2),
+                   "roofline": {"bound": "hbm", "kernel": "decode_split_kernel<128,4>",
+                                "achieved": round(split_gbs, 1), "peak": peak_hbm, "unit": "GB/s",
+                                "frac": round(split_gbs / peak_hbm, 4),
+                                "traffic": traffic.get("decode_split_kernel<128,4>"),
+                                "peak_source": f"hbm_gbs of {peak_src}"},
+                   "gqa_decode_1641": {"split_us": round(t_split3 * 1e3, 2),
+                                       "merge_us": round(t_merge3 * 1e3, 2),
+                                       "kv_bytes": kv3,
+                                       "GB_per_s": round(kv3 / (max(t_split3 + t_merge3, 1e-9) * 1e-3) / 1e9, 1)}},
+        "prefill_us": round(t_prefill * 1e3, 2),
+        "wall_ms_timed_region": round(wall_ms, 3),
+        "gpu_launches": (int(do_prefill) + 4 * int(do_decode)) * args.steps,
+        "e2e": e2e,
+        "clocks": clocks,
+    }
+    return line
+
+
+def run_e2e(args, attn, W, dev, stream, P, dec, flops):
+    """Same step through the public API from pinned host buffers: H2D of every
+    input, the kernels, D2H of every output, all inside the timed region."""
+    import torch
+
+    qh, kh, vh = [t.pin_memory() for t in W.prefill_inputs_for(P)]
+    qd, kd, vd = [torch.empty_like(t, device=dev) for t in (qh, kh, vh)]
+    oh = torch.empty((P.B, P.Sq, P.Hq, P.d), dtype=torch.bfloat16).pin_memory()
+    lh = torch.empty((P.B, P.Hq, P.Sq), dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
+    d2h = oh.numel() * 2 + lh.numel() * 4
+    dec_h = {}
+    for name, dd in dec.items():
+        hs = [t.pin_memory() for t in dd["host"]]
+        ds = [torch.empty_like(t, device=dev) for t in hs]
+        sh = dd["shape"]
+        oh2 = torch.empty((sh.B, sh.Hq, sh.d), dtype=torch.bfloat16).pin_memory()
+        lh2 = torch.empty((sh.B, sh.Hq), dtype=torch.float32).pin_memory()
+        dec_h[name] = (hs, ds, oh2, lh2, sh, dd["kv_bytes"])
+        h2d += sum(t.numel() * t.element_size() for t in hs)
+        d2h += oh2.numel() * 2 + lh2.numel() * 4
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        for h, d_ in zip((qh, kh, vh), (qd, kd, vd)):
+            d_.copy_(h, non_blocking=True)
+        o, lse = attn.prefill(qd, kd, vd, causal=P.causal, scale=P.scale)
+        oh.copy_(o, non_blocking=True)
+        lh.copy_(lse, non_blocking=True)
+        if ev is not None:
+            ev[1].record(stream)
+        i = 2
+        for name, (hs, ds, oh2, lh2, sh, _) in dec_h.items():
+            for h, d_ in zip(hs, ds):
+                d_.copy_(h, non_blocking=True)
+            o2, l2 = attn.decode(ds[0], ds[1], ds[2], ds[3], sh.n_splits, sh.min_rows_per_split,
+                                 sh.scale)
+            oh2.copy_(o2, non_blocking=True)
+            lh2.copy_(l2, non_blocking=True)
+            if ev is not None:
+                ev[i].record(stream)
+            i += 1
+
+    for _ in range(max(1, min(args.warmup, 3))):
+        step()
+    torch.cuda.synchronize()
+    n = max(1, min(args.steps, 20))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
+    for s in range(n):
+        step(evs[s])
+    torch.cuda.synchronize()
+    t_pre = sum(e[0].elapsed_time(e[1]) for e in evs) / n
+    names = list(dec_h)
+    t_d5 = sum(e[2].elapsed_time(e[3]) for e in evs) / n
+    kv5 = dec_h[names[1]][5]
+    return {"value": round(flops / (t_pre * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "steps": n, "prefill_ms": round(t_pre, 4),
+            "decode_ragged_GB_per_s": round(kv5 / (t_d5 * 1e-3) / 1e9, 1),
+            "decode_ragged_ms": round(t_d5, 4),
+            "note": "pinned host buffers; H2D of all inputs and D2H of O and LSE inside the timed region"}
+
+
+def load_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if present."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f)
+    return {}
+
+
+# --------------------------------------------------------------------------- CPU baseline
+def cpu_baseline(budget_s: float = 12.0, seed: int = 0):
+    """The fp64 oracle as it stands, timed on the host cores over a bounded sample
+    of the prefill workload: every query row of a strided subset of rows of all
+    heads.  Returns (GFLOP/s, threads, sample description)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from attn_forward_tcgen05_gb300 import workloads as W
+
+    P = W.GQA_PREFILL
+    q, k, v = W.prefill_inputs_for(P)
+    qn, kn, vn = (t.to(torch.float64).numpy() for t in (q, k, v))
+    cores = oracle.num_cores()
+    # calibrate on a small sample, then size the sample to the time budget
+    stride = 64
+    rows = [(0, h, i) for h in range(P.Hq) for i in range(stride // 2, P.Sq, stride)]
+    t0 = time.perf_counter()
+    oracle.sdpa_rows(qn, kn, vn, P.causal, P.scale, rows, nthreads=cores)
+    dt = time.perf_counter() - t0
+    target = max(1, int(len(rows) * budget_s / max(dt, 1e-3)))
+    stride2 = max(1, int(P.Sq * P.Hq / target))
+    rng = np.random.default_rng(seed)
+    rows = [(0, h, i) for h in range(P.Hq) for i in range(int(rng.integers(stride2)), P.Sq, stride2)]
+    t0 = time.perf_counter()
+    oracle.sdpa_rows(qn, kn, vn, P.causal, P.scale, rows, nthreads=cores)
+    dt = time.perf_counter() - t0
+    fl = sum(4 * P.d * (i + 1) for _, _, i in rows)
+    return fl / dt / 1e9, cores, dt, len(rows), stride2
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the fp64 CPU oracle as it stands, on the same workload."""
+    if rank != 0:
+        return None
+    from attn_forward_tcgen05_gb300 import workloads as W
+    P = W.GQA_PREFILL
+    per_step = []
+    info = None
+    for s in range(args.warmup + args.steps):
+        budget = 2.0 if s < args.warmup else 6.0
+        g, cores, dt, n_rows, stride = cpu_baseline(budget_s=budget, seed=s)
+        if s >= args.warmup:
+            per_step.append(g)
+            info = (cores, n_rows, stride)
+    val = statistics.median(per_step) / 1e3  # TFLOP/s
+    cores, n_rows, stride = info
+    sample = (f"{n_rows} query rows (every {stride}th row of each of the {P.Hq} heads) of "
+              f"{P.name}; 4*d FLOPs per admissible (query, key) pair")
+    return {"metric": METRIC, "value": round(val, 6), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": P.name, "B": P.B, "Hq": P.Hq, "Hkv": P.Hkv, "Sq": P.Sq,
+                       "d": P.d, "causal": P.causal},
+            "cpu_baseline": {"value": round(val, 6), "unit": "TFLOP/s", "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(val, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--only", choices=("prefill", "decode"), default=None,
+                    help="time only one part of the step (profiling runs)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus:
+        if args.gpus > 1:
+            sys.exit(f"--gpus {args.gpus} needs torchrun with {args.gpus} processes")
+    if args.impl == "reference":
+        if world > 1 and rank != 0:
+            return
+        line = run_reference(args, rank, world)
+        print(json.dumps(line))
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    line = run_ours(args, rank, world, local_rank)
+    if rank == 0 and line is not None:
+        if not args.no_cpu_baseline and not args.only:
+            g, cores, dt, n_rows, stride = cpu_baseline()
+            line["cpu_baseline"] = {
+                "value": round(g / 1e3, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                "seconds": round(dt, 2),
+                "sample": f"{n_rows} query rows (every {stride}th row of each head) of "
+                          f"{W_name()}; fp64, all host threads"}
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def W_name():
+    from attn_forward_tcgen05_gb300 import workloads as W
+    return W.GQA_PREFILL.name
+
+
+if __name__ == "__main__":
+    main()

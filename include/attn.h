@@ -1,0 +1,172 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) attention-forward engine.
+ *
+ * Exact scaled-dot-product attention with online softmax,
+ *     O = softmax(scale * Q K^T + causal mask) V,   LSE_i = ln sum_j exp(scale * q_i . k_j),
+ * in two shapes: a prefill FMHA (tcgen05 tensor cores, TMEM accumulators, TMA
+ * loads) and a GQA split-KV decode (per-split partials, then an LSE-weighted
+ * merge) on CUDA cores.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Pointers are DEVICE pointers owned by the caller (e.g. torch tensors'
+ *    data_ptr()).  The library allocates nothing per call and never frees a
+ *    caller's buffer.  It keeps one small static device word per device for
+ *    error reporting.
+ *  - bf16 buffers hold raw bfloat16 bits (attn_bf16_t).  Every tensor is
+ *    dense, row-major, contiguous in the layout stated for it, and 16-byte
+ *    aligned (the TMA engine reads whole 16-byte units).
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream).  A return of ATTN_OK means "validated and enqueued".
+ *    Faults that can only be seen on the device (a pipeline wait that ran out
+ *    of time) are reported by attn_sync_check().
+ *  - On ATTN_ERR_INVALID_ARG / ATTN_ERR_UNSUPPORTED nothing is launched and no
+ *    output is written.  There is no fallback path: an unsupported shape is an
+ *    error, never a slow substitute.
+ *  - Empty work (B == 0, Sq == 0) is a valid no-op returning ATTN_OK.
+ *
+ * Causal alignment: query i of Sq sits at key position i + (Skv - Sq)
+ * (bottom-right); with Sq == Skv this is the usual lower-triangular mask.  A
+ * query with no admissible key (only possible when Sq > Skv) gets O = 0 and
+ * LSE = -inf.  GQA: query head hq reads KV head hq / (Hq / Hkv).
+ */
+#ifndef ATTN_GB300_ATTN_H
+#define ATTN_GB300_ATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t attn_bf16_t;         /* raw bfloat16 bits */
+typedef struct CUstream_st* attn_stream_t; /* == cudaStream_t */
+
+/* status codes */
+#define ATTN_OK 0
+#define ATTN_ERR_INVALID_ARG (-1)    /* null/misaligned pointer, bad size, Hq % Hkv != 0, ... */
+#define ATTN_ERR_UNSUPPORTED (-2)    /* head_dim not in {64, 128, 256}, unknown dtype code */
+#define ATTN_ERR_CUDA (-3)           /* a CUDA runtime/driver call or a launch failed */
+#define ATTN_ERR_DEVICE_TIMEOUT (-4) /* a kernel's bounded wait ran out (attn_sync_check only) */
+
+/* output dtype codes */
+#define ATTN_F32 0
+#define ATTN_BF16 1
+
+/*
+ * attn_prefill_fwd -- exact attention forward, prefill shape (FMHA).
+ *
+ * Computes, for every batch b, query head hq and query row i,
+ *   O[b,i,hq,:] = sum_j P_ij V[b,j,hk,:],  P_ij = exp(S_ij - LSE_i),
+ *   S_ij = scale * Q[b,i,hq,:] . K[b,j,hk,:]  (j admissible),  hk = hq / (Hq/Hkv),
+ *   LSE[b,hq,i] = ln sum_j exp(S_ij)          (natural log).
+ * The pages this follows: "60 . r57 -- FA KV staging double buffering
+ * (REVERTED)", section 2.3 (online softmax: running row max and an
+ * exp(m_old - m_new) rescale of O at every KV tile boundary, which regroups
+ * the exact softmax sum); "STAGE_D.md -- FMHA Kernel Development", Kernel
+ * Output (O from P = exp(S*scale - row_max), LSE from the row sum), Architecture
+ * (TMA warp, MMA warp, softmax warps) and TMEM Layout (S, P and O in tensor
+ * memory).  Unlike that page, O is normalised inside the kernel and LSE is in
+ * natural-log units.
+ *
+ * Arguments
+ *   q    bf16 [B][Sq][Hq][d]      queries
+ *   k    bf16 [B][Skv][Hkv][d]    keys
+ *   v    bf16 [B][Skv][Hkv][d]    values
+ *   o    [B][Sq][Hq][d], fp32 (o_dtype = ATTN_F32) or bf16 (ATTN_BF16)
+ *   lse  fp32 [B][Hq][Sq]
+ *   B, Hq, Hkv, Sq, Skv   sizes: B, Sq, Skv >= 0; Hq, Hkv >= 1; Hq % Hkv == 0;
+ *                         Sq, Skv < 2^31; every tensor < 2^31 rows of d elements
+ *   d                     head dim: 64, 128 or 256
+ *   causal                0 = full attention, else bottom-right causal mask
+ *   scale                 softmax scale (finite, > 0), e.g. 1/sqrt(d)
+ *   o_dtype               ATTN_F32 or ATTN_BF16
+ *   stream                CUDA stream the work is enqueued on
+ * Returns ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED or ATTN_ERR_CUDA.
+ */
+int attn_prefill_fwd(const attn_bf16_t* q, const attn_bf16_t* k, const attn_bf16_t* v, void* o,
+                     float* lse, int B, int Hq, int Hkv, int Sq, int Skv, int d, int causal,
+                     float scale, int o_dtype, attn_stream_t stream);
+
+/*
+ * attn_decode_split -- one-token GQA decode, split-KV partials.
+ *
+ * For every batch b, KV head hk and split s, the rows [lo, hi) of sequence b
+ * (split rule below) are streamed once; the G = Hq/Hkv query heads that share
+ * hk all use each loaded K/V row.  Per query head hq and split s:
+ *   part_lse[b,hq,s]  = ln sum_{j in [lo,hi)} exp(s_j),   s_j = scale * q[b,hq,:] . kcache[b,j,hk,:]
+ *   part_o[b,hq,s,:]  = sum_{j in [lo,hi)} exp(s_j - part_lse[b,hq,s]) vcache[b,j,hk,:]
+ * i.e. each partial O is normalised within its own split (not globally), so
+ * attn_merge needs only (part_o, part_lse).  An empty split (lo == hi) gets
+ * part_lse = -inf and part_o = 0.
+ * Split rule: chunk_b = max(ceil(L_b / n_splits), min_rows_per_split); split s
+ * covers [s*chunk_b, min(L_b, (s+1)*chunk_b)).
+ * Follows "66 . D2: explicit K+V register staging", section 3.2 (one split =
+ * rows [lo, hi) of one sequence and KV head; score, running max, running sum
+ * and running O) and section 2.2 (K and V loads issued ahead of the
+ * exp/shuffle chain -- here by a TMA producer warp into a shared-memory ring).
+ *
+ * Arguments
+ *   q         bf16 [B][Hq][d]             one query token per sequence
+ *   kcache    bf16 [B][max_kv][Hkv][d]    keys; rows >= kv_lens[b] are never read as data
+ *   vcache    bf16 [B][max_kv][Hkv][d]    values
+ *   kv_lens   int32 [B] (device)          L_b, 0 <= L_b <= max_kv (values are trusted
+ *                                         to be in range; they are clamped on the device)
+ *   B, Hq, Hkv, d, max_kv                 B >= 0, Hq % Hkv == 0, Hq/Hkv <= 16, d == 128, max_kv >= 1
+ *   scale                                 softmax scale (finite, > 0)
+ *   n_splits                              >= 1 and <= 1024
+ *   min_rows_per_split                    >= 0
+ *   part_o    fp32 [B][Hq][n_splits][d]   output (scratch for attn_merge)
+ *   part_lse  fp32 [B][Hq][n_splits]      output
+ */
+int attn_decode_split(const attn_bf16_t* q, const attn_bf16_t* kcache, const attn_bf16_t* vcache,
+                      const int* kv_lens, int B, int Hq, int Hkv, int d, int max_kv, float scale,
+                      int n_splits, int min_rows_per_split, float* part_o, float* part_lse,
+                      attn_stream_t stream);
+
+/*
+ * attn_merge -- LSE-weighted combine of split partials.
+ *
+ *   M = max_s part_lse[b,hq,s],  w_s = exp(part_lse[b,hq,s] - M),
+ *   o[b,hq,:]  = sum_s w_s part_o[b,hq,s,:] / sum_s w_s,
+ *   lse[b,hq]  = M + ln sum_s w_s.
+ * Empty splits (part_lse = -inf) are skipped without reading their part_o; if
+ * every split is empty, o = 0 and lse = -inf.  Follows the split-combine step
+ * of "66 . D2: explicit K+V register staging", section 5.2, and the LSE merge
+ * of two partial results in "STAGE_D.md -- FMHA Kernel Development", D5.
+ *
+ * Arguments
+ *   part_o    fp32 [B][Hq][n_splits][d],  part_lse fp32 [B][Hq][n_splits]
+ *   o         [B][Hq][d], fp32 or bf16 per o_dtype;  lse fp32 [B][Hq]
+ *   B >= 0, Hq >= 1, n_splits in [1, 1024], d in {64, 128, 256}
+ */
+int attn_merge(const float* part_o, const float* part_lse, void* o, float* lse, int B, int Hq,
+               int n_splits, int d, int o_dtype, attn_stream_t stream);
+
+/*
+ * attn_sync_check -- synchronise `stream`, then read and clear this device's
+ * error word.  Returns ATTN_OK, ATTN_ERR_DEVICE_TIMEOUT (a kernel's bounded
+ * wait gave up; that kernel's outputs are invalid) or ATTN_ERR_CUDA.
+ */
+int attn_sync_check(attn_stream_t stream);
+
+/* Human-readable text for a status code (static storage, never NULL). */
+const char* attn_strerror(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int attn_version(void);
+
+/*
+ * attn_debug_wait_timeout -- test hook for the bounded-wait machinery.
+ * Launches one CTA that waits on an mbarrier nobody arrives on, with a limit of
+ * `limit_ns` nanoseconds (1e3 .. 1e10), then records ATTN_ERR_DEVICE_TIMEOUT in
+ * the error word and exits.  attn_sync_check() then reports the timeout.  The
+ * kernel never hangs and never faults.
+ */
+int attn_debug_wait_timeout(unsigned long long limit_ns, attn_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_ATTN_H */

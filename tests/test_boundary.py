@@ -1,0 +1,78 @@
+"""The C-ABI library: it loads, exports every declared symbol, and rejects bad
+arguments on the host (no GPU needed: validation runs before any CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import attn_forward_tcgen05_gb300 as attn
+from attn_forward_tcgen05_gb300 import build as attn_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    attn_build.build()
+    return attn.load()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:int|const char\*)\s+(attn_\w+)\s*\(", text, re.M)))
+
+
+def test_exports_every_declared_symbol(lib):
+    syms = declared_symbols()
+    assert len(syms) >= 7
+    for s in syms:
+        assert hasattr(lib, s), f"{s} declared in attn.h but not exported"
+
+
+def test_version_and_strerror(lib):
+    assert attn.attn_version() >= 10000
+    for code in (0, -1, -2, -3, -4):
+        assert attn.attn_strerror(code)
+    assert attn.attn_strerror(12345) == "unknown status"
+
+
+N = None  # null pointer
+P = ctypes.c_void_p(16)  # an aligned non-null dummy (never dereferenced: validation fails first)
+M = ctypes.c_void_p(18)  # misaligned
+
+
+def test_prefill_validation(lib):
+    f = attn.attn_prefill_fwd
+    assert f(P, P, P, P, P, 1, 2, 2, 4, 4, 96, 1, 0.5, 0, N) == attn.ATTN_ERR_UNSUPPORTED  # d
+    assert f(P, P, P, P, P, 1, 2, 2, 4, 4, 64, 1, 0.5, 7, N) == attn.ATTN_ERR_UNSUPPORTED  # dtype
+    assert f(P, P, P, P, P, 1, 3, 2, 4, 4, 64, 1, 0.5, 0, N) == attn.ATTN_ERR_INVALID_ARG  # Hq % Hkv
+    assert f(P, P, P, P, P, -1, 2, 2, 4, 4, 64, 1, 0.5, 0, N) == attn.ATTN_ERR_INVALID_ARG
+    assert f(P, P, P, P, P, 1, 2, 2, 4, 4, 64, 1, 0.0, 0, N) == attn.ATTN_ERR_INVALID_ARG  # scale
+    assert f(P, P, P, P, P, 1, 2, 2, 4, 4, 64, 1, float("nan"), 0, N) == attn.ATTN_ERR_INVALID_ARG
+    assert f(N, P, P, P, P, 1, 2, 2, 4, 4, 64, 1, 0.5, 0, N) == attn.ATTN_ERR_INVALID_ARG  # null q
+    assert f(P, P, M, P, P, 1, 2, 2, 4, 4, 64, 1, 0.5, 0, N) == attn.ATTN_ERR_INVALID_ARG  # misaligned v
+    assert f(N, N, N, N, N, 0, 2, 2, 4, 4, 64, 1, 0.5, 0, N) == attn.ATTN_OK  # empty batch: no-op
+    assert f(N, N, N, N, N, 2, 2, 2, 0, 4, 64, 1, 0.5, 0, N) == attn.ATTN_OK  # no queries: no-op
+
+
+def test_decode_and_merge_validation(lib):
+    f = attn.attn_decode_split
+    assert f(P, P, P, P, 1, 28, 4, 96, 10, 0.1, 8, 1, P, P, N) == attn.ATTN_ERR_UNSUPPORTED
+    assert f(P, P, P, P, 1, 28, 5, 128, 10, 0.1, 8, 1, P, P, N) == attn.ATTN_ERR_INVALID_ARG
+    assert f(P, P, P, P, 1, 34, 2, 128, 10, 0.1, 8, 1, P, P, N) == attn.ATTN_ERR_INVALID_ARG  # G > 16
+    assert f(P, P, P, P, 1, 28, 4, 128, 10, 0.1, 0, 1, P, P, N) == attn.ATTN_ERR_INVALID_ARG  # n_splits
+    assert f(P, P, P, P, 1, 28, 4, 128, 0, 0.1, 8, 1, P, P, N) == attn.ATTN_ERR_INVALID_ARG  # max_kv
+    assert f(P, P, P, N, 1, 28, 4, 128, 10, 0.1, 8, 1, P, P, N) == attn.ATTN_ERR_INVALID_ARG  # lens
+    assert f(N, N, N, N, 0, 28, 4, 128, 10, 0.1, 8, 1, N, N, N) == attn.ATTN_OK
+    g = attn.attn_merge
+    assert g(P, P, P, P, 1, 4, 8, 100, 1, N) == attn.ATTN_ERR_UNSUPPORTED
+    assert g(P, P, P, P, 1, 4, 0, 128, 1, N) == attn.ATTN_ERR_INVALID_ARG
+    assert g(P, P, M, P, 1, 4, 8, 128, 1, N) == attn.ATTN_ERR_INVALID_ARG
+    assert g(N, N, N, N, 0, 4, 8, 128, 1, N) == attn.ATTN_OK
+
+
+def test_debug_wait_limits(lib):
+    assert attn.attn_debug_wait_timeout(10, N) == attn.ATTN_ERR_INVALID_ARG
+    assert attn.attn_debug_wait_timeout(10**11, N) == attn.ATTN_ERR_INVALID_ARG

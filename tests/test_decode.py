@@ -1,0 +1,74 @@
+"""Split-KV decode and merge against the fp64 oracle, through the C ABI."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from attn_forward_tcgen05_gb300 import decode_split, merge
+from attn_forward_tcgen05_gb300 import workloads as W
+from tests.tolerances import check_lse, check_o
+
+pytestmark = pytest.mark.gpu
+
+
+def _compare(q, kc, vc, lens, n_splits, min_rows, scale, out_dtype=torch.bfloat16):
+    po, pl = decode_split(q.cuda(), kc.cuda(), vc.cuda(), lens.cuda(), n_splits, min_rows, scale)
+    o, lse = merge(po, pl, out_dtype)
+    torch.cuda.synchronize()
+    rpo, rpl = oracle.decode_split(q, kc, vc, lens, scale, n_splits, min_rows)
+    ro, rl = oracle.decode(q, kc, vc, lens, scale)
+    check_lse(pl.cpu().numpy(), rpl, "part_lse")
+    check_o(po.cpu().numpy(), rpo, False, "part_o")
+    check_o(o.float().cpu().numpy(), ro, out_dtype == torch.bfloat16, "O")
+    check_lse(lse.cpu().numpy(), rl, "LSE")
+
+
+def test_gqa_decode_1641():
+    s = W.GQA_DECODE
+    q, kc, vc, lens = W.decode_inputs_for(s)
+    _compare(q, kc, vc, lens, s.n_splits, s.min_rows_per_split, s.scale)
+
+
+@pytest.mark.parametrize("n_splits,min_rows", [(1, 1), (8, 1), (16, 64), (3, 0)])
+def test_nkv_edges(n_splits, min_rows):
+    lens = torch.tensor([1, 29, 52, 512, 1641, 0], dtype=torch.int32)
+    q, kc, vc = W.decode_inputs(6, 28, 4, 128, lens, 321)
+    _compare(q, kc, vc, lens, n_splits, min_rows, 1.0 / math.sqrt(128))
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 4), (10, 2), (16, 2), (32, 2)])
+def test_head_ratios_and_dims(d, Hq, Hkv):
+    lens = torch.tensor([33, 700, 95], dtype=torch.int32)
+    q, kc, vc = W.decode_inputs(3, Hq, Hkv, d, lens, 17 + d + Hq, Lmax=720)
+    _compare(q, kc, vc, lens, 4, 16, 1.0 / math.sqrt(d), torch.float32)
+
+
+def test_large_scores():
+    lens = torch.tensor([900, 64], dtype=torch.int32)
+    q, kc, vc = W.decode_inputs(2, 8, 2, 128, lens, 5)
+    q = (q.float() * 4).to(torch.bfloat16)
+    _compare(q, kc, vc, lens, 5, 1, 0.5)
+
+
+def test_ragged_b64_full():
+    s = W.RAGGED_DECODE
+    q, kc, vc, lens = W.decode_inputs_for(s)
+    _compare(q, kc, vc, lens, s.n_splits, s.min_rows_per_split, s.scale)
+
+
+def test_merge_random_partials():
+    rng = np.random.default_rng(2)
+    B, Hq, S, d = 3, 5, 7, 128
+    po = torch.from_numpy(rng.standard_normal((B, Hq, S, d)).astype(np.float32))
+    pl = torch.from_numpy((rng.standard_normal((B, Hq, S)) * 4).astype(np.float32))
+    pl[0, 1, 2:] = -math.inf
+    pl[1, 3, :] = -math.inf          # every split empty: O = 0, LSE = -inf
+    po[pl == -math.inf] = 0.0
+    o, lse = merge(po.cuda(), pl.cuda(), torch.float32)
+    torch.cuda.synchronize()
+    ro, rl = oracle.merge(po, pl)
+    check_o(o.cpu().numpy(), ro, False)
+    check_lse(lse.cpu().numpy(), rl)

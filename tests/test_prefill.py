@@ -1,0 +1,117 @@
+"""Prefill FMHA (tcgen05) against the fp64 oracle, through the C ABI.
+
+Small shapes are compared element by element; the full-size workloads are
+run in the benchmark's launch configuration and compared on sampled rows
+that the oracle computes one by one.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from attn_forward_tcgen05_gb300 import prefill
+from attn_forward_tcgen05_gb300 import workloads as W
+from tests.tolerances import check_lse, check_o
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(q, k, v, causal, scale, out_dtype):
+    o, lse = prefill(q.cuda(), k.cuda(), v.cuda(), causal=causal, scale=scale, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    return o.float().cpu().numpy(), lse.cpu().numpy()
+
+
+def _full_compare(B, Hq, Hkv, Sq, Skv, d, causal, scale, seed, out_dtype=torch.float32, amp=1.0):
+    q, k, v = W.prefill_inputs(B, Hq, Hkv, Sq, Skv, d, seed)
+    if amp != 1.0:
+        q = (q.float() * amp).to(torch.bfloat16)
+        k = (k.float() * amp).to(torch.bfloat16)
+    o, lse = _run(q, k, v, causal, scale, out_dtype)
+    ro, rl = oracle.sdpa(q, k, v, causal, scale)
+    check_o(o, ro, out_dtype == torch.bfloat16)
+    check_lse(lse, rl)
+
+
+def test_tiny_mha_causal_f32():
+    s = W.TINY
+    _full_compare(s.B, s.Hq, s.Hkv, s.Sq, s.Skv, s.d, s.causal, s.scale, s.seed, torch.float32)
+
+
+SHAPES = [
+    # B, Hq, Hkv, Sq, Skv, causal
+    (1, 2, 1, 129, 129, True),    # GQA 2:1, ragged tail (129 = 128 + 1)
+    (1, 2, 2, 1, 1, True),        # single row
+    (1, 2, 2, 127, 127, True),
+    (1, 3, 3, 257, 257, True),    # two query tiles + one row
+    (2, 4, 2, 300, 300, False),
+    (1, 2, 1, 100, 333, True),    # Sq < Skv, bottom-right causal
+    (1, 2, 2, 300, 130, True),    # Sq > Skv: leading rows have no key
+    (1, 1, 1, 64, 1000, False),   # 8 KV tiles: O rescales across tiles
+    (1, 2, 2, 5, 0, True),        # no keys at all
+    (1, 4, 1, 384, 384, True),    # GQA 4:1, three full query tiles
+]
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16], ids=["o_f32", "o_bf16"])
+def test_small_shapes(shape, d, out_dtype):
+    B, Hq, Hkv, Sq, Skv, causal = shape
+    _full_compare(B, Hq, Hkv, Sq, Skv, d, causal, 1.0 / math.sqrt(d), 77 + d + Sq, out_dtype)
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_large_scores_force_rescale(d):
+    # |scores| of several tens: the running max jumps by more than 2^8 between tiles
+    _full_compare(1, 2, 2, 200, 700, d, False, 0.35, 5, torch.float32, amp=3.0)
+    _full_compare(1, 2, 2, 260, 260, d, True, 0.35, 6, torch.float32, amp=3.0)
+
+
+def test_deterministic():
+    q, k, v = W.prefill_inputs(1, 4, 2, 333, 333, 128, 9)
+    a = prefill(q.cuda(), k.cuda(), v.cuda(), causal=True)
+    b = prefill(q.cuda(), k.cuda(), v.cuda(), causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def _sample_rows(B, Hq, Sq, n_random, seed):
+    rng = np.random.default_rng(seed)
+    fixed = [0, 1, 2, 127, 128, 129, 255, 256, Sq // 2, Sq - 129, Sq - 128, Sq - 2, Sq - 1]
+    rows = set()
+    for i in fixed:
+        if 0 <= i < Sq:
+            rows.add((int(rng.integers(B)), int(rng.integers(Hq)), i))
+    while len(rows) < len(fixed) + n_random:
+        rows.add((int(rng.integers(B)), int(rng.integers(Hq)), int(rng.integers(Sq))))
+    return sorted(rows)
+
+
+def _full_size(shape: W.PrefillShape, out_dtype, n_random=40):
+    q, k, v = W.prefill_inputs_for(shape)
+    o, lse = prefill(q.cuda(), k.cuda(), v.cuda(), causal=shape.causal, scale=shape.scale,
+                     out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    rows = _sample_rows(shape.B, shape.Hq, shape.Sq, n_random, shape.seed)
+    ro, rl = oracle.sdpa_rows(q, k, v, shape.causal, shape.scale, rows)
+    idx_b = torch.tensor([r[0] for r in rows])
+    idx_h = torch.tensor([r[1] for r in rows])
+    idx_i = torch.tensor([r[2] for r in rows])
+    go = o.float().cpu()[idx_b, idx_i, idx_h].numpy()
+    gl = lse.cpu()[idx_b, idx_h, idx_i].numpy()
+    check_o(go, ro, out_dtype == torch.bfloat16, f"{shape.name} O")
+    check_lse(gl, rl, f"{shape.name} LSE")
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+
+
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32], ids=["o_bf16", "o_f32"])
+def test_gqa_prefill_3314_sampled(out_dtype):
+    _full_size(W.GQA_PREFILL, out_dtype)
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_mha_noncausal_4096_sampled(d):
+    _full_size(W.mha_sweep(d), torch.bfloat16, n_random=24)
