@@ -10,7 +10,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/attn.h"
+#include "attn.h"
 #include "internal.h"
 #include "ptx.cuh"
 
