@@ -21,6 +21,7 @@ ATTN_ERR_INVALID_ARG = -1
 ATTN_ERR_UNSUPPORTED = -2
 ATTN_ERR_CUDA = -3
 ATTN_ERR_DEVICE_TIMEOUT = -4
+ATTN_ERR_SCRATCH_TOO_SMALL = -5
 ATTN_F32 = 0
 ATTN_BF16 = 1
 
@@ -55,8 +56,11 @@ def load(path: str | None = None):
         lib.attn_strerror.restype = ctypes.c_char_p
         lib.attn_version.argtypes = []
         lib.attn_debug_wait_timeout.argtypes = [ull, vp]
+        lib.attn_decode_noalloc.argtypes = [vp, vp, vp, vp] + [i] * 5 + [f, i, i, vp, vp, i, vp]
+        lib.attn_decode_noalloc_scratch_bytes.argtypes = []
+        lib.attn_decode_noalloc_scratch_bytes.restype = ull
         for name in ("attn_prefill_fwd", "attn_decode_split", "attn_merge", "attn_sync_check",
-                     "attn_version", "attn_debug_wait_timeout"):
+                     "attn_version", "attn_debug_wait_timeout", "attn_decode_noalloc"):
             getattr(lib, name).restype = i
         _lib = lib
         return lib
@@ -76,6 +80,17 @@ def attn_decode_split(q, kcache, vcache, kv_lens, B, Hq, Hkv, d, max_kv, scale, 
 
 def attn_merge(part_o, part_lse, o, lse, B, Hq, n_splits, d, o_dtype, stream) -> int:
     return load().attn_merge(part_o, part_lse, o, lse, B, Hq, n_splits, d, o_dtype, stream)
+
+
+def attn_decode_noalloc(q, kcache, vcache, kv_lens, B, Hq, Hkv, d, max_kv, scale, n_splits,
+                        min_rows_per_split, o, lse, o_dtype, stream) -> int:
+    return load().attn_decode_noalloc(q, kcache, vcache, kv_lens, B, Hq, Hkv, d, max_kv,
+                                      float(scale), n_splits, min_rows_per_split, o, lse, o_dtype,
+                                      stream)
+
+
+def attn_decode_noalloc_scratch_bytes() -> int:
+    return int(load().attn_decode_noalloc_scratch_bytes())
 
 
 def attn_sync_check(stream) -> int:

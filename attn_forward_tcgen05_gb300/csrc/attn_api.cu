@@ -92,6 +92,7 @@ const char* attn_strerror(int status) {
     case ATTN_ERR_UNSUPPORTED: return "unsupported configuration (head dim or dtype code)";
     case ATTN_ERR_CUDA: return "CUDA runtime or launch error";
     case ATTN_ERR_DEVICE_TIMEOUT: return "a kernel's bounded pipeline wait timed out";
+    case ATTN_ERR_SCRATCH_TOO_SMALL: return "problem too large for the library's static decode scratch (24 MiB)";
     default: return "unknown status";
   }
 }

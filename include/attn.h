@@ -48,6 +48,7 @@ typedef struct CUstream_st* attn_stream_t; /* == cudaStream_t */
 #define ATTN_ERR_UNSUPPORTED (-2)    /* head_dim not in {64, 128, 256}, unknown dtype code */
 #define ATTN_ERR_CUDA (-3)           /* a CUDA runtime/driver call or a launch failed */
 #define ATTN_ERR_DEVICE_TIMEOUT (-4) /* a kernel's bounded wait ran out (attn_sync_check only) */
+#define ATTN_ERR_SCRATCH_TOO_SMALL (-5) /* attn_decode_noalloc: problem exceeds the static scratch */
 
 /* output dtype codes */
 #define ATTN_F32 0
@@ -112,7 +113,8 @@ int attn_prefill_fwd(const attn_bf16_t* q, const attn_bf16_t* k, const attn_bf16
  *   vcache    bf16 [B][max_kv][Hkv][d]    values
  *   kv_lens   int32 [B] (device)          L_b, 0 <= L_b <= max_kv (values are trusted
  *                                         to be in range; they are clamped on the device)
- *   B, Hq, Hkv, d, max_kv                 B >= 0, Hq % Hkv == 0, Hq/Hkv <= 16, d == 128, max_kv >= 1
+ *   B, Hq, Hkv, d, max_kv                 B >= 0, Hq % Hkv == 0, Hq/Hkv <= 16, d in {64,128,256},
+ *                                         max_kv >= 1
  *   scale                                 softmax scale (finite, > 0)
  *   n_splits                              >= 1 and <= 1024
  *   min_rows_per_split                    >= 0
@@ -142,6 +144,43 @@ int attn_decode_split(const attn_bf16_t* q, const attn_bf16_t* kcache, const att
  */
 int attn_merge(const float* part_o, const float* part_lse, void* o, float* lse, int B, int Hq,
                int n_splits, int d, int o_dtype, attn_stream_t stream);
+
+/*
+ * attn_decode_noalloc -- attn_decode_split followed by attn_merge, for callers
+ * that cannot allocate device memory.  (The pages have no counterpart: this
+ * entry point exists for callers, not for the method.)
+ *
+ * The split partials that attn_decode_split writes to a caller-provided buffer
+ * live here in a fixed array of device memory owned by the library, so the
+ * caller passes only inputs and outputs.  It is meant for callers that cannot
+ * call cudaMalloc: code under a memory pool that has already reserved the
+ * device's memory, code that must not call cudaMalloc/cudaFree because both
+ * may synchronise the whole device, and plain C callers without a device
+ * allocator.  Nothing is allocated per call, and no allocating library
+ * routine is called.
+ *
+ *  - Limit: B * Hq * n_splits * (d + 1) * 4 bytes (each part rounded up to 256
+ *    bytes) must fit in attn_decode_noalloc_scratch_bytes() = 24 MiB; larger
+ *    problems return ATTN_ERR_SCRATCH_TOO_SMALL before any launch.
+ *  - The array is reserved on every GPU that loads the library and stays
+ *    reserved until the process exits.
+ *  - The first call on a device looks up the array's device address (with that
+ *    device current) and caches it; make that first call before any stream
+ *    capture.
+ *  - All calls on a device share the array; each call writes every entry it
+ *    later reads, so nothing needs to start at zero, but calls whose work
+ *    overlaps on the GPU (e.g. on two streams) race on it.
+ * Arguments, layouts and the split rule are those of attn_decode_split, with
+ * the outputs of attn_merge: o [B][Hq][d] (fp32 or bf16 per o_dtype), lse fp32
+ * [B][Hq].
+ */
+int attn_decode_noalloc(const attn_bf16_t* q, const attn_bf16_t* kcache, const attn_bf16_t* vcache,
+                        const int* kv_lens, int B, int Hq, int Hkv, int d, int max_kv, float scale,
+                        int n_splits, int min_rows_per_split, void* o, float* lse, int o_dtype,
+                        attn_stream_t stream);
+
+/* Size in bytes of the static scratch array attn_decode_noalloc uses (24 MiB). */
+unsigned long long attn_decode_noalloc_scratch_bytes(void);
 
 /*
  * attn_sync_check -- synchronise `stream`, then read and clear this device's

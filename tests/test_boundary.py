@@ -21,7 +21,7 @@ def lib():
 
 def declared_symbols():
     text = open(HEADER).read()
-    return sorted(set(re.findall(r"^\s*(?:int|const char\*)\s+(attn_\w+)\s*\(", text, re.M)))
+    return sorted(set(re.findall(r"^\s*(?:int|const char\*|unsigned long long)\s+(attn_\w+)\s*\(", text, re.M)))
 
 
 def test_exports_every_declared_symbol(lib):
