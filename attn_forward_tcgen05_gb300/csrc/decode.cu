@@ -11,17 +11,19 @@
 // (32 rows of K and of V per stage) into a shared-memory ring, so the loads of
 // later tiles are in flight while the consumer warps work on earlier ones.
 //
-// Work mapping (per CTA = one (batch, KV head, split)):
-//   * warp 4 (producer): TMA loads of K and V tiles into the ring;
-//   * warps 0..3 (consumers): warp w owns tiles w, w+4, w+8, ... of the split.
-//     Scores: lane = row of the tile, the whole head dim of that row from
-//     shared memory against every query head of the group (q kept in shared
-//     memory in fp32, pre-multiplied by scale * log2(e)).  Softmax: warp
-//     max by shuffles, exp2 on the MUFU.  P.V: lane = d/32 consecutive dims,
-//     one V row per step, p broadcast from shared memory.
-//   * at the end the four warps' partial (m, l, O) are merged through shared
-//     memory and the split's normalised O and its LSE are written.
-// Everything is fp32 on CUDA cores; no tensor cores.
+// Work mapping: one CTA per split unit (batch, KV head, split), 6 warps.
+// Consumer warps 0..3 each own one ring stage (32 rows of K and 32 of V) and
+// take tiles w, w+4, w+8, ... of the unit for all G query heads of the group,
+// so every loaded K/V row serves all G heads.  Warp 4 streams K tiles and
+// warp 5 streams V tiles with TMA; a consumer hands its K half back right
+// after the score phase, so its next K tile loads during softmax and P.V.
+// Per tile: scores with lane = row (the head dim of that row from shared
+// memory against q, kept in shared memory in fp32, pre-multiplied by
+// scale * log2(e)), warp-shuffle max, exp2 on the MUFU, then P.V with
+// lane = d/32 dims and p broadcast from shared memory.  Both products run on
+// packed fp32 pairs (fma.f32x2).  At the end the four warps' partial
+// (m, l, O) are merged through shared memory and the split's normalised O
+// and LSE are written.  Everything is fp32 on CUDA cores; no tensor cores.
 #include <cmath>
 
 #include "internal.h"
@@ -30,30 +32,38 @@
 namespace attn {
 namespace {
 
-constexpr int kNumConsumerWarps = 4;
-constexpr int kDecodeThreads = (kNumConsumerWarps + 1) * 32;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+
+constexpr int kConsumerWarps = 4;                   // one ring stage each
+constexpr int kDecodeThreads = (kConsumerWarps + 2) * 32;  // + K producer + V producer
 
 template <int D, int GMAX>
 struct DecodeCfg {
   static constexpr int kTile = kDecodeTileRows;        // rows per stage
   static constexpr int kPanels = D / 64;               // 128-byte swizzled panels per row
   static constexpr int kPanelBytes = kTile * 128;      // one panel of one tile
-  static constexpr int kKBytes = kPanels * kPanelBytes;
-  static constexpr int kStageBytes = 2 * kKBytes;      // K then V
-  static constexpr int kStages = kNumConsumerWarps;    // one stage per consumer warp
-  static constexpr int kRingBytes = kStages * kStageBytes;
+  static constexpr int kKBytes = kPanels * kPanelBytes;  // the K half of a stage (V half: same)
+  static constexpr int kStageBytes = 2 * kKBytes;
+  static constexpr int kRingBytes = kConsumerWarps * kStageBytes;
   static constexpr int kQBytes = GMAX * D * 4;                             // fp32 q
-  static constexpr int kPBytes = kNumConsumerWarps * kTile * GMAX * 4;     // p per warp [row][g]
-  static constexpr int kCombBytes = kNumConsumerWarps * GMAX * (D + 2) * 4;
-  static_assert(kCombBytes <= kRingBytes, "combine area must fit in the ring");
+  static constexpr int kPBytes = kConsumerWarps * kTile * GMAX * 4;        // p [warp][row][g]
   static constexpr int kBarOffset = kRingBytes + kQBytes + kPBytes;
-  static constexpr int kSmemBytes = kBarOffset + 2 * kStages * 8 + 16 + 1024;  // + align slack
+  static constexpr int kBarBytes = 4 * kConsumerWarps * 8 + 16;  // fullK, fullV, emptyK, emptyV, abort
+  static constexpr int kSmemBytes = kBarOffset + kBarBytes + 1024;  // + align slack
+  // three CTAs per SM for small head groups, two otherwise (register budget)
+  static constexpr int kMinBlocks = GMAX <= 4 ? 3 : 2;
 };
 
 __device__ __forceinline__ float bf16lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
+// two bf16 (low, high half of x) as an fp32 pair
+__device__ __forceinline__ uint64_t bf16x2_to_f2(uint32_t x) { return f2pack(bf16lo(x), bf16hi(x)); }
+__device__ __forceinline__ float f2sum(uint64_t a) {
+  float lo, hi;
+  f2unpack(a, lo, hi);
+  return lo + hi;
+}
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -68,18 +78,25 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 __device__ __forceinline__ void consumer_bar_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kNumConsumerWarps * 32) : "memory");
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
 }
 
+// One CTA per split unit (batch b, KV head hk, split s).  Consumer warp w owns
+// ring stage w and takes tiles w, w+4, w+8, ... of the unit, for all G query
+// heads of the group.  A stage has a K half and a V half with their own
+// barriers: the warp hands the K half back as soon as its scores are done, so
+// the K producer warp refills it with the warp's next K tile while the warp is
+// still in softmax and P.V; the V producer warp refills the V half after P.V.
 template <int D, int GMAX>
-__global__ void __launch_bounds__(kDecodeThreads)
+__global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<D, GMAX>::kMinBlocks)
     decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const uint16_t* __restrict__ q,
                         const int* __restrict__ kv_lens, float* __restrict__ part_o,
                         float* __restrict__ part_lse, int Hq, int Hkv, int max_kv, int n_splits,
                         int min_rows, float scale, uint32_t* err) {
   using C = DecodeCfg<D, GMAX>;
-  constexpr int DPL = D / 32;  // output dims per lane in the P.V phase
+  constexpr int DPL = D / 32;   // output dims per lane in the P.V phase
+  constexpr int DP2 = DPL / 2;  // ... as fp32 pairs
   const int s_idx = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
   const int G = Hq / Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -90,15 +107,15 @@ __global__ void __launch_bounds__(kDecodeThreads)
   long long chunk = ((long long)L + n_splits - 1) / n_splits;
   if (chunk < min_rows) chunk = min_rows;
   if (chunk < 1) chunk = 1;
-  long long lo_ll = (long long)s_idx * chunk, hi_ll = lo_ll + chunk;
+  const long long lo_ll = (long long)s_idx * chunk, hi_ll = lo_ll + chunk;
   const int lo = (int)(lo_ll < L ? lo_ll : L), hi = (int)(hi_ll < L ? hi_ll : L);
+  const size_t row_base = ((size_t)b * Hq + (size_t)hk * G) * n_splits + s_idx;  // head g: + g*n_splits
 
   if (lo >= hi) {  // empty split: o = 0, lse = -inf; nothing is read
     for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
       const int g = i / D, t = i % D;
-      const size_t row = ((size_t)b * Hq + (size_t)hk * G + g) * n_splits + s_idx;
-      part_o[row * D + t] = 0.f;
-      if (t == 0) part_lse[row] = -INFINITY;
+      part_o[(row_base + (size_t)g * n_splits) * D + t] = 0.f;
+      if (t == 0) part_lse[row_base + (size_t)g * n_splits] = -INFINITY;
     }
     return;
   }
@@ -106,19 +123,23 @@ __global__ void __launch_bounds__(kDecodeThreads)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* ring = smem;
-  float* qs = reinterpret_cast<float*>(smem + C::kRingBytes);                   // [GMAX][D]
-  float* pbuf = reinterpret_cast<float*>(smem + C::kRingBytes + C::kQBytes);    // [warp][row][GMAX]
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
-  uint64_t* empty = full + C::kStages;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + C::kStages);
+  uint8_t* ring = smem;                                                          // [warp] K|V
+  float* qs = reinterpret_cast<float*>(smem + C::kRingBytes);                    // [GMAX][D]
+  float* pbuf = reinterpret_cast<float*>(smem + C::kRingBytes + C::kQBytes);     // [warp][row][GMAX]
+  uint64_t* fullK = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
+  uint64_t* fullV = fullK + kConsumerWarps;
+  uint64_t* emptyK = fullV + kConsumerWarps;
+  uint64_t* emptyV = emptyK + kConsumerWarps;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(emptyV + kConsumerWarps);
 
   const int T = (hi - lo + C::kTile - 1) / C::kTile;  // tiles in this split
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      mbar_init(&fullK[w], 1);
+      mbar_init(&fullV[w], 1);
+      mbar_init(&emptyK[w], 1);
+      mbar_init(&emptyV[w], 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -133,135 +154,134 @@ __global__ void __launch_bounds__(kDecodeThreads)
   for (int i = threadIdx.x; i < (GMAX - G) * D; i += blockDim.x) qs[G * D + i] = 0.f;
   __syncthreads();
 
-  if (warp == kNumConsumerWarps) {
-    // ================= producer warp =================
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      const uint64_t pol = l2_policy_evict_first();
-      int t = 0;
-      for (; t < T; ++t) {
-        const int s = t % C::kStages, k = t / C::kStages;
-        if (!mbar_wait(&empty[s], (k & 1) ^ 1, err, abort_flag)) break;
-        mbar_arrive_expect_tx(&full[s], C::kStageBytes);
-        uint8_t* kdst = ring + s * C::kStageBytes;
-        uint8_t* vdst = kdst + C::kKBytes;
-        const int row = lo + t * C::kTile;
+  if (warp >= kConsumerWarps) {
+    // ================= producer warps: warp 4 streams K, warp 5 streams V =================
+    // Tile t goes to consumer warp t % 4 (its (t / 4)-th use of its stage).  The
+    // whole warp runs the loop; one elected lane issues each copy.
+    const bool is_k = warp == kConsumerWarps;
+    const CUtensorMap* map = is_k ? &tm_k : &tm_v;
+    uint64_t* fullX = is_k ? fullK : fullV;
+    uint64_t* emptyX = is_k ? emptyK : emptyV;
+    if (lane == 0) tma_prefetch_desc(map);
+    const uint64_t pol = l2_policy_evict_first();
+    int t = 0;
+    for (; t < T; ++t) {
+      const int w = t % kConsumerWarps, k = t / kConsumerWarps;
+      if (!mbar_wait_warp(&emptyX[w], (k & 1) ^ 1, err, abort_flag)) break;
+      mbar_arrive_expect_tx_e(&fullX[w], C::kKBytes);
+      uint8_t* dst = ring + w * C::kStageBytes + (is_k ? 0 : C::kKBytes);
+      const int row = lo + t * C::kTile;
 #pragma unroll
-        for (int p = 0; p < C::kPanels; ++p) {
-          tma_load_4d_hint(kdst + p * C::kPanelBytes, &tm_k, &full[s], p * 64, hk, row, b, pol);
-          tma_load_4d_hint(vdst + p * C::kPanelBytes, &tm_v, &full[s], p * 64, hk, row, b, pol);
-        }
-      }
-      if (t < T) {
-        // aborted: let the copies already issued land before the CTA exits
-        for (int u = (t - C::kStages > 0 ? t - C::kStages : 0); u < t; ++u)
-          mbar_wait(&full[u % C::kStages], (u / C::kStages) & 1, nullptr, nullptr, 100000000ull);
-      }
+      for (int p = 0; p < C::kPanels; ++p)
+        tma_load_4d_hint_e(dst + p * C::kPanelBytes, map, &fullX[w], p * 64, hk, row, b, pol);
     }
-    return;  // the producer takes no part in the combine
+    if (t < T && lane == 0) {
+      // aborted: let the copies already issued land before the CTA exits
+      for (int u = (t - kConsumerWarps > 0 ? t - kConsumerWarps : 0); u < t; ++u)
+        mbar_wait(&fullX[u % kConsumerWarps], (u / kConsumerWarps) & 1, nullptr, nullptr,
+                  100000000ull);
+    }
+    return;  // the producers take no part in the combine
   }
 
   // ================= consumer warps =================
-  float m[GMAX], lsum[GMAX], o[GMAX][DPL];
+  float m[GMAX], lsum[GMAX];
+  uint64_t o2[GMAX][DP2];  // O as fp32 pairs: dims lane*DPL + 2e, +1
 #pragma unroll
   for (int g = 0; g < GMAX; ++g) {
     m[g] = -INFINITY;
     lsum[g] = 0.f;
 #pragma unroll
-    for (int e = 0; e < DPL; ++e) o[g][e] = 0.f;
+    for (int e = 0; e < DP2; ++e) o2[g][e] = f2pack(0.f, 0.f);
   }
   float* pw = pbuf + warp * C::kTile * GMAX;
+  const uint8_t* kt = ring + warp * C::kStageBytes;  // this warp's stage
+  const uint8_t* vt = kt + C::kKBytes;
 
   bool ok = true;
-  for (int t = warp; t < T; t += kNumConsumerWarps) {
-    const int s = t % C::kStages, k = t / C::kStages;
-    if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[s], k & 1, err, abort_flag))) {
+  for (int i = 0, t = warp; t < T; ++i, t += kConsumerWarps) {
+    const uint32_t par = (uint32_t)i & 1u;
+    const int row0 = lo + t * C::kTile;
+    const int nrows = min(C::kTile, hi - row0);
+    if (!__all_sync(0xFFFFFFFFu, mbar_wait(&fullK[warp], par, err, abort_flag))) {
       ok = false;
       break;
     }
-    const uint8_t* kt = ring + s * C::kStageBytes;
-    const uint8_t* vt = kt + C::kKBytes;
-    const int row0 = lo + t * C::kTile;
-    const int nrows = min(C::kTile, hi - row0);
 
-    // ---- scores: lane = row ----
-    float acc[GMAX];
+    // ---- scores: lane = row; fp32 pairs along the head dim ----
+    uint64_t acc[GMAX];
 #pragma unroll
-    for (int g = 0; g < GMAX; ++g) acc[g] = 0.f;
+    for (int g = 0; g < GMAX; ++g) acc[g] = f2pack(0.f, 0.f);
 #pragma unroll
     for (int c = 0; c < D / 8; ++c) {
       const int p = c >> 3, cc = c & 7;
       const uint4 kv = *reinterpret_cast<const uint4*>(kt + p * C::kPanelBytes + lane * 128 +
                                                        ((cc ^ (lane & 7)) << 4));
-      const float k0 = bf16lo(kv.x), k1 = bf16hi(kv.x), k2 = bf16lo(kv.y), k3 = bf16hi(kv.y);
-      const float k4 = bf16lo(kv.z), k5 = bf16hi(kv.z), k6 = bf16lo(kv.w), k7 = bf16hi(kv.w);
+      const uint64_t k01 = bf16x2_to_f2(kv.x), k23 = bf16x2_to_f2(kv.y);
+      const uint64_t k45 = bf16x2_to_f2(kv.z), k67 = bf16x2_to_f2(kv.w);
 #pragma unroll
       for (int g = 0; g < GMAX; ++g) {
         if (g < G) {
-          const float4 qa = *reinterpret_cast<const float4*>(qs + g * D + c * 8);
-          const float4 qb = *reinterpret_cast<const float4*>(qs + g * D + c * 8 + 4);
-          float a = acc[g];
-          a = fmaf(qa.x, k0, a);
-          a = fmaf(qa.y, k1, a);
-          a = fmaf(qa.z, k2, a);
-          a = fmaf(qa.w, k3, a);
-          a = fmaf(qb.x, k4, a);
-          a = fmaf(qb.y, k5, a);
-          a = fmaf(qb.z, k6, a);
-          a = fmaf(qb.w, k7, a);
+          const ulonglong2 qa = *reinterpret_cast<const ulonglong2*>(qs + g * D + c * 8);
+          const ulonglong2 qb = *reinterpret_cast<const ulonglong2*>(qs + g * D + c * 8 + 4);
+          uint64_t a = acc[g];
+          a = fma2(qa.x, k01, a);
+          a = fma2(qa.y, k23, a);
+          a = fma2(qb.x, k45, a);
+          a = fma2(qb.y, k67, a);
           acc[g] = a;
         }
       }
     }
+    // the K half of the stage is no longer needed: the K producer may refill it
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&emptyK[warp]);
     const bool valid = lane < nrows;
 
     // ---- online softmax per query head (log2 domain) ----
 #pragma unroll
     for (int g = 0; g < GMAX; ++g) {
       if (g < G) {
-        const float sv = valid ? acc[g] : -INFINITY;
+        const float sv = valid ? f2sum(acc[g]) : -INFINITY;
         const float tmax = warp_max(sv);  // finite: every tile has >= 1 valid row
         const float m_new = fmaxf(m[g], tmax);
         const float corr = ex2_approx(m[g] - m_new);  // m = -inf -> 0
         const float pv = ex2_approx(sv - m_new);      // invalid -> 0
         lsum[g] = fmaf(lsum[g], corr, pv);           // per-lane partial sum
         m[g] = m_new;
+        const uint64_t c2 = f2pack(corr, corr);
 #pragma unroll
-        for (int e = 0; e < DPL; ++e) o[g][e] *= corr;
+        for (int e = 0; e < DP2; ++e) o2[g][e] = mul2(o2[g][e], c2);
         pw[lane * GMAX + g] = pv;
       }
     }
     __syncwarp();
+    if (!__all_sync(0xFFFFFFFFu, mbar_wait(&fullV[warp], par, err, abort_flag))) {
+      ok = false;
+      break;
+    }
 
     // ---- O += P V: lane = DPL consecutive dims ----
 #pragma unroll 2
     for (int r = 0; r < nrows; ++r) {
-      float vf[DPL];
+      uint64_t vf[DP2];
       if constexpr (D == 64) {
         const uint32_t x = *reinterpret_cast<const uint32_t*>(
             vt + r * 128 + (((lane >> 2) ^ (r & 7)) << 4) + (lane & 3) * 4);
-        vf[0] = bf16lo(x);
-        vf[1] = bf16hi(x);
+        vf[0] = bf16x2_to_f2(x);
       } else if constexpr (D == 128) {
         const uint2 x = *reinterpret_cast<const uint2*>(
             vt + (lane >> 4) * C::kPanelBytes + r * 128 + ((((lane & 15) >> 1) ^ (r & 7)) << 4) +
             (lane & 1) * 8);
-        vf[0] = bf16lo(x.x);
-        vf[1] = bf16hi(x.x);
-        vf[2] = bf16lo(x.y);
-        vf[3] = bf16hi(x.y);
+        vf[0] = bf16x2_to_f2(x.x);
+        vf[1] = bf16x2_to_f2(x.y);
       } else {
         const uint4 x = *reinterpret_cast<const uint4*>(vt + (lane >> 3) * C::kPanelBytes + r * 128 +
                                                         (((lane & 7) ^ (r & 7)) << 4));
-        vf[0] = bf16lo(x.x);
-        vf[1] = bf16hi(x.x);
-        vf[2] = bf16lo(x.y);
-        vf[3] = bf16hi(x.y);
-        vf[4] = bf16lo(x.z);
-        vf[5] = bf16hi(x.z);
-        vf[6] = bf16lo(x.w);
-        vf[7] = bf16hi(x.w);
+        vf[0] = bf16x2_to_f2(x.x);
+        vf[1] = bf16x2_to_f2(x.y);
+        vf[2] = bf16x2_to_f2(x.z);
+        vf[3] = bf16x2_to_f2(x.w);
       }
       const float* pr = pw + r * GMAX;
 #pragma unroll
@@ -271,26 +291,28 @@ __global__ void __launch_bounds__(kDecodeThreads)
           const float pp[4] = {p4.x, p4.y, p4.z, p4.w};
 #pragma unroll
           for (int gg = 0; gg < 4; ++gg) {
+            const uint64_t p2 = f2pack(pp[gg], pp[gg]);
 #pragma unroll
-            for (int e = 0; e < DPL; ++e) o[g4 + gg][e] = fmaf(pp[gg], vf[e], o[g4 + gg][e]);
+            for (int e = 0; e < DP2; ++e) o2[g4 + gg][e] = fma2(p2, vf[e], o2[g4 + gg][e]);
           }
         }
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
+    if (lane == 0) mbar_arrive(&emptyV[warp]);
   }
 
   // ---- combine the consumer warps' partials through shared memory ----
-  consumer_bar_sync();  // every consumer is done with the ring
+  consumer_bar_sync();  // every consumer is done with its stage
   float* comb = reinterpret_cast<float*>(ring);  // [warp][g][D + 2]: o[0..D), m, l
+  static_assert(kConsumerWarps * GMAX * (D + 2) * 4 <= C::kRingBytes, "combine area");
 #pragma unroll
   for (int g = 0; g < GMAX; ++g) {
     if (g < G) {
       const float lw = warp_sum(lsum[g]);
       float* cw = comb + (warp * GMAX + g) * (D + 2);
 #pragma unroll
-      for (int e = 0; e < DPL; ++e) cw[lane * DPL + e] = o[g][e];
+      for (int e = 0; e < DP2; ++e) f2unpack(o2[g][e], cw[lane * DPL + 2 * e], cw[lane * DPL + 2 * e + 1]);
       if (lane == 0) {
         cw[D] = m[g];
         cw[D + 1] = lw;
@@ -299,20 +321,20 @@ __global__ void __launch_bounds__(kDecodeThreads)
   }
   consumer_bar_sync();
   if (!ok || *abort_flag) return;
-  for (int i = threadIdx.x; i < G * D; i += kNumConsumerWarps * 32) {
-    const int g = i / D, t = i % D;
+  for (int idx = threadIdx.x; idx < G * D; idx += kConsumerWarps * 32) {
+    const int g = idx / D, t = idx % D;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kNumConsumerWarps; ++w) M = fmaxf(M, comb[(w * GMAX + g) * (D + 2) + D]);
+    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, comb[(w * GMAX + g) * (D + 2) + D]);
     float Lsum = 0.f, acc = 0.f;
 #pragma unroll
-    for (int w = 0; w < kNumConsumerWarps; ++w) {
+    for (int w = 0; w < kConsumerWarps; ++w) {
       const float* cw = comb + (w * GMAX + g) * (D + 2);
       const float f = ex2_approx(cw[D] - M);  // warps without tiles: m = -inf -> 0
       Lsum = fmaf(cw[D + 1], f, Lsum);
       acc = fmaf(cw[t], f, acc);
     }
-    const size_t row = ((size_t)b * Hq + (size_t)hk * G + g) * n_splits + s_idx;
+    const size_t row = row_base + (size_t)g * n_splits;
     part_o[row * D + t] = acc / Lsum;
     if (t == 0) part_lse[row] = (M + log2f(Lsum)) * kLn2;
   }
@@ -327,7 +349,7 @@ __global__ void __launch_bounds__(128)
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
   const float* pl = part_lse + (size_t)row * n_splits;
-  const float* po = part_o + (size_t)row * n_splits * D;
+  const float* po = part_o + (size_t)row * n_splits * D + lane * DPL;
   float M = -INFINITY;
   for (int s = lane; s < n_splits; s += 32) M = fmaxf(M, pl[s]);
   M = warp_max(M);
@@ -336,19 +358,46 @@ __global__ void __launch_bounds__(128)
   for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
   float wsum = 0.f;
   if (M != -INFINITY) {
-    for (int s = 0; s < n_splits; ++s) {
-      const float ls = pl[s];
-      if (ls == -INFINITY) continue;  // empty split: its part_o is not read
-      const float w = ex2_approx((ls - M) * kLog2e);
+    for (int s0 = 0; s0 < n_splits; s0 += 32) {
+      // lane j holds the weight of split s0 + j (0 for empty or missing splits)
+      const int s = s0 + lane;
+      const float ls = s < n_splits ? pl[s] : -INFINITY;
+      const float w = ls == -INFINITY ? 0.f : ex2_approx((ls - M) * kLog2e);
       wsum += w;
-      const float* src = po + (size_t)s * D + lane * DPL;
+      uint32_t live = __ballot_sync(0xFFFFFFFFu, w > 0.f);  // empty splits are never read
+      while (live) {
+        // up to four non-empty splits per round: their loads are issued together
+        int idx[4];
+        float wk[4];
 #pragma unroll
-      for (int e = 0; e < DPL; e += 2) {
-        const float2 x = *reinterpret_cast<const float2*>(src + e);
-        acc[e] = fmaf(w, x.x, acc[e]);
-        acc[e + 1] = fmaf(w, x.y, acc[e + 1]);
+        for (int u = 0; u < 4; ++u) {
+          idx[u] = live ? __ffs(live) - 1 : -1;
+          if (live) live &= live - 1;
+          wk[u] = __shfl_sync(0xFFFFFFFFu, w, idx[u] < 0 ? 0 : idx[u]);
+        }
+        float x[4][DPL];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (idx[u] >= 0) {
+            const float* src = po + (size_t)(s0 + idx[u]) * D;
+#pragma unroll
+            for (int e = 0; e < DPL; e += 2) {
+              const float2 v2 = *reinterpret_cast<const float2*>(src + e);
+              x[u][e] = v2.x;
+              x[u][e + 1] = v2.y;
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (idx[u] >= 0) {
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) acc[e] = fmaf(wk[u], x[u][e], acc[e]);
+          }
+        }
       }
     }
+    wsum = warp_sum(wsum);
   }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
   if (o_bf16) {

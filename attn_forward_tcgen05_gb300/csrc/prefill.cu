@@ -50,13 +50,22 @@ struct PrefillCfg {
   static constexpr int kPanels = D / 64;                   // 128-byte panels per row
   static constexpr int kPanelBytes = 128 * 128;            // 128 rows x 128 bytes
   static constexpr int kTileBytes = kPanels * kPanelBytes; // one 128 x d bf16 tile
-  static constexpr int kStages = (D == 64) ? 4 : (D == 128 ? 2 : 1);  // K and V ring depth
+#ifndef ATTN_PREFILL_KSTAGES
+  static constexpr int kStagesK = (D == 64) ? 4 : (D == 128 ? 2 : 1);  // K ring depth
+#else
+  static constexpr int kStagesK = ATTN_PREFILL_KSTAGES;
+#endif
+#ifndef ATTN_PREFILL_VSTAGES
+  static constexpr int kStagesV = (D == 64) ? 4 : (D == 128 ? 2 : 1);  // V ring depth
+#else
+  static constexpr int kStagesV = ATTN_PREFILL_VSTAGES;
+#endif
   static constexpr int kQOff = 0;
   static constexpr int kKOff = NQ * kTileBytes;
-  static constexpr int kVOff = kKOff + kStages * kTileBytes;
-  static constexpr int kBarOff = kVOff + kStages * kTileBytes;
-  // barriers: fullQ, fullK[S], emptyK[S], fullV[S], emptyV[S], S[NQ][NS], P[NQ], O[NQ], Fin[NQ]
-  static constexpr int kNumBars = 1 + 4 * kStages + NQ * NS + 3 * NQ;
+  static constexpr int kVOff = kKOff + kStagesK * kTileBytes;
+  static constexpr int kBarOff = kVOff + kStagesV * kTileBytes;
+  // barriers: fullQ, fullK[SK], emptyK[SK], fullV[SV], emptyV[SV], S[NQ][NS], P[NQ], O[NQ], Fin[NQ]
+  static constexpr int kNumBars = 1 + 2 * kStagesK + 2 * kStagesV + NQ * NS + 3 * NQ;
   static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;
   // NQ softmax warpgroups + one control warpgroup (MMA warp, TMA warp, two spare warps).
   static constexpr int kThreads = (4 * NQ + 4) * 32;
@@ -139,10 +148,10 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
   uint64_t* bar_q = bars;
   uint64_t* bar_fullK = bars + 1;
-  uint64_t* bar_emptyK = bar_fullK + C::kStages;
-  uint64_t* bar_fullV = bar_emptyK + C::kStages;
-  uint64_t* bar_emptyV = bar_fullV + C::kStages;
-  uint64_t* bar_S = bar_emptyV + C::kStages;  // [NQ][NS]
+  uint64_t* bar_emptyK = bar_fullK + C::kStagesK;
+  uint64_t* bar_fullV = bar_emptyK + C::kStagesK;
+  uint64_t* bar_emptyV = bar_fullV + C::kStagesV;
+  uint64_t* bar_S = bar_emptyV + C::kStagesV;  // [NQ][NS]
   uint64_t* bar_P = bar_S + NQ * NS;          // [NQ]
   uint64_t* bar_O = bar_P + NQ;               // [NQ] one phase per P.V MMA group
   uint64_t* bar_Fin = bar_O + NQ;             // [NQ] last P.V done
@@ -158,9 +167,11 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
-    for (int s = 0; s < C::kStages; ++s) {
+    for (int s = 0; s < C::kStagesK; ++s) {
       mbar_init(&bar_fullK[s], 1);
       mbar_init(&bar_emptyK[s], 1);
+    }
+    for (int s = 0; s < C::kStagesV; ++s) {
       mbar_init(&bar_fullV[s], 1);
       mbar_init(&bar_emptyV[s], 1);
     }
@@ -187,111 +198,129 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
     if constexpr (NQ == 2) setmaxnreg_dec<C::kCtlRegs>();  // whole warpgroup, same instruction
   if (warp == C::kTmaWarp) {
     // =========================== TMA producer ===========================
-    if (lane == 0 && n_kv > 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
+    // The whole warp runs the loop; one elected lane issues each copy.
+    if (n_kv > 0) {
+      if (lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+      }
       uint32_t qbytes = 0;
 #pragma unroll
       for (int t = 0; t < NQ; ++t)
         if (ti[t].n_kv > 0) qbytes += C::kTileBytes;
-      mbar_arrive_expect_tx(bar_q, qbytes);
+      mbar_arrive_expect_tx_e(bar_q, qbytes);
 #pragma unroll
       for (int t = 0; t < NQ; ++t) {
         if (ti[t].n_kv > 0) {
 #pragma unroll
           for (int p = 0; p < C::kPanels; ++p)
-            tma_load_4d(sQ + t * C::kTileBytes + p * C::kPanelBytes, &tm_q, bar_q, p * 64, hq,
-                        ti[t].q0, b);
+            tma_load_4d_e(sQ + t * C::kTileBytes + p * C::kPanelBytes, &tm_q, bar_q, p * 64, hq,
+                          ti[t].q0, b);
         }
       }
-      int j = 0;
-      for (; j < n_kv; ++j) {
-        const int s = j % C::kStages;
-        const uint32_t ph = (uint32_t)(j / C::kStages) & 1u;
-        if (!mbar_wait(&bar_emptyK[s], ph ^ 1u, err, abort_flag)) break;
-        mbar_arrive_expect_tx(&bar_fullK[s], C::kTileBytes);
+      // K(j) and V(j) alternate; each ring has its own depth
+      int jk = 0, jv = 0;
+      bool aborted = false;
+      while (jv < n_kv) {
+        if (jk < n_kv && jk <= jv) {
+          const int s = jk % C::kStagesK;
+          const uint32_t ph = (uint32_t)(jk / C::kStagesK) & 1u;
+          if (!mbar_wait_warp(&bar_emptyK[s], ph ^ 1u, err, abort_flag)) { aborted = true; break; }
+          mbar_arrive_expect_tx_e(&bar_fullK[s], C::kTileBytes);
 #pragma unroll
-        for (int p = 0; p < C::kPanels; ++p)
-          tma_load_4d(sK + s * C::kTileBytes + p * C::kPanelBytes, &tm_k, &bar_fullK[s], p * 64, hk,
-                      j * kPrefillTileN, b);
-        if (!mbar_wait(&bar_emptyV[s], ph ^ 1u, err, abort_flag)) break;
-        mbar_arrive_expect_tx(&bar_fullV[s], C::kTileBytes);
-#pragma unroll
-        for (int p = 0; p < C::kPanels; ++p)
-          tma_load_4d(sV + s * C::kTileBytes + p * C::kPanelBytes, &tm_v, &bar_fullV[s], p * 64, hk,
-                      j * kPrefillTileN, b);
-      }
-      if (j < n_kv) {
-        // aborted: let the copies already issued land before shared memory is released
-        for (int u2 = max(0, j - C::kStages); u2 <= j && u2 < n_kv; ++u2) {
-          const int s = u2 % C::kStages;
-          const uint32_t ph = (uint32_t)(u2 / C::kStages) & 1u;
-          mbar_wait(&bar_fullK[s], ph, nullptr, nullptr, 100000000ull);
-          mbar_wait(&bar_fullV[s], ph, nullptr, nullptr, 100000000ull);
+          for (int p = 0; p < C::kPanels; ++p)
+            tma_load_4d_e(sK + s * C::kTileBytes + p * C::kPanelBytes, &tm_k, &bar_fullK[s], p * 64,
+                          hk, jk * kPrefillTileN, b);
+          ++jk;
+          continue;
         }
+        const int s = jv % C::kStagesV;
+        const uint32_t ph = (uint32_t)(jv / C::kStagesV) & 1u;
+        if (!mbar_wait_warp(&bar_emptyV[s], ph ^ 1u, err, abort_flag)) { aborted = true; break; }
+        mbar_arrive_expect_tx_e(&bar_fullV[s], C::kTileBytes);
+#pragma unroll
+        for (int p = 0; p < C::kPanels; ++p)
+          tma_load_4d_e(sV + s * C::kTileBytes + p * C::kPanelBytes, &tm_v, &bar_fullV[s], p * 64,
+                        hk, jv * kPrefillTileN, b);
+        ++jv;
+      }
+      if (aborted) {
+        // let the copies already issued land before shared memory is released
+        for (int u2 = max(0, jk - C::kStagesK); u2 < jk; ++u2)
+          mbar_wait(&bar_fullK[u2 % C::kStagesK], (uint32_t)(u2 / C::kStagesK) & 1u, nullptr, nullptr,
+                    100000000ull);
+        for (int u2 = max(0, jv - C::kStagesV); u2 < jv; ++u2)
+          mbar_wait(&bar_fullV[u2 % C::kStagesV], (uint32_t)(u2 / C::kStagesV) & 1u, nullptr, nullptr,
+                    100000000ull);
       }
     }
   } else if (warp == C::kMmaWarp) {
     // =========================== MMA issuer ===========================
-    if (lane == 0 && n_kv > 0) {
+    // The whole warp runs the loop with warp-uniform descriptors; one elected
+    // lane issues each tcgen05.mma / commit.
+    if (n_kv > 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);  // Q, K both K-major
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, 0, 1);    // P (TMEM), V MN-major
-      const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV);
-      bool ok = mbar_wait(bar_q, 0, err, abort_flag);
+      constexpr uint64_t kTileDesc = (uint64_t)(C::kTileBytes >> 4);  // descriptor step per tile
+      uint64_t dq[NQ];
+#pragma unroll
+      for (int t = 0; t < NQ; ++t)
+        dq[t] = smem_desc(smem_u32(sQ + t * C::kTileBytes), 16, 1024, kSwizzle128B);
+      const uint64_t dk0 = smem_desc(smem_u32(sK), 16, 1024, kSwizzle128B);
+      const uint64_t dv0 = smem_desc(smem_u32(sV), C::kPanelBytes, 1024, kSwizzle128B);
+      bool ok = mbar_wait_warp(bar_q, 0, err, abort_flag);
       tc_fence_after();
 
       // S_t(j) = Q_t K_j^T into S buffer `buf`
       auto issue_s = [&](int t, int j, int buf) {
-        const uint32_t kbase = sKa + (j % C::kStages) * C::kTileBytes;
-        const uint32_t qbase = sQa + t * C::kTileBytes;
+        const uint64_t dk = dk0 + (uint64_t)(j % C::kStagesK) * kTileDesc;
         const uint32_t d_tmem = tmem + C::s_col(t, buf);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kPanelBytes + (kk & 3) * 32;
-          mma_ss(d_tmem, smem_desc(qbase + off, 16, 1024, kSwizzle128B),
-                 smem_desc(kbase + off, 16, 1024, kSwizzle128B), idesc_s, kk > 0 ? 1u : 0u);
+          const uint64_t off = (uint64_t)(((kk >> 2) * C::kPanelBytes + (kk & 3) * 32) >> 4);
+          mma_ss_e(d_tmem, dq[t] + off, dk + off, idesc_s, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&bar_S[t * NS + buf]);
+        mma_commit_e(&bar_S[t * NS + buf]);
       };
       // O_t += P_t(j) V_j, P read from TMEM over S buffer `buf`
       auto issue_pv = [&](int t, int j, int buf) {
-        const uint32_t vbase = sVa + (j % C::kStages) * C::kTileBytes;
+        const uint64_t dv = dv0 + (uint64_t)(j % C::kStagesV) * kTileDesc;
         const uint32_t p_tmem = tmem + C::s_col(t, buf);
         const uint32_t d_tmem = tmem + C::o_col(t);
 #pragma unroll
-        for (int kk = 0; kk < kPrefillTileN / 16; ++kk) {
-          mma_ts(d_tmem, p_tmem + kk * 8, smem_desc(vbase + kk * 2048, C::kPanelBytes, 1024, kSwizzle128B),
-                 idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(&bar_O[t]);
-        if (j == ti[t].n_kv - 1) mma_commit(&bar_Fin[t]);
+        for (int kk = 0; kk < kPrefillTileN / 16; ++kk)
+          mma_ts_e(d_tmem, p_tmem + kk * 8, dv + (uint64_t)(kk * (2048 >> 4)), idesc_o,
+                   (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit_e(&bar_O[t]);
+        if (j == ti[t].n_kv - 1) mma_commit_e(&bar_Fin[t]);
       };
 
       if (ok) {
         // prologue: S of the first KV tile (and the second one with two S buffers)
-        ok = mbar_wait(&bar_fullK[0], 0, err, abort_flag);
+        ok = mbar_wait_warp(&bar_fullK[0], 0, err, abort_flag);
         tc_fence_after();
         if (ok) {
 #pragma unroll
           for (int t = 0; t < NQ; ++t)
             if (ti[t].n_kv > 0) issue_s(t, 0, 0);
-          mma_commit(&bar_emptyK[0]);
+          mma_commit_e(&bar_emptyK[0]);
         }
         if constexpr (NQ == 1) {
           if (ok && n_kv > 1) {
-            ok = mbar_wait(&bar_fullK[1 % C::kStages], (uint32_t)(1 / C::kStages) & 1u, err, abort_flag);
+            ok = mbar_wait_warp(&bar_fullK[1 % C::kStagesK], (uint32_t)(1 / C::kStagesK) & 1u, err,
+                                abort_flag);
             tc_fence_after();
             if (ok) {
               issue_s(0, 1, 1);
-              mma_commit(&bar_emptyK[1 % C::kStages]);
+              mma_commit_e(&bar_emptyK[1 % C::kStagesK]);
             }
           }
         }
         for (int j = 0; ok && j < n_kv; ++j) {
-          const int s = j % C::kStages;
-          const uint32_t ph = (uint32_t)(j / C::kStages) & 1u;
-          if (!mbar_wait(&bar_fullV[s], ph, err, abort_flag)) break;
+          const int s = j % C::kStagesV;
+          const uint32_t ph = (uint32_t)(j / C::kStagesV) & 1u;
+          if (!mbar_wait_warp(&bar_fullV[s], ph, err, abort_flag)) break;
           tc_fence_after();
           if constexpr (NQ == 2) {
             const int jn = j + 1;
@@ -299,14 +328,17 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
 #pragma unroll
             for (int t = 0; t < NQ; ++t) {
               if (j < ti[t].n_kv) {
-                if (!mbar_wait(&bar_P[t], (uint32_t)j & 1u, err, abort_flag)) { ok = false; break; }
+                if (!mbar_wait_warp(&bar_P[t], (uint32_t)j & 1u, err, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 issue_pv(t, j, 0);
               }
               if (jn < ti[t].n_kv) {
                 if (!k_ready) {
-                  const int sn = jn % C::kStages;
-                  if (!mbar_wait(&bar_fullK[sn], (uint32_t)(jn / C::kStages) & 1u, err, abort_flag)) { ok = false; break; }
+                  const int sn = jn % C::kStagesK;
+                  if (!mbar_wait_warp(&bar_fullK[sn], (uint32_t)(jn / C::kStagesK) & 1u, err, abort_flag)) {
+                    ok = false;
+                    break;
+                  }
                   tc_fence_after();
                   k_ready = true;
                 }
@@ -314,24 +346,24 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
               }
             }
             if (!ok) break;
-            if (k_ready) mma_commit(&bar_emptyK[jn % C::kStages]);
+            if (k_ready) mma_commit_e(&bar_emptyK[jn % C::kStagesK]);
+            mma_commit_e(&bar_emptyV[s]);
           } else {
             // two S buffers: S(j+1) was issued one iteration ahead; issue S(j+2) after PV(j)
-            if (!mbar_wait(&bar_P[0], (uint32_t)j & 1u, err, abort_flag)) break;
+            if (!mbar_wait_warp(&bar_P[0], (uint32_t)j & 1u, err, abort_flag)) break;
             tc_fence_after();
             issue_pv(0, j, j & 1);
             // release V(j) before waiting on K(j+2): the producer loads V(j+1) ahead of K(j+2)
-            mma_commit(&bar_emptyV[s]);
+            mma_commit_e(&bar_emptyV[s]);
             const int jn = j + 2;
             if (jn < n_kv) {
-              const int sn = jn % C::kStages;
-              if (!mbar_wait(&bar_fullK[sn], (uint32_t)(jn / C::kStages) & 1u, err, abort_flag)) break;
+              const int sn = jn % C::kStagesK;
+              if (!mbar_wait_warp(&bar_fullK[sn], (uint32_t)(jn / C::kStagesK) & 1u, err, abort_flag)) break;
               tc_fence_after();
               issue_s(0, jn, jn & 1);
-              mma_commit(&bar_emptyK[sn]);
+              mma_commit_e(&bar_emptyK[sn]);
             }
           }
-          if constexpr (NQ == 2) mma_commit(&bar_emptyV[s]);
         }
       }
     }

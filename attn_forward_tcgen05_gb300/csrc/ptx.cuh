@@ -1,10 +1,10 @@
 // ptx.cuh -- thin inline-PTX wrappers for sm_103a: mbarrier, TMA (cp.async.bulk.tensor),
 // tcgen05 (TMEM alloc / MMA / commit / ld / st) and bounded waits.
 //
-// Every wait on an mbarrier here is bounded: after ATTN_WAIT_LIMIT_NS of
-// %globaltimer time it records an error code in the library's device error
-// word, raises the CTA-wide abort flag and returns false, so a kernel can
-// wind down (drain its copies, free TMEM) instead of hanging the GPU.
+// Every wait on an mbarrier here is bounded: after about ATTN_WAIT_LIMIT_NS
+// (counted in SM cycles) it records an error code in the library's device
+// error word, raises the CTA-wide abort flag and returns false, so a kernel
+// can wind down (drain its copies, free TMEM) instead of hanging the GPU.
 #pragma once
 #include <cstdint>
 #include <cuda.h>
@@ -14,8 +14,15 @@
 #ifndef ATTN_WAIT_LIMIT_NS
 #define ATTN_WAIT_LIMIT_NS 4000000000ull  // 4 s: far beyond any healthy pipeline wait
 #endif
+#ifndef ATTN_TRY_WAIT_HINT_NS
+#define ATTN_TRY_WAIT_HINT_NS 1000000u    // 1 ms cap on one hardware suspend of try_wait
+#endif
 
 namespace attn {
+
+// Cycles per nanosecond at the highest SM clock (2070 MHz): converts a wait
+// limit in nanoseconds into a cycle budget for clock64().
+constexpr double kMaxSmClockGHz = 2.07;
 
 // Device error codes written to the error word (first one wins).
 enum : uint32_t {
@@ -26,12 +33,6 @@ enum : uint32_t {
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ uint64_t globaltimer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
 }
 
 // ---------------------------------------------------------------- mbarrier
@@ -58,34 +59,37 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
 
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity) {
   uint32_t ok;
+  // suspend-time hint (ns): the waiting thread sleeps at most this long before re-checking
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar_addr), "r"(parity)
+      : "r"(bar_addr), "r"(parity), "r"(ATTN_TRY_WAIT_HINT_NS)
       : "memory");
   return ok != 0;
 }
 
 // Wait until the phase with parity `parity` of `bar` has completed.  Bounded:
-// gives up after ATTN_WAIT_LIMIT_NS (or as soon as another thread of the CTA
-// raised *abort), records kErrWaitTimeout in *err and returns false.
+// gives up after about limit_ns (measured with the SM cycle counter, which is
+// cheap to read, at the maximum SM clock), or as soon as another thread of the
+// CTA raised *abort; records kErrWaitTimeout in *err and returns false.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err,
                                           volatile int* abort,
                                           uint64_t limit_ns = ATTN_WAIT_LIMIT_NS) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (;;) {
-#pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(a, parity)) return true;
-    if (abort != nullptr && *abort) return false;
-    if (globaltimer_ns() - t0 > limit_ns) {
-      if (err) atomicCAS(err, kErrNone, kErrWaitTimeout);
-      if (abort) *abort = 1;
-      return false;
+  const long long t0 = clock64();
+  const long long limit_cycles = (long long)(limit_ns * kMaxSmClockGHz);
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(a, parity)) return true;
+    if ((n & 63u) == 0) {
+      if (abort != nullptr && *abort) return false;
+      if (clock64() - t0 > limit_cycles) {
+        if (err) atomicCAS(err, kErrNone, kErrWaitTimeout);
+        if (abort) *abort = 1;
+        return false;
+      }
     }
   }
 }
@@ -254,6 +258,82 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
       "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]),
       "r"(r[30]), "r"(r[31])
       : "memory");
+}
+
+// ---------------------------------------------------------------- elected issue
+// The issuing warp runs its loop in lock-step (every lane computes the same
+// descriptors and coordinates, so they stay in uniform registers) and one lane,
+// chosen by elect.sync inside the same instruction sequence, issues the
+// asynchronous operation.  Issuing from a divergent single-lane branch instead
+// makes every tcgen05.mma / TMA issue far slower.
+__device__ __forceinline__ void mma_ss_e(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_ts_e(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit_e(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx_e(uint64_t* bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+      "r"(bytes)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d_e(void* smem_dst, const CUtensorMap* map, uint64_t* bar,
+                                              int c0, int c1, int c2, int c3) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];\n\t}" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d_hint_e(void* smem_dst, const CUtensorMap* map,
+                                                   uint64_t* bar, int c0, int c1, int c2, int c3,
+                                                   uint64_t policy) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;\n\t}" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "l"(policy)
+      : "memory");
+}
+
+// Warp-uniform bounded wait: every lane polls, the warp agrees on the result.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, uint32_t* err,
+                                               volatile int* abort) {
+  return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, err, abort));
 }
 
 // ---------------------------------------------------------------- descriptors
