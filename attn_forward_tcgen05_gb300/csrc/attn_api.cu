@@ -123,8 +123,8 @@ int attn_prefill_fwd(const attn_bf16_t* q, const attn_bf16_t* k, const attn_bf16
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (Skv == 0) return from_cuda(attn::launch_prefill_empty_kv(a, s));
   int rc = encode_bf16_4d(&a.tm_q, q, d, Hq, Sq, B, attn::kPrefillTileM);
-  if (rc == ATTN_OK) rc = encode_bf16_4d(&a.tm_k, k, d, Hkv, Skv, B, attn::kPrefillTileN);
-  if (rc == ATTN_OK) rc = encode_bf16_4d(&a.tm_v, v, d, Hkv, Skv, B, attn::kPrefillTileN);
+  if (rc == ATTN_OK) rc = encode_bf16_4d(&a.tm_k, k, d, Hkv, Skv, B, attn::kPrefillKVStageRows);
+  if (rc == ATTN_OK) rc = encode_bf16_4d(&a.tm_v, v, d, Hkv, Skv, B, attn::kPrefillKVStageRows);
   if (rc != ATTN_OK) return rc;
   return from_cuda(attn::launch_prefill(a, s));
 }

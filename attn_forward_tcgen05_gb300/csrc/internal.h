@@ -9,7 +9,8 @@ namespace attn {
 
 // Prefill launch description (already validated by the C-ABI layer).
 struct PrefillArgs {
-  CUtensorMap tm_q, tm_k, tm_v;  // 4-D maps {d, H, S, B}, box {64, 1, 128, 1}, 128B swizzle
+  CUtensorMap tm_q, tm_k, tm_v;  // 4-D maps {d, H, S, B}, box {64, 1, rows, 1}, 128B swizzle:
+                                 // rows = kPrefillTileM for Q, kPrefillKVStageRows for K, V
   void* o;                       // [B][Sq][Hq][d], fp32 or bf16
   float* lse;                    // [B][Hq][Sq]
   int B, Hq, Hkv, Sq, Skv, d, causal, o_bf16;
@@ -39,9 +40,10 @@ struct MergeArgs {
 
 // Rows of a KV tile streamed by the decode producer per pipeline stage.
 constexpr int kDecodeTileRows = 32;
-// Rows of a Q tile / KV tile in the prefill kernel.
+// Rows of a Q tile in the prefill kernel, and of one TMA-loaded K / V stage
+// (the kernel may compute on sub-tiles of a stage).
 constexpr int kPrefillTileM = 128;
-constexpr int kPrefillTileN = 128;
+constexpr int kPrefillKVStageRows = 128;
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill_empty_kv(const PrefillArgs& a, cudaStream_t stream);

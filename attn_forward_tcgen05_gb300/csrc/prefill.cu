@@ -1,17 +1,22 @@
 // prefill.cu -- exact attention forward (FMHA) on the 5th-generation tensor cores.
 //
 // Per CTA: NQ query tiles of 128 rows of one (batch, query head), streamed
-// against 128-row K/V tiles of the matching KV head.  Warp roles:
+// against K/V tiles of BN = 128 rows of the matching KV head, which arrive by
+// TMA in stages of 128 rows (the kernel also runs 64-row tiles, two per stage,
+// with one TMA box per 128 rows: the copy engine's cost grows with the number
+// of boxes much more than with their size).  Warp roles:
 //   * warps 0 .. 4*NQ-1  softmax warpgroups, one per query tile (thread = row):
 //       read S from TMEM, apply the causal / length mask, keep the running
 //       row max m and row sum l, rescale O in TMEM when m grows by more than
 //       2^8, write P (bf16) back into TMEM over S, and finally normalise O and
 //       store O and LSE;
-//   * warp 4*NQ       MMA issuer (one thread): S = Q K^T and O += P V with
-//       tcgen05.mma (kind::f16, bf16 in, fp32 accumulate in TMEM; P is the A
-//       operand straight from TMEM);
-//   * warp 4*NQ+1     TMA producer (one thread): Q once, then a ring of K and
-//       V stages, each 128 rows x d, 128-byte swizzled.
+//   * warp 4*NQ       MMA issuer: S = Q K^T and O += P V with tcgen05.mma
+//       (kind::f16, bf16 in, fp32 accumulate in TMEM; P is the A operand
+//       straight from TMEM);
+//   * warp 4*NQ+1     TMA producer: Q once, then a ring of K and a ring of V
+//       stages, each 128 rows x d, 128-byte swizzled.
+// The MMA and TMA warps run their loops as whole warps (warp-uniform
+// descriptors); one elected lane issues each instruction.
 //
 // The algorithm is the online softmax of "60 . r57 -- FA KV staging double
 // buffering (REVERTED)", section 2.3 (at every KV tile boundary
@@ -21,16 +26,24 @@
 // kept in TMEM as the A operand of the P.V MMA).  What differs from that page:
 // O is normalised in-kernel (each thread owns one TMEM lane = one row, so the
 // TMEM round trip is a plain 32x32b load/store with matching shapes), LSE is in
-// natural-log units, and the O rescale is skipped while the running max has
-// grown by at most 2^8 (the final O / l uses the same stale max in numerator
-// and denominator, so the result is unchanged up to rounding).
+// natural-log units, the O rescale is skipped while the running max has grown
+// by at most 2^8 (the final O / l uses the same stale max in numerator and
+// denominator, so the result is unchanged up to rounding), and for d = 256
+// the query tile has two S buffers.
 //
-// TMEM columns (512 allocated, 128 lanes):
-//   NQ = 2 (d <= 128):  tile t: S/P at t*(128 + d) ... one S buffer per tile
-//   NQ = 1 (d == 256):  S buffers at 0 and 128, O at 256
-// Scheduling (MMA issue order) keeps the tensor pipe busy while the softmax
-// warps work:  NQ = 2:  PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) ...
-//              NQ = 1:  S(j+1) PV(j) ...  (two S buffers)
+// TMEM columns (512 allocated, 128 lanes): O of tile t at t*d, then the S
+// buffers, BN = 128 columns each:  d = 256: O_0 S_00 S_01;  d <= 128:
+// O_0 O_1 S_0 S_1 (one S buffer per tile).  With two S buffers the MMA warp computes
+// S(j+1) = Q K(j+1)^T while the softmax warps work on S(j); the issue order
+// per KV tile j is  S_0(j+1) [S_1(j+1)] P_0(j).V(j) [P_1(j).V(j)],  so the
+// tensor pipe is never idle waiting for a softmax pass.  P(j) lives in the S
+// buffer of tile j, and S(j+2) overwrites it only after P(j).V(j) (issued
+// earlier, executed in order) has read it.  With one S buffer per tile (d <=
+// 128: two S buffers per tile would leave room for 64-key tiles only, which
+// need twice the MMA instructions per key, each re-reading Q from shared
+// memory; measured slower) the order
+// is  P_0(j).V(j) S_0(j+1) P_1(j).V(j) S_1(j+1):  S_t(j+1) follows P_t(j).V(j),
+// and each tile's softmax overlaps the other tile's MMAs.
 #include <cmath>
 
 #include "internal.h"
@@ -46,10 +59,22 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when m 
 template <int D>
 struct PrefillCfg {
   static constexpr int NQ = (D <= 128) ? 2 : 1;            // query tiles per CTA
-  static constexpr int NS = (NQ == 2) ? 1 : 2;             // S buffers per query tile
+#ifndef ATTN_PREFILL_NS
+  static constexpr int NS = (D == 256) ? 2 : 1;            // S buffers per query tile
+#else
+  static constexpr int NS = ATTN_PREFILL_NS;
+#endif
+  // rows of a K / V tile (S has BN columns): TMEM holds NQ O tiles of d columns
+  // and NQ*NS S buffers of BN columns
+  static constexpr int BN = (NQ * D + NQ * NS * 128 <= 512) ? 128 : 64;
+  static constexpr int kStageRows = kPrefillKVStageRows;   // rows of a TMA-loaded K / V stage
+  static constexpr int kSub = kStageRows / BN;             // KV tiles per stage
   static constexpr int kPanels = D / 64;                   // 128-byte panels per row
-  static constexpr int kPanelBytes = 128 * 128;            // 128 rows x 128 bytes
-  static constexpr int kTileBytes = kPanels * kPanelBytes; // one 128 x d bf16 tile
+  static constexpr int kQPanelBytes = kPrefillTileM * 128; // one panel of a Q tile
+  static constexpr int kKVPanelBytes = kStageRows * 128;   // one panel of a K / V stage
+  static constexpr int kSubBytes = BN * 128;               // offset of tile h of a stage in a panel
+  static constexpr int kQTileBytes = kPanels * kQPanelBytes;
+  static constexpr int kKVStageBytes = kPanels * kKVPanelBytes;
 #ifndef ATTN_PREFILL_KSTAGES
   static constexpr int kStagesK = (D == 64) ? 4 : (D == 128 ? 2 : 1);  // K ring depth
 #else
@@ -61,11 +86,13 @@ struct PrefillCfg {
   static constexpr int kStagesV = ATTN_PREFILL_VSTAGES;
 #endif
   static constexpr int kQOff = 0;
-  static constexpr int kKOff = NQ * kTileBytes;
-  static constexpr int kVOff = kKOff + kStagesK * kTileBytes;
-  static constexpr int kBarOff = kVOff + kStagesV * kTileBytes;
-  // barriers: fullQ, fullK[SK], emptyK[SK], fullV[SV], emptyV[SV], S[NQ][NS], P[NQ], O[NQ], Fin[NQ]
-  static constexpr int kNumBars = 1 + 2 * kStagesK + 2 * kStagesV + NQ * NS + 3 * NQ;
+  static constexpr int kKOff = NQ * kQTileBytes;
+  static constexpr int kVOff = kKOff + kStagesK * kKVStageBytes;
+  static constexpr int kBarOff = kVOff + kStagesV * kKVStageBytes;
+  // barriers: fullQ, fullK[SK], emptyK[SK], fullV[SV], emptyV[SV], S[NQ][NS],
+  // P[NQ][NS], O[NQ], Fin[NQ].  S and P have one barrier per S buffer, so each
+  // is at most one phase ahead of the warp that waits on it.
+  static constexpr int kNumBars = 1 + 2 * kStagesK + 2 * kStagesV + 2 * NQ * NS + 2 * NQ;
   static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;
   // NQ softmax warpgroups + one control warpgroup (MMA warp, TMA warp, two spare warps).
   static constexpr int kThreads = (4 * NQ + 4) * 32;
@@ -81,14 +108,13 @@ struct PrefillCfg {
   static_assert(NQ != 2 || (4 * NQ * kSoftmaxRegs + 4 * kCtlRegs) * 32 <= kThreads * kLaunchRegs,
                 "register split exceeds the launch allocation");
   static constexpr uint32_t kTmemCols = 512;
-  // TMEM column of S buffer `buf` of tile t, and of O of tile t
+  __host__ __device__ static constexpr uint32_t o_col(int t) { return (uint32_t)(t * D); }
   __host__ __device__ static constexpr uint32_t s_col(int t, int buf) {
-    return NQ == 2 ? (uint32_t)(t * (128 + D)) : (uint32_t)(buf * 128);
+    return (uint32_t)(NQ * D + (t * NS + buf) * BN);
   }
-  __host__ __device__ static constexpr uint32_t o_col(int t) {
-    return NQ == 2 ? (uint32_t)(t * (128 + D) + 128) : 256u;
-  }
-  static_assert(NQ * (NS * 128 + D) <= 512, "TMEM budget");
+  static_assert(NQ * D + NQ * NS * BN <= 512, "TMEM budget");
+  static_assert(BN % 32 == 0 && BN <= 128, "S is read in 32-column loads; P.V has K = BN");
+  static_assert(kStageRows % BN == 0 && kSubBytes % 1024 == 0, "tiles start on a swizzle atom");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
@@ -99,6 +125,7 @@ struct TileInfo {
   int kv_lo;   // every existing row of the tile admits keys [0, kv_lo): tiles past it need a mask
 };
 
+template <int BN>
 __device__ __forceinline__ TileInfo tile_info(int q0, int Sq, int Skv, int causal) {
   TileInfo ti;
   ti.q0 = q0;
@@ -115,7 +142,7 @@ __device__ __forceinline__ TileInfo tile_info(int q0, int Sq, int Skv, int causa
     kv_hi = (int)(hi < 0 ? 0 : (hi > Skv ? Skv : hi));
     kv_lo = (int)(lo < 0 ? 0 : (lo > Skv ? Skv : lo));
   }
-  ti.n_kv = (kv_hi + kPrefillTileN - 1) / kPrefillTileN;
+  ti.n_kv = (kv_hi + BN - 1) / BN;
   ti.kv_lo = kv_lo;
   return ti;
 }
@@ -127,7 +154,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
                     float* __restrict__ lse_ptr, int Hq, int Hkv, int Sq, int Skv, int causal,
                     int o_bf16, float scale, int n_units_per_head_batch, uint32_t* err) {
   using C = PrefillCfg<D>;
-  constexpr int NQ = C::NQ, NS = C::NS;
+  constexpr int NQ = C::NQ, NS = C::NS, BN = C::BN;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // ---- work unit: longest causal work first ----
@@ -151,16 +178,17 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
   uint64_t* bar_emptyK = bar_fullK + C::kStagesK;
   uint64_t* bar_fullV = bar_emptyK + C::kStagesK;
   uint64_t* bar_emptyV = bar_fullV + C::kStagesV;
-  uint64_t* bar_S = bar_emptyV + C::kStagesV;  // [NQ][NS]
-  uint64_t* bar_P = bar_S + NQ * NS;          // [NQ]
-  uint64_t* bar_O = bar_P + NQ;               // [NQ] one phase per P.V MMA group
-  uint64_t* bar_Fin = bar_O + NQ;             // [NQ] last P.V done
+  uint64_t* bar_S = bar_emptyV + C::kStagesV;  // [NQ][NS] S of a KV tile computed
+  uint64_t* bar_P = bar_S + NQ * NS;           // [NQ][NS] P of a KV tile stored
+  uint64_t* bar_O = bar_P + NQ * NS;           // [NQ] one phase per P.V MMA group
+  uint64_t* bar_Fin = bar_O + NQ;              // [NQ] last P.V done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   TileInfo ti[NQ];
 #pragma unroll
-  for (int t = 0; t < NQ; ++t) ti[t] = tile_info(qb * NQ * kPrefillTileM + t * kPrefillTileM, Sq, Skv, causal);
+  for (int t = 0; t < NQ; ++t)
+    ti[t] = tile_info<BN>(qb * NQ * kPrefillTileM + t * kPrefillTileM, Sq, Skv, causal);
   int n_kv = 0;
 #pragma unroll
   for (int t = 0; t < NQ; ++t) n_kv = max(n_kv, ti[t].n_kv);
@@ -175,9 +203,11 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
       mbar_init(&bar_fullV[s], 1);
       mbar_init(&bar_emptyV[s], 1);
     }
-    for (int i = 0; i < NQ * NS; ++i) mbar_init(&bar_S[i], 1);
+    for (int i = 0; i < NQ * NS; ++i) {
+      mbar_init(&bar_S[i], 1);
+      mbar_init(&bar_P[i], 4);  // one arrive per softmax warp
+    }
     for (int t = 0; t < NQ; ++t) {
-      mbar_init(&bar_P[t], 4);  // one arrive per softmax warp
       mbar_init(&bar_O[t], 1);
       mbar_init(&bar_Fin[t], 1);
     }
@@ -198,7 +228,6 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
     if constexpr (NQ == 2) setmaxnreg_dec<C::kCtlRegs>();  // whole warpgroup, same instruction
   if (warp == C::kTmaWarp) {
     // =========================== TMA producer ===========================
-    // The whole warp runs the loop; one elected lane issues each copy.
     if (n_kv > 0) {
       if (lane == 0) {
         tma_prefetch_desc(&tm_q);
@@ -208,41 +237,44 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
       uint32_t qbytes = 0;
 #pragma unroll
       for (int t = 0; t < NQ; ++t)
-        if (ti[t].n_kv > 0) qbytes += C::kTileBytes;
+        if (ti[t].n_kv > 0) qbytes += C::kQTileBytes;
       mbar_arrive_expect_tx_e(bar_q, qbytes);
 #pragma unroll
       for (int t = 0; t < NQ; ++t) {
         if (ti[t].n_kv > 0) {
 #pragma unroll
           for (int p = 0; p < C::kPanels; ++p)
-            tma_load_4d_e(sQ + t * C::kTileBytes + p * C::kPanelBytes, &tm_q, bar_q, p * 64, hq,
+            tma_load_4d_e(sQ + t * C::kQTileBytes + p * C::kQPanelBytes, &tm_q, bar_q, p * 64, hq,
                           ti[t].q0, b);
         }
       }
-      // K(j) and V(j) alternate; each ring has its own depth
-      int jk = 0, jv = 0;
+      // Stages of kSub KV tiles.  The MMA warp takes the K stage of tile j+1
+      // before the V stage of tile j, so K stage uk goes out before V stage uv
+      // while uk*kSub - 1 <= uv*kSub.
+      const int n_st = (n_kv + C::kSub - 1) / C::kSub;
+      int jk = 0, jv = 0;  // next K / V stage
       bool aborted = false;
-      while (jv < n_kv) {
-        if (jk < n_kv && jk <= jv) {
+      while (jv < n_st) {
+        if (jk < n_st && jk * C::kSub <= jv * C::kSub + 1) {
           const int s = jk % C::kStagesK;
           const uint32_t ph = (uint32_t)(jk / C::kStagesK) & 1u;
           if (!mbar_wait_warp(&bar_emptyK[s], ph ^ 1u, err, abort_flag)) { aborted = true; break; }
-          mbar_arrive_expect_tx_e(&bar_fullK[s], C::kTileBytes);
+          mbar_arrive_expect_tx_e(&bar_fullK[s], C::kKVStageBytes);
 #pragma unroll
           for (int p = 0; p < C::kPanels; ++p)
-            tma_load_4d_e(sK + s * C::kTileBytes + p * C::kPanelBytes, &tm_k, &bar_fullK[s], p * 64,
-                          hk, jk * kPrefillTileN, b);
+            tma_load_4d_e(sK + s * C::kKVStageBytes + p * C::kKVPanelBytes, &tm_k, &bar_fullK[s], p * 64,
+                          hk, jk * C::kStageRows, b);
           ++jk;
           continue;
         }
         const int s = jv % C::kStagesV;
         const uint32_t ph = (uint32_t)(jv / C::kStagesV) & 1u;
         if (!mbar_wait_warp(&bar_emptyV[s], ph ^ 1u, err, abort_flag)) { aborted = true; break; }
-        mbar_arrive_expect_tx_e(&bar_fullV[s], C::kTileBytes);
+        mbar_arrive_expect_tx_e(&bar_fullV[s], C::kKVStageBytes);
 #pragma unroll
         for (int p = 0; p < C::kPanels; ++p)
-          tma_load_4d_e(sV + s * C::kTileBytes + p * C::kPanelBytes, &tm_v, &bar_fullV[s], p * 64,
-                        hk, jv * kPrefillTileN, b);
+          tma_load_4d_e(sV + s * C::kKVStageBytes + p * C::kKVPanelBytes, &tm_v, &bar_fullV[s], p * 64,
+                        hk, jv * C::kStageRows, b);
         ++jv;
       }
       if (aborted) {
@@ -257,114 +289,121 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
     }
   } else if (warp == C::kMmaWarp) {
     // =========================== MMA issuer ===========================
-    // The whole warp runs the loop with warp-uniform descriptors; one elected
-    // lane issues each tcgen05.mma / commit.
     if (n_kv > 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);  // Q, K both K-major
-      constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, 0, 1);    // P (TMEM), V MN-major
-      constexpr uint64_t kTileDesc = (uint64_t)(C::kTileBytes >> 4);  // descriptor step per tile
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, BN, 0, 0);  // Q, K both K-major
+      constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, 0, 1);   // P (TMEM), V MN-major
+      // descriptor start of KV tile j: its stage, then its rows within each panel
+      auto kv_tile_desc = [&](uint64_t d0, int j, int stages) -> uint64_t {
+        const int off = ((j / C::kSub) % stages) * C::kKVStageBytes + (j % C::kSub) * C::kSubBytes;
+        return d0 + (uint64_t)(off >> 4);
+      };
       uint64_t dq[NQ];
 #pragma unroll
       for (int t = 0; t < NQ; ++t)
-        dq[t] = smem_desc(smem_u32(sQ + t * C::kTileBytes), 16, 1024, kSwizzle128B);
+        dq[t] = smem_desc(smem_u32(sQ + t * C::kQTileBytes), 16, 1024, kSwizzle128B);
       const uint64_t dk0 = smem_desc(smem_u32(sK), 16, 1024, kSwizzle128B);
-      const uint64_t dv0 = smem_desc(smem_u32(sV), C::kPanelBytes, 1024, kSwizzle128B);
+      // V as the MN-major B operand: consecutive 64-column panels are kKVPanelBytes apart
+      const uint64_t dv0 = smem_desc(smem_u32(sV), C::kKVPanelBytes, 1024, kSwizzle128B);
       bool ok = mbar_wait_warp(bar_q, 0, err, abort_flag);
       tc_fence_after();
 
-      // S_t(j) = Q_t K_j^T into S buffer `buf`
-      auto issue_s = [&](int t, int j, int buf) {
-        const uint64_t dk = dk0 + (uint64_t)(j % C::kStagesK) * kTileDesc;
-        const uint32_t d_tmem = tmem + C::s_col(t, buf);
+      // S_t(j) = Q_t K_j^T into S buffer j % NS of tile t
+      auto issue_s = [&](int t, int j) {
+        const uint64_t dk = kv_tile_desc(dk0, j, C::kStagesK);
+        const uint32_t d_tmem = tmem + C::s_col(t, j % NS);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t off = (uint64_t)(((kk >> 2) * C::kPanelBytes + (kk & 3) * 32) >> 4);
-          mma_ss_e(d_tmem, dq[t] + off, dk + off, idesc_s, kk > 0 ? 1u : 0u);
+          // k-step of 16 elements: 32 bytes inside a 128-byte panel, then the next panel
+          const uint64_t offq = (uint64_t)(((kk >> 2) * C::kQPanelBytes + (kk & 3) * 32) >> 4);
+          const uint64_t offk = (uint64_t)(((kk >> 2) * C::kKVPanelBytes + (kk & 3) * 32) >> 4);
+          mma_ss_e(d_tmem, dq[t] + offq, dk + offk, idesc_s, kk > 0 ? 1u : 0u);
         }
-        mma_commit_e(&bar_S[t * NS + buf]);
+        mma_commit_e(&bar_S[t * NS + j % NS]);
       };
-      // O_t += P_t(j) V_j, P read from TMEM over S buffer `buf`
-      auto issue_pv = [&](int t, int j, int buf) {
-        const uint64_t dv = dv0 + (uint64_t)(j % C::kStagesV) * kTileDesc;
+      // O_t += P_t(j) V_j, P read from TMEM over S buffer j % NS; tile j is the
+      // (j / NS)-th use of that buffer
+      auto issue_pv = [&](int t, int j) -> bool {
+        const int buf = j % NS;
+        if (!mbar_wait_warp(&bar_P[t * NS + buf], (uint32_t)(j / NS) & 1u, err, abort_flag)) return false;
+        tc_fence_after();
+        const uint64_t dv = kv_tile_desc(dv0, j, C::kStagesV);
         const uint32_t p_tmem = tmem + C::s_col(t, buf);
         const uint32_t d_tmem = tmem + C::o_col(t);
 #pragma unroll
-        for (int kk = 0; kk < kPrefillTileN / 16; ++kk)
+        for (int kk = 0; kk < BN / 16; ++kk)  // 16 keys = 8 TMEM columns of bf16 pairs, 2048 B of V
           mma_ts_e(d_tmem, p_tmem + kk * 8, dv + (uint64_t)(kk * (2048 >> 4)), idesc_o,
                    (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit_e(&bar_O[t]);
         if (j == ti[t].n_kv - 1) mma_commit_e(&bar_Fin[t]);
+        return true;
       };
 
       if (ok) {
-        // prologue: S of the first KV tile (and the second one with two S buffers)
+        // prologue: S of the first KV tile
         ok = mbar_wait_warp(&bar_fullK[0], 0, err, abort_flag);
         tc_fence_after();
         if (ok) {
 #pragma unroll
           for (int t = 0; t < NQ; ++t)
-            if (ti[t].n_kv > 0) issue_s(t, 0, 0);
-          mma_commit_e(&bar_emptyK[0]);
+            if (ti[t].n_kv > 0) issue_s(t, 0);
+          if (C::kSub == 1 || n_kv == 1) mma_commit_e(&bar_emptyK[0]);
         }
-        if constexpr (NQ == 1) {
-          if (ok && n_kv > 1) {
-            ok = mbar_wait_warp(&bar_fullK[1 % C::kStagesK], (uint32_t)(1 / C::kStagesK) & 1u, err,
-                                abort_flag);
+      }
+      // a stage is waited for at its first tile and released after its last one
+      auto first_of_stage = [&](int j) { return j % C::kSub == 0; };
+      auto last_of_stage = [&](int j) { return j % C::kSub == C::kSub - 1 || j == n_kv - 1; };
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int jn = j + 1;
+        if constexpr (NS == 1) {
+          // one S buffer per tile: S_t(j+1) overwrites P_t(j), so it follows P_t(j).V(j);
+          // the tiles alternate so one tile's softmax runs while the other's MMAs do
+          const int u = j / C::kSub, s = u % C::kStagesV;
+          if (first_of_stage(j)) {
+            if (!mbar_wait_warp(&bar_fullV[s], (uint32_t)(u / C::kStagesV) & 1u, err, abort_flag)) break;
             tc_fence_after();
-            if (ok) {
-              issue_s(0, 1, 1);
-              mma_commit_e(&bar_emptyK[1 % C::kStagesK]);
-            }
           }
-        }
-        for (int j = 0; ok && j < n_kv; ++j) {
-          const int s = j % C::kStagesV;
-          const uint32_t ph = (uint32_t)(j / C::kStagesV) & 1u;
-          if (!mbar_wait_warp(&bar_fullV[s], ph, err, abort_flag)) break;
-          tc_fence_after();
-          if constexpr (NQ == 2) {
-            const int jn = j + 1;
-            bool k_ready = false;
+          const int un = jn / C::kSub, sn = un % C::kStagesK;
+          bool k_ready = false;
 #pragma unroll
-            for (int t = 0; t < NQ; ++t) {
-              if (j < ti[t].n_kv) {
-                if (!mbar_wait_warp(&bar_P[t], (uint32_t)j & 1u, err, abort_flag)) { ok = false; break; }
+          for (int t = 0; t < NQ; ++t) {
+            if (ok && j < ti[t].n_kv) ok = issue_pv(t, j);
+            if (ok && jn < ti[t].n_kv) {
+              if (!k_ready && first_of_stage(jn)) {
+                ok = mbar_wait_warp(&bar_fullK[sn], (uint32_t)(un / C::kStagesK) & 1u, err, abort_flag);
                 tc_fence_after();
-                issue_pv(t, j, 0);
               }
-              if (jn < ti[t].n_kv) {
-                if (!k_ready) {
-                  const int sn = jn % C::kStagesK;
-                  if (!mbar_wait_warp(&bar_fullK[sn], (uint32_t)(jn / C::kStagesK) & 1u, err, abort_flag)) {
-                    ok = false;
-                    break;
-                  }
-                  tc_fence_after();
-                  k_ready = true;
-                }
-                issue_s(t, jn, 0);
-              }
-            }
-            if (!ok) break;
-            if (k_ready) mma_commit_e(&bar_emptyK[jn % C::kStagesK]);
-            mma_commit_e(&bar_emptyV[s]);
-          } else {
-            // two S buffers: S(j+1) was issued one iteration ahead; issue S(j+2) after PV(j)
-            if (!mbar_wait_warp(&bar_P[0], (uint32_t)j & 1u, err, abort_flag)) break;
-            tc_fence_after();
-            issue_pv(0, j, j & 1);
-            // release V(j) before waiting on K(j+2): the producer loads V(j+1) ahead of K(j+2)
-            mma_commit_e(&bar_emptyV[s]);
-            const int jn = j + 2;
-            if (jn < n_kv) {
-              const int sn = jn % C::kStagesK;
-              if (!mbar_wait_warp(&bar_fullK[sn], (uint32_t)(jn / C::kStagesK) & 1u, err, abort_flag)) break;
-              tc_fence_after();
-              issue_s(0, jn, jn & 1);
-              mma_commit_e(&bar_emptyK[sn]);
+              k_ready = true;
+              if (ok) issue_s(t, jn);
             }
           }
+          if (!ok) break;
+          if (k_ready && last_of_stage(jn)) mma_commit_e(&bar_emptyK[sn]);
+          if (last_of_stage(j)) mma_commit_e(&bar_emptyV[s]);
+          continue;
         }
+        // S(j+1) into the other S buffer: its previous P was read by P.V(j-1), issued before
+        if (jn < n_kv) {
+          const int un = jn / C::kSub, sn = un % C::kStagesK;
+          if (first_of_stage(jn)) {
+            if (!mbar_wait_warp(&bar_fullK[sn], (uint32_t)(un / C::kStagesK) & 1u, err, abort_flag)) break;
+            tc_fence_after();
+          }
+#pragma unroll
+          for (int t = 0; t < NQ; ++t)
+            if (jn < ti[t].n_kv) issue_s(t, jn);
+          if (last_of_stage(jn)) mma_commit_e(&bar_emptyK[sn]);
+        }
+        const int u = j / C::kSub, s = u % C::kStagesV;
+        if (first_of_stage(j)) {
+          if (!mbar_wait_warp(&bar_fullV[s], (uint32_t)(u / C::kStagesV) & 1u, err, abort_flag)) break;
+          tc_fence_after();
+        }
+#pragma unroll
+        for (int t = 0; t < NQ; ++t) {
+          if (ok && j < ti[t].n_kv) ok = issue_pv(t, j);
+        }
+        if (!ok) break;
+        if (last_of_stage(j)) mma_commit_e(&bar_emptyV[s]);
       }
     }
   }
@@ -388,25 +427,23 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
     bool ok = true;
 
     for (int j = 0; j < my.n_kv; ++j) {
-      const int buf = (NS == 1) ? 0 : (j & 1);
-      const uint32_t sph = (NS == 1) ? ((uint32_t)j & 1u) : ((uint32_t)(j >> 1) & 1u);
+      const int buf = j % NS;
+      const uint32_t sph = (uint32_t)(j / NS) & 1u;
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bar_S[t * NS + buf], sph, err, abort_flag))) {
         ok = false;
         break;
       }
       tc_fence_after();
       const uint32_t s_addr = lane_addr + C::s_col(t, buf);
-      uint32_t sr[128];
-      tmem_ld32(s_addr + 0, sr + 0);
-      tmem_ld32(s_addr + 32, sr + 32);
-      tmem_ld32(s_addr + 64, sr + 64);
-      tmem_ld32(s_addr + 96, sr + 96);
+      uint32_t sr[BN];
+#pragma unroll
+      for (int c0 = 0; c0 < BN; c0 += 32) tmem_ld32(s_addr + c0, sr + c0);
       tmem_wait_ld();
       // mask: keys at or past row_bound (causal bound or Skv)
-      if ((j + 1) * kPrefillTileN > my.kv_lo) {
-        const int lim = row_bound - j * kPrefillTileN;
+      if ((j + 1) * BN > my.kv_lo) {
+        const int lim = row_bound - j * BN;
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
+        for (int c = 0; c < BN; ++c)
           if (c >= lim) sr[c] = __float_as_uint(-INFINITY);
       }
       // row max: four independent chains of three-input max
@@ -415,7 +452,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
       for (int a = 0; a < 4; ++a)
         mx[a] = max3f(__uint_as_float(sr[3 * a]), __uint_as_float(sr[3 * a + 1]), __uint_as_float(sr[3 * a + 2]));
 #pragma unroll
-      for (int c = 12; c < 128; c += 2)
+      for (int c = 12; c < BN; c += 2)
         mx[(c >> 1) & 3] = max3f(mx[(c >> 1) & 3], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
       const float m_tile = fmaxf(max3f(mx[0], mx[1], mx[2]), mx[3]) * sl2;
       const float m_new = fmaxf(m_used, m_tile);
@@ -453,7 +490,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
       // P.V MMA uses (for O / l: consistent weights, so P rounding cancels for flat V)
       uint64_t lex2 = f2pack(0.f, 0.f), lrd2 = f2pack(0.f, 0.f);
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
+      for (int h = 0; h < BN / 32; ++h) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
@@ -466,7 +503,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
           lex2 = add2(lex2, f2pack(p0, p1));
           lrd2 = add2(lrd2, f2pack(__uint_as_float(pk[e] << 16), __uint_as_float(pk[e] & 0xFFFF0000u)));
         }
-        tmem_st16(s_addr + 16 * h, pk);  // P: bf16 pairs over the first 64 columns of S
+        tmem_st16(s_addr + 16 * h, pk);  // P: bf16 pairs over the first BN/2 columns of S
       }
       {
         float a0, a1, b0, b1;
@@ -475,10 +512,11 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
         l += a0 + a1;
         l_rnd += b0 + b1;
       }
+      // publish P(j): the MMA warp reads it as the A operand of P.V
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_P[t]);
+      if (lane == 0) mbar_arrive(&bar_P[t * NS + buf]);
     }
 
     // ---- epilogue: O / l and LSE ----

@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import oracle
-from attn_forward_tcgen05_gb300 import decode_split, merge
+from attn_forward_tcgen05_gb300 import decode_split, merge, sync_check
 from attn_forward_tcgen05_gb300 import workloads as W
 from tests.tolerances import check_lse, check_o
 
@@ -16,7 +16,7 @@ pytestmark = pytest.mark.gpu
 def _compare(q, kc, vc, lens, n_splits, min_rows, scale, out_dtype=torch.bfloat16):
     po, pl = decode_split(q.cuda(), kc.cuda(), vc.cuda(), lens.cuda(), n_splits, min_rows, scale)
     o, lse = merge(po, pl, out_dtype)
-    torch.cuda.synchronize()
+    sync_check()  # a bounded pipeline wait that ran out would surface here
     rpo, rpl = oracle.decode_split(q, kc, vc, lens, scale, n_splits, min_rows)
     ro, rl = oracle.decode(q, kc, vc, lens, scale)
     check_lse(pl.cpu().numpy(), rpl, "part_lse")

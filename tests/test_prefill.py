@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import oracle
-from attn_forward_tcgen05_gb300 import prefill
+from attn_forward_tcgen05_gb300 import prefill, sync_check
 from attn_forward_tcgen05_gb300 import workloads as W
 from tests.tolerances import check_lse, check_o
 
@@ -20,7 +20,7 @@ pytestmark = pytest.mark.gpu
 
 def _run(q, k, v, causal, scale, out_dtype):
     o, lse = prefill(q.cuda(), k.cuda(), v.cuda(), causal=causal, scale=scale, out_dtype=out_dtype)
-    torch.cuda.synchronize()
+    sync_check()  # a bounded pipeline wait that ran out would surface here
     return o.float().cpu().numpy(), lse.cpu().numpy()
 
 
@@ -94,7 +94,7 @@ def _full_size(shape: W.PrefillShape, out_dtype, n_random=40):
     q, k, v = W.prefill_inputs_for(shape)
     o, lse = prefill(q.cuda(), k.cuda(), v.cuda(), causal=shape.causal, scale=shape.scale,
                      out_dtype=out_dtype)
-    torch.cuda.synchronize()
+    sync_check()
     rows = _sample_rows(shape.B, shape.Hq, shape.Sq, n_random, shape.seed)
     ro, rl = oracle.sdpa_rows(q, k, v, shape.causal, shape.scale, rows)
     idx_b = torch.tensor([r[0] for r in rows])
@@ -115,3 +115,10 @@ def test_gqa_prefill_3314_sampled(out_dtype):
 @pytest.mark.parametrize("d", [64, 128, 256])
 def test_mha_noncausal_4096_sampled(d):
     _full_size(W.mha_sweep(d), torch.bfloat16, n_random=24)
+
+
+def test_many_heads_long_kv_d256():
+    # 148 query tiles of 128 rows against 64 KV tiles each, with KV rows 75 KB apart
+    shape = W.PrefillShape("d256_h148_kv8192", 1, 148, 148, 128, 8192, 256, False,
+                           1.0 / 16.0, "bf16", 77)
+    _full_size(shape, torch.bfloat16, n_random=16)
