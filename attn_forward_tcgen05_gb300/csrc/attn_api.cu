@@ -152,8 +152,8 @@ int attn_decode_split(const attn_bf16_t* q, const attn_bf16_t* kcache, const att
   a.n_splits = n_splits; a.min_rows = min_rows_per_split; a.scale = scale;
   a.err = err_word();
   if (a.err == nullptr) return ATTN_ERR_CUDA;
-  int rc = encode_bf16_4d(&a.tm_k, kcache, d, Hkv, max_kv, B, attn::kDecodeTileRows);
-  if (rc == ATTN_OK) rc = encode_bf16_4d(&a.tm_v, vcache, d, Hkv, max_kv, B, attn::kDecodeTileRows);
+  int rc = encode_bf16_4d(&a.tm_k, kcache, d, Hkv, max_kv, B, attn::kDecodeStageRows);
+  if (rc == ATTN_OK) rc = encode_bf16_4d(&a.tm_v, vcache, d, Hkv, max_kv, B, attn::kDecodeStageRows);
   if (rc != ATTN_OK) return rc;
   return from_cuda(attn::launch_decode_split(a, reinterpret_cast<cudaStream_t>(stream)));
 }

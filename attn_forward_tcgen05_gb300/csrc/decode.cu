@@ -7,21 +7,28 @@
 // running max, a running sum and a running O, and rescales both by
 // exp(m_old - m_new) when the max grows.  Section 2.2 of that page moves the
 // K and V loads ahead of the exp/shuffle dependency chain; here the same idea
-// is carried by the GB300 copy engine: one producer warp issues TMA tile loads
-// (32 rows of K and of V per stage) into a shared-memory ring, so the loads of
-// later tiles are in flight while the consumer warps work on earlier ones.
+// is carried by the GB300 copy engine: producer warps issue TMA loads (64 rows
+// of K and of V per stage) into a shared-memory ring, so the loads of later
+// stages are in flight while the consumer warps work on earlier ones.  The
+// copy engine's throughput is set by the number of boxes far more than by
+// their size (about one box per 300 cycles per SM up to 16 KB), so a stage is
+// one 64-row box per 128-byte panel: 32-row boxes capped the kernel at about
+// 14 bytes per cycle per SM, below the HBM rate.
 //
 // Work mapping: one CTA per split unit (batch, KV head, split), 6 warps.
-// Consumer warps 0..3 each own one ring stage (32 rows of K and 32 of V) and
-// take tiles w, w+4, w+8, ... of the unit for all G query heads of the group,
-// so every loaded K/V row serves all G heads.  Warp 4 streams K tiles and
-// warp 5 streams V tiles with TMA; a consumer hands its K half back right
-// after the score phase, so its next K tile loads during softmax and P.V.
+// Consumer warps 0..3 form two pairs; pair p owns ring stage p and takes the
+// stages u = p, p+2, p+4, ... of the unit, warp h of the pair the rows
+// [32h, 32h+32) of each, for all G query heads of the group, so every loaded
+// K/V row serves all G heads.  Warp 4 streams K and warp 5 streams V with
+// TMA; a pair hands its K half back right after the score phase, so its next
+// K stage loads during softmax and P.V.
 // Per tile: scores with lane = row (the head dim of that row from shared
-// memory against q, kept in shared memory in fp32, pre-multiplied by
-// scale * log2(e)), warp-shuffle max, exp2 on the MUFU, then P.V with
-// lane = d/32 dims and p broadcast from shared memory.  Both products run on
-// packed fp32 pairs (fma.f32x2).  At the end the four warps' partial
+// memory against q, kept in shared memory as bf16: every lane reads all of q
+// for every row, and shared-memory wavefronts, not HBM, were the limit with
+// an fp32 copy), scaled by scale * log2(e) once per score, warp-shuffle max,
+// exp2 on the MUFU, then P.V with lane = d/32 dims and each row's weights
+// broadcast from shared memory (a shuffle per row and head instead was about
+// 1.5x slower).  Both products run on packed fp32 pairs (fma.f32x2).  At the end the four warps' partial
 // (m, l, O) are merged through shared memory and the split's normalised O
 // and LSE are written.  Everything is fp32 on CUDA cores; no tensor cores.
 #include <cmath>
@@ -40,16 +47,20 @@ constexpr int kDecodeThreads = (kConsumerWarps + 2) * 32;  // + K producer + V p
 
 template <int D, int GMAX>
 struct DecodeCfg {
-  static constexpr int kTile = kDecodeTileRows;        // rows per stage
+  static constexpr int kTile = 32;                     // rows per consumer warp and stage
+  static constexpr int kStageRows = kDecodeStageRows;  // rows per stage (one TMA box per panel)
+  static constexpr int kWarpsPerStage = kStageRows / kTile;
+  static constexpr int kStages = kConsumerWarps / kWarpsPerStage;
   static constexpr int kPanels = D / 64;               // 128-byte swizzled panels per row
-  static constexpr int kPanelBytes = kTile * 128;      // one panel of one tile
+  static constexpr int kPanelBytes = kStageRows * 128; // one panel of one stage
   static constexpr int kKBytes = kPanels * kPanelBytes;  // the K half of a stage (V half: same)
   static constexpr int kStageBytes = 2 * kKBytes;
-  static constexpr int kRingBytes = kConsumerWarps * kStageBytes;
-  static constexpr int kQBytes = GMAX * D * 4;                             // fp32 q
+  static constexpr int kRingBytes = kStages * kStageBytes;
+  static_assert(kConsumerWarps % kWarpsPerStage == 0, "whole warp groups per stage");
+  static constexpr int kQBytes = GMAX * D * 2;                             // bf16 q [GMAX][D]
   static constexpr int kPBytes = kConsumerWarps * kTile * GMAX * 4;        // p [warp][row][g]
   static constexpr int kBarOffset = kRingBytes + kQBytes + kPBytes;
-  static constexpr int kBarBytes = 4 * kConsumerWarps * 8 + 16;  // fullK, fullV, emptyK, emptyV, abort
+  static constexpr int kBarBytes = 4 * kStages * 8 + 16;  // fullK, fullV, emptyK, emptyV, abort
   static constexpr int kSmemBytes = kBarOffset + kBarBytes + 1024;  // + align slack
   // three CTAs per SM for small head groups, two otherwise (register budget)
   static constexpr int kMinBlocks = GMAX <= 4 ? 3 : 2;
@@ -124,62 +135,59 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<D, GMAX>::kMinBlocks
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* ring = smem;                                                          // [warp] K|V
-  float* qs = reinterpret_cast<float*>(smem + C::kRingBytes);                    // [GMAX][D]
-  float* pbuf = reinterpret_cast<float*>(smem + C::kRingBytes + C::kQBytes);     // [warp][row][GMAX]
+  uint16_t* qs = reinterpret_cast<uint16_t*>(smem + C::kRingBytes);  // [GMAX][D] bf16
   uint64_t* fullK = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
-  uint64_t* fullV = fullK + kConsumerWarps;
-  uint64_t* emptyK = fullV + kConsumerWarps;
-  uint64_t* emptyV = emptyK + kConsumerWarps;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(emptyV + kConsumerWarps);
+  uint64_t* fullV = fullK + C::kStages;
+  uint64_t* emptyK = fullV + C::kStages;
+  uint64_t* emptyV = emptyK + C::kStages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(emptyV + C::kStages);
 
-  const int T = (hi - lo + C::kTile - 1) / C::kTile;  // tiles in this split
+  const int U = (hi - lo + C::kStageRows - 1) / C::kStageRows;  // stages in this split
 
   if (threadIdx.x == 0) {
-    for (int w = 0; w < kConsumerWarps; ++w) {
+    for (int w = 0; w < C::kStages; ++w) {
       mbar_init(&fullK[w], 1);
       mbar_init(&fullV[w], 1);
-      mbar_init(&emptyK[w], 1);
-      mbar_init(&emptyV[w], 1);
+      mbar_init(&emptyK[w], C::kWarpsPerStage);  // every warp of the stage's group releases it
+      mbar_init(&emptyV[w], C::kWarpsPerStage);
     }
     *abort_flag = 0;
     fence_mbar_init();
   }
-  // q of the group, fp32, pre-scaled into the log2 domain
+  // q of the group, bf16 as given; scores are scaled into the log2 domain later
   const float qscale = scale * kLog2e;
   for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
     const int g = i / D, t = i % D;
-    const uint16_t raw = q[((size_t)b * Hq + (size_t)hk * G + g) * D + t];
-    qs[g * D + t] = __uint_as_float((uint32_t)raw << 16) * qscale;
+    qs[g * D + t] = q[((size_t)b * Hq + (size_t)hk * G + g) * D + t];
   }
-  for (int i = threadIdx.x; i < (GMAX - G) * D; i += blockDim.x) qs[G * D + i] = 0.f;
+  for (int i = threadIdx.x; i < (GMAX - G) * D; i += blockDim.x) qs[G * D + i] = 0;
   __syncthreads();
 
   if (warp >= kConsumerWarps) {
     // ================= producer warps: warp 4 streams K, warp 5 streams V =================
-    // Tile t goes to consumer warp t % 4 (its (t / 4)-th use of its stage).  The
-    // whole warp runs the loop; one elected lane issues each copy.
+    // Stage u of the unit goes to ring slot u % kStages (its (u / kStages)-th
+    // use).  The whole warp runs the loop; one elected lane issues each copy.
     const bool is_k = warp == kConsumerWarps;
     const CUtensorMap* map = is_k ? &tm_k : &tm_v;
     uint64_t* fullX = is_k ? fullK : fullV;
     uint64_t* emptyX = is_k ? emptyK : emptyV;
     if (lane == 0) tma_prefetch_desc(map);
     const uint64_t pol = l2_policy_evict_first();
-    int t = 0;
-    for (; t < T; ++t) {
-      const int w = t % kConsumerWarps, k = t / kConsumerWarps;
+    int u = 0;
+    for (; u < U; ++u) {
+      const int w = u % C::kStages, k = u / C::kStages;
       if (!mbar_wait_warp(&emptyX[w], (k & 1) ^ 1, err, abort_flag)) break;
       mbar_arrive_expect_tx_e(&fullX[w], C::kKBytes);
       uint8_t* dst = ring + w * C::kStageBytes + (is_k ? 0 : C::kKBytes);
-      const int row = lo + t * C::kTile;
+      const int row = lo + u * C::kStageRows;
 #pragma unroll
       for (int p = 0; p < C::kPanels; ++p)
         tma_load_4d_hint_e(dst + p * C::kPanelBytes, map, &fullX[w], p * 64, hk, row, b, pol);
     }
-    if (t < T && lane == 0) {
+    if (u < U && lane == 0) {
       // aborted: let the copies already issued land before the CTA exits
-      for (int u = (t - kConsumerWarps > 0 ? t - kConsumerWarps : 0); u < t; ++u)
-        mbar_wait(&fullX[u % kConsumerWarps], (u / kConsumerWarps) & 1, nullptr, nullptr,
-                  100000000ull);
+      for (int v = (u - C::kStages > 0 ? u - C::kStages : 0); v < u; ++v)
+        mbar_wait(&fullX[v % C::kStages], (v / C::kStages) & 1, nullptr, nullptr, 100000000ull);
     }
     return;  // the producers take no part in the combine
   }
@@ -194,18 +202,34 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<D, GMAX>::kMinBlocks
 #pragma unroll
     for (int e = 0; e < DP2; ++e) o2[g][e] = f2pack(0.f, 0.f);
   }
-  float* pw = pbuf + warp * C::kTile * GMAX;
-  const uint8_t* kt = ring + warp * C::kStageBytes;  // this warp's stage
+  float* pw = reinterpret_cast<float*>(smem + C::kRingBytes + C::kQBytes) + warp * C::kTile * GMAX;
+  const int slot = warp / C::kWarpsPerStage;    // ring slot of this warp's group
+  const int half = warp % C::kWarpsPerStage;    // its 32 rows within each stage
+  // this warp's rows of a stage: rows [32*half, 32*half + 32) of every panel
+  const uint8_t* kt = ring + slot * C::kStageBytes + half * C::kTile * 128;
   const uint8_t* vt = kt + C::kKBytes;
 
   bool ok = true;
-  for (int i = 0, t = warp; t < T; ++i, t += kConsumerWarps) {
+  for (int i = 0, u = slot; u < U; ++i, u += C::kStages) {
     const uint32_t par = (uint32_t)i & 1u;
-    const int row0 = lo + t * C::kTile;
-    const int nrows = min(C::kTile, hi - row0);
-    if (!__all_sync(0xFFFFFFFFu, mbar_wait(&fullK[warp], par, err, abort_flag))) {
+    const int row0 = lo + u * C::kStageRows + half * C::kTile;
+    // rows of this warp in the stage: 0 for the upper half of a short last stage,
+    // which the warp still waits for and releases (the stage's barriers count it)
+    const int nrows = max(0, min(C::kTile, hi - row0));
+    if (!__all_sync(0xFFFFFFFFu, mbar_wait(&fullK[slot], par, err, abort_flag))) {
       ok = false;
       break;
+    }
+    if (nrows == 0) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&emptyK[slot]);
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&fullV[slot], par, err, abort_flag))) {
+        ok = false;
+        break;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&emptyV[slot]);
+      continue;
     }
 
     // ---- scores: lane = row; fp32 pairs along the head dim ----
@@ -222,27 +246,27 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<D, GMAX>::kMinBlocks
 #pragma unroll
       for (int g = 0; g < GMAX; ++g) {
         if (g < G) {
-          const ulonglong2 qa = *reinterpret_cast<const ulonglong2*>(qs + g * D + c * 8);
-          const ulonglong2 qb = *reinterpret_cast<const ulonglong2*>(qs + g * D + c * 8 + 4);
+          const uint4 qv = *reinterpret_cast<const uint4*>(qs + g * D + c * 8);  // 8 bf16, broadcast
           uint64_t a = acc[g];
-          a = fma2(qa.x, k01, a);
-          a = fma2(qa.y, k23, a);
-          a = fma2(qb.x, k45, a);
-          a = fma2(qb.y, k67, a);
+          a = fma2(bf16x2_to_f2(qv.x), k01, a);
+          a = fma2(bf16x2_to_f2(qv.y), k23, a);
+          a = fma2(bf16x2_to_f2(qv.z), k45, a);
+          a = fma2(bf16x2_to_f2(qv.w), k67, a);
           acc[g] = a;
         }
       }
     }
-    // the K half of the stage is no longer needed: the K producer may refill it
+    // the K half of the stage is no longer needed by this warp: once both warps of
+    // the group are done the K producer may refill it
     __syncwarp();
-    if (lane == 0) mbar_arrive(&emptyK[warp]);
+    if (lane == 0) mbar_arrive(&emptyK[slot]);
     const bool valid = lane < nrows;
 
     // ---- online softmax per query head (log2 domain) ----
 #pragma unroll
     for (int g = 0; g < GMAX; ++g) {
       if (g < G) {
-        const float sv = valid ? f2sum(acc[g]) : -INFINITY;
+        const float sv = valid ? f2sum(acc[g]) * qscale : -INFINITY;
         const float tmax = warp_max(sv);  // finite: every tile has >= 1 valid row
         const float m_new = fmaxf(m[g], tmax);
         const float corr = ex2_approx(m[g] - m_new);  // m = -inf -> 0
@@ -256,7 +280,7 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<D, GMAX>::kMinBlocks
       }
     }
     __syncwarp();
-    if (!__all_sync(0xFFFFFFFFu, mbar_wait(&fullV[warp], par, err, abort_flag))) {
+    if (!__all_sync(0xFFFFFFFFu, mbar_wait(&fullV[slot], par, err, abort_flag))) {
       ok = false;
       break;
     }
@@ -299,7 +323,7 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<D, GMAX>::kMinBlocks
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&emptyV[warp]);
+    if (lane == 0) mbar_arrive(&emptyV[slot]);
   }
 
   // ---- combine the consumer warps' partials through shared memory ----

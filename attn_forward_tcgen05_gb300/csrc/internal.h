@@ -20,7 +20,7 @@ struct PrefillArgs {
 
 // Decode-split launch description.
 struct DecodeArgs {
-  CUtensorMap tm_k, tm_v;  // 4-D maps {d, Hkv, max_kv, B}, box {64, 1, 32, 1}, 128B swizzle
+  CUtensorMap tm_k, tm_v;  // 4-D maps {d, Hkv, max_kv, B}, box {64, 1, kDecodeStageRows, 1}, 128B swizzle
   const uint16_t* q;       // [B][Hq][d] bf16
   const int* kv_lens;      // [B]
   float* part_o;           // [B][Hq][n_splits][d]
@@ -38,8 +38,9 @@ struct MergeArgs {
   int B, Hq, n_splits, d, o_bf16;
 };
 
-// Rows of a KV tile streamed by the decode producer per pipeline stage.
-constexpr int kDecodeTileRows = 32;
+// Rows of a K / V stage loaded by one TMA box in the decode kernel (two
+// consumer warps share a stage, 32 rows each).
+constexpr int kDecodeStageRows = 64;
 // Rows of a Q tile in the prefill kernel, and of one TMA-loaded K / V stage
 // (the kernel may compute on sub-tiles of a stage).
 constexpr int kPrefillTileM = 128;

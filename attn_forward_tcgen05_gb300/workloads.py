@@ -14,7 +14,8 @@ Workloads (names used throughout the tests and the benchmark):
                         8 splits (min 1 row per split), merged to O bf16 + LSE fp32
 * ``mha_noncausal_4096_d{64,128,256}``  B=2, Hq=Hkv=16, S=4096, non-causal, scale 1/sqrt(d)
 * ``ragged_gqa_decode_b64`` B=64, Hq=32, Hkv=8, d=128, KV lengths ~ U[512, 8192],
-                        16 splits with at least 512 rows each, O bf16 + LSE fp32
+                        at most 8 splits of at least 1024 rows each (1 to 8 per
+                        sequence, chosen by its length), O bf16 + LSE fp32
 """
 from __future__ import annotations
 
@@ -67,8 +68,8 @@ def mha_sweep(d: int) -> PrefillShape:
                         1.0 / math.sqrt(float(d)), "bf16", 1000 + 4 * 10 + d // 64)
 
 
-RAGGED_DECODE = DecodeShape("ragged_gqa_decode_b64", 64, 32, 8, 128, 1.0 / math.sqrt(128.0), 16,
-                            512, 1005, len_range=(512, 8192))
+RAGGED_DECODE = DecodeShape("ragged_gqa_decode_b64", 64, 32, 8, 128, 1.0 / math.sqrt(128.0), 8,
+                            1024, 1005, len_range=(512, 8192))
 
 
 def _gen(seed: int) -> torch.Generator:

@@ -59,6 +59,14 @@ def test_ragged_b64_full():
     _compare(q, kc, vc, lens, s.n_splits, s.min_rows_per_split, s.scale)
 
 
+def test_ragged_b64_sixteen_splits():
+    # the same batch split finer: 16 splits of at least 512 rows, so short
+    # sequences leave up to 15 empty splits that the merge must skip
+    s = W.RAGGED_DECODE
+    q, kc, vc, lens = W.decode_inputs_for(s)
+    _compare(q, kc, vc, lens, 16, 512, s.scale)
+
+
 def test_merge_random_partials():
     rng = np.random.default_rng(2)
     B, Hq, S, d = 3, 5, 7, 128
