@@ -123,10 +123,10 @@ int attn_prefill_fwd(const attn_bf16_t* q, const attn_bf16_t* k, const attn_bf16
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (Skv == 0) return from_cuda(attn::launch_prefill_empty_kv(a, s));
   int rc = encode_bf16_4d(&a.tm_q, q, d, Hq, Sq, B, attn::kPrefillTileM);
-  if (rc == ATTN_OK) rc = encode_bf16_4d(&a.tm_k, k, d, Hkv, Skv, B, attn::kPrefillKVStageRows);
+  if (rc == ATTN_OK) rc = encode_bf16_4d(&a.tm_k, k, d, Hkv, Skv, B, attn::prefill_k_box_rows(d));
   if (rc == ATTN_OK) rc = encode_bf16_4d(&a.tm_v, v, d, Hkv, Skv, B, attn::kPrefillKVStageRows);
   if (rc != ATTN_OK) return rc;
-  return from_cuda(attn::launch_prefill(a, s));
+  return from_cuda(attn::prefill_uses_pair(d) ? attn::launch_prefill_pair(a, s) : attn::launch_prefill(a, s));
 }
 
 int attn_decode_split(const attn_bf16_t* q, const attn_bf16_t* kcache, const attn_bf16_t* vcache,

@@ -10,7 +10,8 @@ namespace attn {
 // Prefill launch description (already validated by the C-ABI layer).
 struct PrefillArgs {
   CUtensorMap tm_q, tm_k, tm_v;  // 4-D maps {d, H, S, B}, box {64, 1, rows, 1}, 128B swizzle:
-                                 // rows = kPrefillTileM for Q, kPrefillKVStageRows for K, V
+                                 // rows = kPrefillTileM for Q, prefill_k_box_rows(d) for K,
+                                 // kPrefillKVStageRows for V
   void* o;                       // [B][Sq][Hq][d], fp32 or bf16
   float* lse;                    // [B][Hq][Sq]
   int B, Hq, Hkv, Sq, Skv, d, causal, o_bf16;
@@ -45,8 +46,19 @@ constexpr int kDecodeStageRows = 64;
 // (the kernel may compute on sub-tiles of a stage).
 constexpr int kPrefillTileM = 128;
 constexpr int kPrefillKVStageRows = 128;
+// Head dims served by the CTA-pair kernel (prefill_pair.cu); there each CTA
+// loads 64 of the 128 K rows of a tile, so the K map's box is 64 rows high.
+// d = 256 runs faster on pairs (1.6 PFLOP/s against 1.24 on the head-dim
+// sweep); d = 128 runs faster on single CTAs with two query tiles, so its pair
+// instantiation is built only when ATTN_PREFILL_PAIR_D128 is defined to 1.
+#ifndef ATTN_PREFILL_PAIR_D128
+#define ATTN_PREFILL_PAIR_D128 0
+#endif
+constexpr bool prefill_uses_pair(int d) { return d == 256 || (ATTN_PREFILL_PAIR_D128 && d == 128); }
+constexpr int prefill_k_box_rows(int d) { return prefill_uses_pair(d) ? kPrefillKVStageRows / 2 : kPrefillKVStageRows; }
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
+cudaError_t launch_prefill_pair(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill_empty_kv(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_decode_split(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);

@@ -1,4 +1,7 @@
-// prefill.cu -- exact attention forward (FMHA) on the 5th-generation tensor cores.
+// prefill.cu -- exact attention forward (FMHA) on the 5th-generation tensor cores,
+// one CTA per query block: used for head dims 64 and 128 (head dim 256 runs on
+// CTA pairs, prefill_pair.cu; the d = 256 configuration below is kept for
+// comparison and is not launched).
 //
 // Per CTA: NQ query tiles of 128 rows of one (batch, query head), streamed
 // against K/V tiles of BN = 128 rows of the matching KV head, which arrive by
@@ -610,7 +613,6 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   switch (a.d) {
     case 64: return launch_prefill_t<64>(a, stream);
     case 128: return launch_prefill_t<128>(a, stream);
-    case 256: return launch_prefill_t<256>(a, stream);
     default: return cudaErrorInvalidValue;
   }
 }

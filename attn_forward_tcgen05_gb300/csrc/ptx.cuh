@@ -336,6 +336,137 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, u
   return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, err, abort));
 }
 
+// ---------------------------------------------------------------- CTA pairs
+// Two CTAs of a cluster (ranks 0 and 1) share one tcgen05 MMA of M = 256: each
+// holds 128 rows of A (in its own shared memory or TMEM) and half of the N
+// columns of B (rank 0 the first half), and receives its 128 rows of D in its
+// own TMEM.  Rank 0 issues the MMAs; completion is multicast to both CTAs'
+// mbarriers at the same shared-memory offset.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of both CTAs: release this CTA's prior writes, wait for the peer.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Shared::cluster address of the variable at `local_addr` in CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t local_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_addr), "r"(rank));
+  return r;
+}
+
+// Arrive on an mbarrier of another CTA of the cluster.  Default semantics
+// (release at CTA scope): the data the arrival announces lives in this CTA's
+// TMEM and is ordered by tcgen05.wait::st and the tcgen05 fences, not by the
+// memory model; a cluster-scope release instead costs a cluster-wide fence per
+// arrival (measured: the pair kernel ran at 2/3 of the speed).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// Bounded wait with acquire at cluster scope: for barriers that receive arrivals
+// from the peer CTA (remote arrives, multicast commits, the peer's TMA bytes).
+__device__ __forceinline__ bool mbar_wait_cl(uint64_t* bar, uint32_t parity, uint32_t* err,
+                                             volatile int* abort,
+                                             uint64_t limit_ns = ATTN_WAIT_LIMIT_NS) {
+  const uint32_t a = smem_u32(bar);
+  auto try_once = [&]() -> bool {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(a), "r"(parity), "r"(ATTN_TRY_WAIT_HINT_NS)
+        : "memory");
+    return ok != 0;
+  };
+  if (try_once()) return true;
+  const long long t0 = clock64();
+  const long long limit_cycles = (long long)(limit_ns * kMaxSmClockGHz);
+  for (uint32_t n = 1;; ++n) {
+    if (try_once()) return true;
+    if ((n & 63u) == 0) {
+      if (abort != nullptr && *abort) return false;
+      if (clock64() - t0 > limit_cycles) {
+        if (err) atomicCAS(err, kErrNone, kErrWaitTimeout);
+        if (abort) *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ bool mbar_wait_cl_warp(uint64_t* bar, uint32_t parity, uint32_t* err,
+                                                  volatile int* abort) {
+  return __all_sync(0xFFFFFFFFu, mbar_wait_cl(bar, parity, err, abort));
+}
+
+// TMEM allocation for a CTA pair: one warp of each CTA executes these together.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* smem_result, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(smem_result)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// Pair MMAs (elected lane of a lock-step warp of rank 0).
+__device__ __forceinline__ void mma2_ss_e(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma2_ts_e(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Completion of this thread's prior pair MMAs arrives on `bar` in both CTAs.
+__device__ __forceinline__ void mma2_commit_both_e(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+      "h"((uint16_t)3)
+      : "memory");
+}
+
+// TMA load into this CTA's shared memory whose bytes complete on an mbarrier
+// of either CTA of the pair (`bar_cluster` from mapa_shared).
+__device__ __forceinline__ void tma_load_4d_pair_e(void* smem_dst, const CUtensorMap* map,
+                                                   uint32_t bar_cluster, int c0, int c1, int c2,
+                                                   int c3) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];\n\t}" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+
 // ---------------------------------------------------------------- descriptors
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading and
 // stride byte offsets (both >> 4), fixed version bits 46-48 = 0b001, swizzle

@@ -118,7 +118,7 @@ def run_ours(args, rank, world, local_rank):
     attn.load()  # fails loudly if the CUDA library is missing
     peaks, peak_src = load_peaks()
 
-    P = W.GQA_PREFILL
+    P = prefill_workload(args.prefill_workload)
     D3 = W.GQA_DECODE
     D5 = W.RAGGED_DECODE
     # inputs resident in HBM before the timed region
@@ -227,16 +227,17 @@ def run_ours(args, rank, world, local_rank):
     traffic = load_traffic()
     # one roofline per hot kernel; the top-level one is the kernel that takes the
     # largest share of the step's device time
-    prefill_roof = {"bound": "tensor", "kernel": "fmha_fwd_kernel<128>", "workload": P.name,
+    pkern = f"fmha_pair_kernel<{P.d}>" if P.d == 256 else f"fmha_fwd_kernel<{P.d}>"
+    prefill_roof = {"bound": "tensor", "kernel": pkern, "workload": P.name,
                     "achieved": round(prefill_tflops / world, 2), "peak": peak_tc,
                     "unit": "TFLOP/s", "frac": round(prefill_tflops / world / peak_tc, 4),
-                    "traffic": traffic.get("fmha_fwd_kernel<128>"),
+                    "traffic": traffic.get(f"{pkern} {P.name}"),
                     "step_share": round(t_prefill / ms_step, 4),
                     "peak_source": f"bf16_tflops (burst) of {peak_src}"}
     decode_roof = {"bound": "hbm", "kernel": "decode_split_kernel<128,4>", "workload": D5.name,
                    "achieved": round(split_gbs, 1), "peak": peak_hbm, "unit": "GB/s",
                    "frac": round(split_gbs / peak_hbm, 4),
-                   "traffic": traffic.get("decode_split_kernel<128,4>"),
+                   "traffic": traffic.get(f"decode_split_kernel<128,4> {D5.name}"),
                    "step_share": round(t_split5 / ms_step, 4),
                    "peak_source": f"hbm_gbs of {peak_src}"}
     if not do_decode:
@@ -351,6 +352,18 @@ def run_e2e(args, attn, W, dev, stream, P, dec, flops):
             "note": "pinned host buffers; H2D of all inputs and D2H of O and LSE inside the timed region"}
 
 
+def prefill_workload(name: str):
+    """The prefill workload of the step: gqa_prefill_3314 by default; the head-dim
+    sweep shapes are selectable for profiling their kernels."""
+    from attn_forward_tcgen05_gb300 import workloads as W
+    shapes = {W.GQA_PREFILL.name: W.GQA_PREFILL}
+    for d in (64, 128, 256):
+        shapes[W.mha_sweep(d).name] = W.mha_sweep(d)
+    if name not in shapes:
+        raise SystemExit(f"unknown prefill workload {name!r}; one of {sorted(shapes)}")
+    return shapes[name]
+
+
 def load_traffic():
     """DRAM bytes per launch from the committed ncu summary, if present."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
@@ -432,6 +445,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--only", choices=("prefill", "decode"), default=None,
                     help="time only one part of the step (profiling runs)")
+    ap.add_argument("--prefill-workload", default="gqa_prefill_3314",
+                    help="prefill workload of the step (the head-dim sweep shapes are for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -9,8 +9,8 @@ two phases more (the parity would then alias and the wait would never end).
 This model restates each role's sequence of waits, arrivals and commits in
 the kernel's order -- rings of K and V stages holding SUB KV tiles each
 (waited for at their first tile, released after their last), two S buffers
-per query tile with one S and one P barrier each (or one S buffer), the O
-and final barriers; per KV tile j the MMA warp issues S(j+1) for every query
+per query tile with one S and one P barrier each (or one S buffer; or three
+with S(j+2) issued ahead and two O barriers), the O and final barriers; per KV tile j the MMA warp issues S(j+1) for every query
 tile, then P(j).V(j) for every query tile (with one S buffer: P_t(j).V(j)
 then S_t(j+1), tile by tile) -- and runs it against exact mbarrier semantics with random TMA, MMA and
 softmax latencies, including the optional O rescale.  It checks every wait
@@ -52,7 +52,7 @@ class Bar:
         return (self.done & 1) != parity
 
 
-def simulate(NQ, SK, SV, n_t, seed, p_per_buffer=True, NS=2, SUB=1):
+def simulate(NQ, SK, SV, n_t, seed, p_per_buffer=True, NS=2, SUB=1, LOOK=1, NO=1):
     """Run one randomised schedule; raises AssertionError on an unsound wait or a deadlock.
 
     p_per_buffer=False keys the P barriers by query tile only (one barrier shared
@@ -71,6 +71,10 @@ def simulate(NQ, SK, SV, n_t, seed, p_per_buffer=True, NS=2, SUB=1):
 
     def p_use(j):
         return j // NS if p_per_buffer else j
+
+    # NO O barriers, P(j).V(j) completing on barrier j % NO (its (j // NO)-th phase)
+    def o_bar(t, j):
+        return bar(("O", t, j % NO))
 
     n = max(n_t)
     n_st = (n + SUB - 1) // SUB
@@ -101,7 +105,7 @@ def simulate(NQ, SK, SV, n_t, seed, p_per_buffer=True, NS=2, SUB=1):
         tma(bar("q"), 1)
         jk = jv = 0
         while jv < n_st:
-            if jk < n_st and jk * SUB <= jv * SUB + 1:
+            if jk < n_st and jk * SUB <= jv * SUB + LOOK:
                 s, u = jk % SK, jk // SK
                 if u > 0:
                     yield wait(bar(("eK", s)), (u & 1) ^ 1, u - 1)
@@ -132,7 +136,7 @@ def simulate(NQ, SK, SV, n_t, seed, p_per_buffer=True, NS=2, SUB=1):
         yield wait(p_bar(t, j % NS), use & 1, use)
         for _ in range(4):
             mma(rng.randint(20, 80))
-        commit(bar(("O", t)))
+        commit(o_bar(t, j))
         if j == n_t[t] - 1:
             commit(bar(("Fin", t)))
 
@@ -144,8 +148,21 @@ def simulate(NQ, SK, SV, n_t, seed, p_per_buffer=True, NS=2, SUB=1):
                 issue_s(t, 0)
         if last(0):
             commit(bar(("eK", 0)))
+        # with LOOK > 1 (one query tile, NS = LOOK + 1 S buffers) the prologue also
+        # issues S(1) .. S(LOOK - 1); the loop then issues S(j + LOOK) before P(j).V(j)
+        for jj in range(1, LOOK):
+            if jj < n:
+                st = jj // SUB
+                sn, un = st % SK, st // SK
+                if first(jj):
+                    yield wait(bar(("fK", sn)), un & 1, un)
+                for t in range(NQ):
+                    if jj < n_t[t]:
+                        issue_s(t, jj)
+                if last(jj):
+                    commit(bar(("eK", sn)))
         for j in range(n):
-            jn = j + 1
+            jn = j + LOOK
             if NS == 1:
                 # one S buffer per tile: P_t(j).V(j), then S_t(j+1), tile by tile
                 st = j // SUB
@@ -194,7 +211,8 @@ def simulate(NQ, SK, SV, n_t, seed, p_per_buffer=True, NS=2, SUB=1):
             yield wait(bar(("S", t, buf)), use & 1, use)
             yield ("sleep", rng.randint(20, 400))
             if j > 0 and rng.random() < 0.3:  # O rescale needs the previous P.V done
-                yield wait(bar(("O", t)), (j - 1) & 1, j - 1)
+                u = (j - 1) // NO
+                yield wait(o_bar(t, j - 1), u & 1, u)
                 yield ("sleep", rng.randint(20, 200))
             for _ in range(4):  # one arrival per softmax warp
                 p_bar(t, buf).arrive()
@@ -247,6 +265,8 @@ CASES = [
     (2, 2, 2, 2, (1, 1)),
     (2, 2, 2, 2, (1, 2)),
     (2, 2, 1, 1, (7, 8)),    # single-stage rings
+    (1, 1, 3, 3, (11,)),     # CTA-pair kernel, d = 128: 3-stage rings
+    (1, 1, 2, 2, (11,)),     # CTA-pair kernel, d = 256
     (1, 1, 1, 1, (9,)),      # d = 256
     (1, 1, 1, 1, (1,)),
     (1, 1, 1, 1, (2,)),
@@ -266,6 +286,37 @@ CASES_ONE_S = [
 def test_prefill_protocol_is_sound(NQ, SUB, SK, SV, n_t):
     for seed in range(120):
         simulate(NQ, SK, SV, list(n_t), seed, SUB=SUB)
+
+
+CASES_LOOKAHEAD = [
+    # CTA-pair kernel, d = 128: three S buffers, S(j+2) issued before P(j).V(j)
+    # query tiles, K stages, V stages, KV tiles
+    (1, 3, 3, (11,)),
+    (1, 3, 3, (1,)),
+    (1, 3, 3, (2,)),
+    (1, 3, 3, (3,)),
+    (1, 2, 2, (7,)),
+    (1, 1, 1, (5,)),
+]
+
+
+@pytest.mark.parametrize("NQ,SK,SV,n_t", CASES_LOOKAHEAD, ids=[str(c) for c in CASES_LOOKAHEAD])
+def test_prefill_protocol_three_s_buffers_is_sound(NQ, SK, SV, n_t):
+    for seed in range(120):
+        simulate(NQ, SK, SV, list(n_t), seed, NS=3, LOOK=2, NO=2)
+
+
+def test_three_s_buffers_with_one_o_barrier_is_unsound():
+    """With S(j+2) issued before P(j).V(j), the softmax of tile j can find
+    P(j-2).V(j-2) still running; one O barrier would then be two phases behind
+    the rescale's wait for P(j-1).V(j-1).  The model must catch this form."""
+    failures = 0
+    for seed in range(200):
+        try:
+            simulate(1, 3, 3, [11], seed, NS=3, LOOK=2, NO=1)
+        except AssertionError:
+            failures += 1
+    assert failures > 0
 
 
 @pytest.mark.parametrize("NQ,SUB,SK,SV,n_t", CASES_ONE_S, ids=[str(c) for c in CASES_ONE_S])
