@@ -49,6 +49,7 @@ def load(path: str | None = None):
         lib = ctypes.CDLL(p)
         vp, i, f, ull = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_ulonglong
         lib.attn_prefill_fwd.argtypes = [vp, vp, vp, vp, vp] + [i] * 7 + [f, i, vp]
+        lib.attn_prefill_varlen.argtypes = [vp] * 7 + [i] * 8 + [f, i, vp]
         lib.attn_decode_split.argtypes = [vp, vp, vp, vp] + [i] * 5 + [f, i, i, vp, vp, vp]
         lib.attn_merge.argtypes = [vp, vp, vp, vp] + [i] * 5 + [vp]
         lib.attn_sync_check.argtypes = [vp]
@@ -59,7 +60,8 @@ def load(path: str | None = None):
         lib.attn_decode_noalloc.argtypes = [vp, vp, vp, vp] + [i] * 5 + [f, i, i, vp, vp, i, vp]
         lib.attn_decode_noalloc_scratch_bytes.argtypes = []
         lib.attn_decode_noalloc_scratch_bytes.restype = ull
-        for name in ("attn_prefill_fwd", "attn_decode_split", "attn_merge", "attn_sync_check",
+        for name in ("attn_prefill_fwd", "attn_prefill_varlen", "attn_decode_split", "attn_merge",
+                     "attn_sync_check",
                      "attn_version", "attn_debug_wait_timeout", "attn_decode_noalloc"):
             getattr(lib, name).restype = i
         _lib = lib
@@ -70,6 +72,13 @@ def load(path: str | None = None):
 def attn_prefill_fwd(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, d, causal, scale, o_dtype, stream) -> int:
     return load().attn_prefill_fwd(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, d, int(causal),
                                    float(scale), o_dtype, stream)
+
+
+def attn_prefill_varlen(q, kcache, vcache, o, lse, cu_seqlens_q, kv_lens, B, Hq, Hkv, total_q,
+                        max_sq, max_kv, d, causal, scale, o_dtype, stream) -> int:
+    return load().attn_prefill_varlen(q, kcache, vcache, o, lse, cu_seqlens_q, kv_lens, B, Hq, Hkv,
+                                      total_q, max_sq, max_kv, d, int(causal), float(scale), o_dtype,
+                                      stream)
 
 
 def attn_decode_split(q, kcache, vcache, kv_lens, B, Hq, Hkv, d, max_kv, scale, n_splits,
@@ -167,6 +176,39 @@ def prefill(q, k, v, causal: bool = True, scale: float | None = None, out_dtype=
                           causal, scale, _out_code(o.dtype), _stream_handle(stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_prefill_fwd")
+    return o, lse
+
+
+def prefill_varlen(q, kcache, vcache, cu_seqlens_q, kv_lens, max_sq: int, causal: bool = True,
+                   scale: float | None = None, out_dtype=None, stream=None, out=None):
+    """Packed variable-length prefill against a KV cache (chunked prefill).
+
+    q [total_q,Hq,d] bf16 (sequences concatenated), kcache/vcache [B,max_kv,Hkv,d] bf16,
+    cu_seqlens_q int32 [B+1] and kv_lens int32 [B] on the GPU; max_sq >= the longest
+    sequence.  Returns (o [total_q,Hq,d] in out_dtype (default bf16), lse [Hq,total_q] fp32)."""
+    torch = _torch()
+    out_dtype = out_dtype or torch.bfloat16
+    _check_tensor(q, "q", torch.bfloat16, 3)
+    _check_tensor(kcache, "kcache", torch.bfloat16, 4)
+    _check_tensor(vcache, "vcache", torch.bfloat16, 4)
+    _check_tensor(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
+    _check_tensor(kv_lens, "kv_lens", torch.int32, 1)
+    total_q, Hq, d = q.shape
+    B, max_kv, Hkv, _ = kcache.shape
+    if cu_seqlens_q.numel() != B + 1 or kv_lens.numel() != B:
+        raise ValueError("cu_seqlens_q must have B+1 entries and kv_lens B")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        o = torch.empty((total_q, Hq, d), dtype=out_dtype, device=q.device)
+        lse = torch.empty((Hq, total_q), dtype=torch.float32, device=q.device)
+    else:
+        o, lse = out
+    rc = attn_prefill_varlen(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(o), _ptr(lse),
+                             _ptr(cu_seqlens_q), _ptr(kv_lens), B, Hq, Hkv, total_q, int(max_sq),
+                             max_kv, d, causal, scale, _out_code(o.dtype), _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_prefill_varlen")
     return o, lse
 
 

@@ -8,6 +8,11 @@
 namespace attn {
 
 // Prefill launch description (already validated by the C-ABI layer).
+// Fixed-length batches: cu_q == nullptr, q/o [B][Sq][Hq][d], k/v [B][Skv][Hkv][d],
+// lse [B][Hq][Sq].  Packed variable-length batches (cu_q != nullptr): sequence b
+// has rows [cu_q[b], cu_q[b+1]) of q/o [total_q][Hq][d] and lse [Hq][total_q]; its
+// keys are rows [0, kv_lens[b]) of k/v [B][Skv][Hkv][d] (Skv = the cache's
+// max_kv); Sq is the longest sequence (it sizes the grid).
 struct PrefillArgs {
   CUtensorMap tm_q, tm_k, tm_v;  // 4-D maps {d, H, S, B}, box {64, 1, rows, 1}, 128B swizzle:
                                  // rows = kPrefillTileM for Q, prefill_k_box_rows(d) for K,
@@ -17,7 +22,36 @@ struct PrefillArgs {
   int B, Hq, Hkv, Sq, Skv, d, causal, o_bf16;
   float scale;
   uint32_t* err;                 // device error word
+  const int* cu_q;               // [B+1] packed query offsets, or nullptr
+  const int* kv_lens;            // [B] keys per sequence (varlen only)
+  int total_q;                   // rows of the packed q (varlen only)
 };
+
+#ifdef __CUDACC__
+// Extent of sequence b inside one prefill launch (see PrefillArgs).
+struct SeqExtent {
+  int Sq, Skv;     // query rows and keys of this sequence
+  int qbase;       // first row of this sequence in q / o / lse
+  int bq;          // batch coordinate of the q map and of the o / lse slabs
+  long long rows;  // rows per batch slab of o / lse
+};
+__device__ __forceinline__ SeqExtent seq_extent(int b, int Sq, int Skv, const int* cu_q,
+                                                const int* kv_lens, int total_q) {
+  SeqExtent e;
+  if (cu_q == nullptr) {
+    e.Sq = Sq; e.Skv = Skv; e.qbase = 0; e.bq = b; e.rows = Sq;
+    return e;
+  }
+  // offsets and lengths are clamped to the buffers the caller described
+  int c0 = cu_q[b], c1 = cu_q[b + 1];
+  c0 = c0 < 0 ? 0 : (c0 > total_q ? total_q : c0);
+  c1 = c1 < c0 ? c0 : (c1 > total_q ? total_q : c1);
+  int kl = kv_lens[b];
+  kl = kl < 0 ? 0 : (kl > Skv ? Skv : kl);
+  e.Sq = min(c1 - c0, Sq); e.Skv = kl; e.qbase = c0; e.bq = 0; e.rows = total_q;
+  return e;
+}
+#endif
 
 // Decode-split launch description.
 struct DecodeArgs {
@@ -53,6 +87,9 @@ constexpr int kPrefillKVStageRows = 128;
 // instantiation is built only when ATTN_PREFILL_PAIR_D128 is defined to 1.
 #ifndef ATTN_PREFILL_PAIR_D128
 #define ATTN_PREFILL_PAIR_D128 0
+#endif
+#ifndef ATTN_PREFILL_PAIR_D128_SLICES
+#define ATTN_PREFILL_PAIR_D128_SLICES 1
 #endif
 constexpr bool prefill_uses_pair(int d) { return d == 256 || (ATTN_PREFILL_PAIR_D128 && d == 128); }
 constexpr int prefill_k_box_rows(int d) { return prefill_uses_pair(d) ? kPrefillKVStageRows / 2 : kPrefillKVStageRows; }

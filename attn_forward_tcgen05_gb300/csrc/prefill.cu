@@ -154,20 +154,24 @@ template <int D>
 __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
     fmha_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, void* __restrict__ o_ptr,
-                    float* __restrict__ lse_ptr, int Hq, int Hkv, int Sq, int Skv, int causal,
-                    int o_bf16, float scale, int n_units_per_head_batch, uint32_t* err) {
+                    float* __restrict__ lse_ptr, int Hq, int Hkv, int Sq_max, int Skv_max, int causal,
+                    int o_bf16, float scale, int n_units_per_head_batch, uint32_t* err,
+                    const int* __restrict__ cu_q, const int* __restrict__ kv_lens, int total_q) {
   using C = PrefillCfg<D>;
   constexpr int NQ = C::NQ, NS = C::NS, BN = C::BN;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // ---- work unit: longest causal work first ----
   const int HB = n_units_per_head_batch;  // Hq * B
-  const int n_blocks_q = (Sq + NQ * kPrefillTileM - 1) / (NQ * kPrefillTileM);
+  const int n_blocks_q = (Sq_max + NQ * kPrefillTileM - 1) / (NQ * kPrefillTileM);
   const int u = blockIdx.x;
   const int qb = causal ? (n_blocks_q - 1 - u / HB) : (u / HB);
   const int hb = u % HB;
   const int hq = hb % Hq, b = hb / Hq;
   const int hk = hq / (Hq / Hkv);
+  // this sequence's query rows and keys (fixed-length or packed varlen batch)
+  const SeqExtent ext = seq_extent(b, Sq_max, Skv_max, cu_q, kv_lens, total_q);
+  const int Sq = ext.Sq, Skv = ext.Skv;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -248,7 +252,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
 #pragma unroll
           for (int p = 0; p < C::kPanels; ++p)
             tma_load_4d_e(sQ + t * C::kQTileBytes + p * C::kQPanelBytes, &tm_q, bar_q, p * 64, hq,
-                          ti[t].q0, b);
+                          ext.qbase + ti[t].q0, ext.bq);
         }
       }
       // Stages of kSub KV tiles.  The MMA warp takes the K stage of tile j+1
@@ -533,7 +537,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
     const float inv_l = have ? 1.f / l_rnd : 0.f;
     const bool row_ok = qrow < Sq;
     const uint32_t o_addr = lane_addr + C::o_col(t);
-    const size_t orow = ((size_t)b * Sq + (size_t)(row_ok ? qrow : 0)) * Hq + hq;
+    const size_t orow = ((size_t)ext.bq * ext.rows + ext.qbase + (size_t)(row_ok ? qrow : 0)) * Hq + hq;
 #pragma unroll
     for (int c0 = 0; c0 < D; c0 += 32) {
       uint32_t ov[32];
@@ -567,7 +571,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
       }
     }
     if (row_ok && ok) {
-      lse_ptr[((size_t)b * Hq + hq) * Sq + qrow] = have ? (m_used + log2f(l)) * kLn2 : -INFINITY;
+      lse_ptr[((size_t)ext.bq * Hq + hq) * ext.rows + ext.qbase + qrow] = have ? (m_used + log2f(l)) * kLn2 : -INFINITY;
     }
   }
 
@@ -603,7 +607,7 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, cudaStream_t stream) {
   if (units > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
   kern<<<(unsigned)units, C::kThreads, C::kSmemBytes, stream>>>(
       a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, a.Hq, a.Hkv, a.Sq, a.Skv, a.causal, a.o_bf16, a.scale,
-      a.Hq * a.B, a.err);
+      a.Hq * a.B, a.err, a.cu_q, a.kv_lens, a.total_q);
   return cudaGetLastError();
 }
 
@@ -618,8 +622,9 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
 }
 
 cudaError_t launch_prefill_empty_kv(const PrefillArgs& a, cudaStream_t stream) {
-  const size_t n_o = (size_t)a.B * a.Sq * a.Hq * a.d;
-  const size_t n_lse = (size_t)a.B * a.Hq * a.Sq;
+  const size_t rows = a.cu_q ? (size_t)a.total_q : (size_t)a.B * a.Sq;
+  const size_t n_o = rows * a.Hq * a.d;
+  const size_t n_lse = rows * a.Hq;
   if (n_o == 0) return cudaSuccess;
   fill_empty_kernel<<<1024, 256, 0, stream>>>(a.o, a.lse, n_o, n_lse, a.o_bf16);
   return cudaGetLastError();

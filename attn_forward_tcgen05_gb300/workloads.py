@@ -16,6 +16,9 @@ Workloads (names used throughout the tests and the benchmark):
 * ``ragged_gqa_decode_b64`` B=64, Hq=32, Hkv=8, d=128, KV lengths ~ U[512, 8192],
                         at most 8 splits of at least 1024 rows each (1 to 8 per
                         sequence, chosen by its length), O bf16 + LSE fp32
+* ``chunked_prefill_gqa_b8`` packed variable-length prefill against a KV cache:
+                        B=8, Hq=28, Hkv=4, d=128, causal, 64-1024 new rows per
+                        sequence after 0-3072 cached ones, O bf16 + LSE fp32
 """
 from __future__ import annotations
 
@@ -70,6 +73,29 @@ def mha_sweep(d: int) -> PrefillShape:
 
 RAGGED_DECODE = DecodeShape("ragged_gqa_decode_b64", 64, 32, 8, 128, 1.0 / math.sqrt(128.0), 8,
                             1024, 1005, len_range=(512, 8192))
+
+
+@dataclass(frozen=True)
+class VarlenShape:
+    """Packed chunked prefill: B sequences, each with Sq_b new query rows after a
+    history of H_b cached tokens (L_b = H_b + Sq_b keys, the new rows last)."""
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    d: int
+    causal: bool
+    scale: float
+    sq_range: tuple[int, int]    # new rows ~ U[lo, hi]
+    hist_range: tuple[int, int]  # cached history ~ U[lo, hi]
+    seed: int
+    out_dtype: str = "bf16"
+
+
+# a chunked-prefill batch of the 7B-class GQA shape: 8 sequences, 64-1024 new
+# tokens each after 0-3072 cached ones
+CHUNKED_PREFILL = VarlenShape("chunked_prefill_gqa_b8", 8, 28, 4, 128, True, 1.0 / math.sqrt(128.0),
+                              (64, 1024), (0, 3072), 1006)
 
 
 def _gen(seed: int) -> torch.Generator:
@@ -140,3 +166,41 @@ def decode_kv_bytes(kv_lens, Hkv, d, elem_bytes=2) -> int:
     """Algorithmic K+V bytes: every cached row of every KV head read once."""
     total = int(torch.as_tensor(kv_lens).to(torch.int64).sum().item())
     return total * Hkv * d * elem_bytes * 2
+
+
+def varlen_inputs(B, Hq, Hkv, d, sq: torch.Tensor, kv_lens: torch.Tensor, seed, max_kv: int | None = None):
+    """Packed q [total_q,Hq,d], kcache/vcache [B,max_kv,Hkv,d] bf16 and cu_seqlens_q
+    int32 [B+1] on the CPU, for new-row counts ``sq`` and key counts ``kv_lens``."""
+    if max_kv is None:
+        max_kv = int(kv_lens.max().item()) if kv_lens.numel() else 0
+    cu = torch.zeros(B + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(sq.to(torch.int64), 0).to(torch.int32)
+    g = _gen(seed + 104729)
+    q = randn_bf16((int(cu[-1].item()), Hq, d), g)
+    kc = randn_bf16((B, max_kv, Hkv, d), g)
+    vc = randn_bf16((B, max_kv, Hkv, d), g)
+    return q, kc, vc, cu
+
+
+def varlen_inputs_for(shape: VarlenShape):
+    """(q, kcache, vcache, cu_seqlens_q, kv_lens) of a chunked-prefill workload."""
+    sq = kv_lengths(shape.B, shape.sq_range[0], shape.sq_range[1], shape.seed)
+    hist = kv_lengths(shape.B, shape.hist_range[0], shape.hist_range[1], shape.seed + 1)
+    kv = (sq + hist).to(torch.int32)
+    q, kc, vc, cu = varlen_inputs(shape.B, shape.Hq, shape.Hkv, shape.d, sq, kv, shape.seed)
+    return q, kc, vc, cu, kv
+
+
+def varlen_flops(cu: torch.Tensor, kv_lens: torch.Tensor, Hq: int, d: int, causal: bool) -> int:
+    """Algorithmic FLOPs of a packed prefill: 4*d per admissible (query, key) pair."""
+    total = 0
+    for b in range(kv_lens.numel()):
+        sq = int(cu[b + 1] - cu[b])
+        L = int(kv_lens[b])
+        if causal:
+            off = L - sq
+            pairs = sum(max(0, min(L, i + off + 1)) for i in range(sq))
+        else:
+            pairs = sq * L
+        total += pairs
+    return 4 * d * Hq * total

@@ -212,6 +212,9 @@ def run_ours(args, rank, world, local_rank):
     else:
         t_prefill_max, t_dec5_max = t_prefill, t_split5 + t_merge5
 
+    # ---- packed variable-length prefill (chunked prefill against a KV cache) ----
+    varlen = None if args.only else time_varlen(args, attn, W, dev, stream, flush, peaks, peak_src)
+
     # ---- end to end through the public API with host buffers ----
     e2e = None if (args.no_e2e or args.only) else run_e2e(args, attn, W, dev, stream, P, dec, flops)
 
@@ -283,9 +286,48 @@ def run_ours(args, rank, world, local_rank):
         "wall_ms_timed_region": round(wall_ms, 3),
         "gpu_launches": (int(do_prefill) + 4 * int(do_decode)) * args.steps,
         "e2e": e2e,
+        "prefill_varlen": varlen,
         "clocks": clocks,
     }
     return line
+
+
+def time_varlen(args, attn, W, dev, stream, flush, peaks, peak_src):
+    """Chunked prefill (packed sequences against a KV cache): average launch time
+    of attn_prefill_varlen over the timed iterations, L2 flushed before each."""
+    import torch
+
+    V = W.CHUNKED_PREFILL
+    q, kc, vc, cu, kv = W.varlen_inputs_for(V)
+    flops = W.varlen_flops(cu, kv, V.Hq, V.d, V.causal)
+    max_sq = int((cu[1:] - cu[:-1]).max())
+    qd, kcd, vcd, cud, kvd = (t.to(dev) for t in (q, kc, vc, cu, kv))
+    o = torch.empty((q.shape[0], V.Hq, V.d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((V.Hq, q.shape[0]), dtype=torch.float32, device=dev)
+
+    def call():
+        attn.prefill_varlen(qd, kcd, vcd, cud, kvd, max_sq, causal=V.causal, scale=V.scale, out=(o, lse))
+
+    for _ in range(args.warmup):
+        call()
+    n = max(1, min(args.steps, 50))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for a, b in evs:
+        flush.zero_()
+        a.record(stream)
+        call()
+        b.record(stream)
+    torch.cuda.synchronize()
+    attn.sync_check()
+    ms = sum(a.elapsed_time(b) for a, b in evs) / n
+    tf = flops / (ms * 1e-3) / 1e12
+    peak_tc = float(peaks["bf16_tflops"])
+    return {"workload": V.name, "B": V.B, "Hq": V.Hq, "Hkv": V.Hkv, "d": V.d, "causal": V.causal,
+            "total_q": int(q.shape[0]), "kv_tokens": int(kv.sum()), "gflop": round(flops / 1e9, 3),
+            "us": round(ms * 1e3, 2), "value": round(tf, 2), "unit": "TFLOP/s", "steps": n,
+            "roofline": {"bound": "tensor", "kernel": "fmha_fwd_kernel<128>", "achieved": round(tf, 2),
+                         "peak": peak_tc, "unit": "TFLOP/s", "frac": round(tf / peak_tc, 4),
+                         "peak_source": f"bf16_tflops (burst) of {peak_src}"}}
 
 
 def run_e2e(args, attn, W, dev, stream, P, dec, flops):

@@ -90,6 +90,43 @@ int attn_prefill_fwd(const attn_bf16_t* q, const attn_bf16_t* k, const attn_bf16
                      float scale, int o_dtype, attn_stream_t stream);
 
 /*
+ * attn_prefill_varlen -- prefill of a packed batch of sequences of different
+ * lengths against a KV cache (chunked prefill).
+ *
+ * Sequence b has Sq_b = cu_seqlens_q[b+1] - cu_seqlens_q[b] query rows, stored
+ * at rows [cu_seqlens_q[b], cu_seqlens_q[b+1]) of q, and L_b = kv_lens[b] keys,
+ * rows [0, L_b) of kcache / vcache (its earlier context followed by its own new
+ * tokens).  For every such row i (0 <= i < Sq_b), query head hq (hk = hq / (Hq/Hkv)):
+ *   O[cu_b + i, hq, :] = sum_j P_ij vcache[b, j, hk, :],   P_ij = exp(S_ij - LSE_i),
+ *   S_ij = scale * q[cu_b + i, hq, :] . kcache[b, j, hk, :],   LSE[hq, cu_b + i] = ln sum_j exp(S_ij),
+ * over the admissible keys j < L_b, and with `causal` only j <= i + (L_b - Sq_b):
+ * the new rows are the last Sq_b positions of the sequence (bottom-right
+ * alignment).  A row with no admissible key gets O = 0 and LSE = -inf.
+ * The pages give the per-sequence key bound `kv_end` of "60 . r57 -- FA KV
+ * staging double buffering (REVERTED)", section 2.2 (KV rows past the end of
+ * the sequence read as zero and are never admitted); the computation per
+ * sequence is the one of attn_prefill_fwd.
+ *
+ * Arguments
+ *   q         bf16 [total_q][Hq][d]        packed queries of all sequences
+ *   kcache    bf16 [B][max_kv][Hkv][d]     keys; rows >= kv_lens[b] are never admitted
+ *   vcache    bf16 [B][max_kv][Hkv][d]     values
+ *   o         [total_q][Hq][d], fp32 (o_dtype = ATTN_F32) or bf16 (ATTN_BF16)
+ *   lse       fp32 [Hq][total_q]
+ *   cu_seqlens_q  int32 [B+1] (device)     non-decreasing, cu[0] = 0, cu[B] = total_q
+ *   kv_lens       int32 [B] (device)       0 <= L_b <= max_kv
+ *                 (device values are trusted to be in range; they are clamped on the device)
+ *   B, Hq, Hkv, total_q, max_sq, max_kv   B, total_q >= 0; Hq % Hkv == 0; max_sq >= every
+ *                                          Sq_b (it sizes the grid); max_kv >= 0
+ *   d, causal, scale, o_dtype, stream      as for attn_prefill_fwd
+ * Returns ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED or ATTN_ERR_CUDA.
+ */
+int attn_prefill_varlen(const attn_bf16_t* q, const attn_bf16_t* kcache, const attn_bf16_t* vcache,
+                        void* o, float* lse, const int* cu_seqlens_q, const int* kv_lens, int B,
+                        int Hq, int Hkv, int total_q, int max_sq, int max_kv, int d, int causal,
+                        float scale, int o_dtype, attn_stream_t stream);
+
+/*
  * attn_decode_split -- one-token GQA decode, split-KV partials.
  *
  * For every batch b, KV head hk and split s, the rows [lo, hi) of sequence b

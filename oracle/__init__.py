@@ -9,7 +9,8 @@ Inputs may be numpy arrays or torch tensors of any float dtype; they are
 widened to fp64 exactly (bf16 -> fp64 is exact).  Layouts are the ones the
 C file states: prefill q/o ``[B, Sq, Hq, d]``, k/v ``[B, Skv, Hkv, d]``,
 lse ``[B, Hq, Sq]``; decode q/o ``[B, Hq, d]``, caches ``[B, Lmax, Hkv, d]``,
-part_o ``[B, Hq, n_splits, d]``, part_lse ``[B, Hq, n_splits]``.
+part_o ``[B, Hq, n_splits, d]``, part_lse ``[B, Hq, n_splits]``; packed
+variable-length prefill q/o ``[total_q, Hq, d]``, lse ``[Hq, total_q]``.
 """
 from __future__ import annotations
 
@@ -112,6 +113,31 @@ def sdpa(q, k, v, causal: bool, scale: float, nthreads: int = 0, lib=None):
     rc = (lib or _load()).oracle_sdpa(_dp(q), _dp(k), _dp(v), B, Hq, Hkv, Sq, Skv, d, int(bool(causal)),
                              float(scale), _dp(o), _dp(lse), int(nthreads))
     _check(rc, "oracle_sdpa")
+    return o, lse
+
+
+def sdpa_varlen(q, kcache, vcache, cu_seqlens_q, kv_lens, causal: bool, scale: float,
+                nthreads: int = 0, lib=None):
+    """Packed variable-length prefill against a KV cache, by its definition: every
+    sequence b is the plain prefill of its own rows q[cu[b]:cu[b+1]] against the
+    keys kcache[b, :kv_lens[b]] (bottom-right causal alignment when Sq_b < L_b:
+    the new rows are the sequence's last positions), computed with ``sdpa``.
+    Layouts: q/o ``[total_q, Hq, d]``, caches ``[B, max_kv, Hkv, d]``, lse ``[Hq, total_q]``.
+    Follows the per-sequence key bound of "60 . r57 -- FA KV staging double
+    buffering (REVERTED)", section 2.2; the per-sequence computation is ``sdpa``."""
+    q, kc, vc = _f64(q), _f64(kcache), _f64(vcache)
+    cu = [int(x) for x in np.asarray(cu_seqlens_q).reshape(-1)]
+    lens = [int(x) for x in np.asarray(kv_lens).reshape(-1)]
+    total_q, Hq, d = q.shape
+    o = np.zeros((total_q, Hq, d), np.float64)
+    lse = np.full((Hq, total_q), -np.inf, np.float64)
+    for b, L in enumerate(lens):
+        c0, c1 = cu[b], cu[b + 1]
+        if c1 <= c0:
+            continue
+        ob, lb = sdpa(q[None, c0:c1], kc[b:b + 1, :L], vc[b:b + 1, :L], causal, scale, nthreads, lib)
+        o[c0:c1] = ob[0]
+        lse[:, c0:c1] = lb[0]
     return o, lse
 
 

@@ -174,6 +174,30 @@ def pin_brute_force_exact(lib=None):
         _close(rl, np.array([el[b, h, i] for b, h, i in rows]), 1e-12, tag + " rows LSE")
 
 
+def pin_varlen_brute_force(lib=None):
+    """Packed variable-length prefill: every sequence against an independent brute
+    force of its own rows and keys (offsets, key ranges, bottom-right causal bound
+    of the new rows after a history, the [Hq, total_q] LSE layout)."""
+    rng = np.random.default_rng(2468)
+    Hq, Hkv, d, max_kv = 4, 2, 3, 7
+    seqs = [(2, 5), (0, 3), (3, 3), (1, 7), (2, 0)]  # (new query rows Sq_b, keys L_b)
+    B = len(seqs)
+    cu = np.cumsum([0] + [sq for sq, _ in seqs]).astype(np.int32)
+    lens = np.array([L for _, L in seqs], np.int32)
+    q = _bf16((int(cu[-1]), Hq, d), rng)
+    kc = _bf16((B, max_kv, Hkv, d), rng)
+    vc = _bf16((B, max_kv, Hkv, d), rng)
+    for causal in (True, False):
+        o, lse = oracle.sdpa_varlen(q, kc, vc, cu, lens, causal, 0.5, lib=lib)
+        assert o.shape == (cu[-1], Hq, d) and lse.shape == (Hq, cu[-1])
+        for b, (sq, L) in enumerate(seqs):
+            if sq == 0:
+                continue
+            eo, el = _exact_attention(q[None, cu[b]:cu[b + 1]], kc[b:b + 1, :L], vc[b:b + 1, :L], causal, 0.5)
+            _close(o[cu[b]:cu[b + 1]], eo[0], 1e-12, f"varlen b={b} causal={causal} O")
+            _close(lse[:, cu[b]:cu[b + 1]], el[0], 1e-12, f"varlen b={b} causal={causal} LSE")
+
+
 # ---------------------------------------------------------------- library routine
 def pin_torch_sdpa(lib=None):
     from torch.nn.attention.bias import causal_lower_right
@@ -338,4 +362,5 @@ ALL_PINS = [
     pin_golden_split_merge, pin_golden_split_rule, pin_brute_force_exact, pin_torch_sdpa,
     pin_rows_sum_to_one, pin_permutation_invariance, pin_linearity_in_v,
     pin_split_merge_equals_unsplit, pin_merge_identity, pin_decode_equals_prefill, pin_closed_forms,
+    pin_varlen_brute_force,
 ]

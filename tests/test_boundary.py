@@ -57,6 +57,22 @@ def test_prefill_validation(lib):
     assert f(N, N, N, N, N, 2, 2, 2, 0, 4, 64, 1, 0.5, 0, N) == attn.ATTN_OK  # no queries: no-op
 
 
+def test_prefill_varlen_validation(lib):
+    f = attn.attn_prefill_varlen
+    #      q  kc vc o  lse cu kv  B  Hq Hkv tot msq mkv d  causal scale dtype stream
+    assert f(P, P, P, P, P, P, P, 2, 2, 2, 10, 8, 16, 96, 1, 0.5, 0, N) == attn.ATTN_ERR_UNSUPPORTED  # d
+    assert f(P, P, P, P, P, P, P, 2, 2, 2, 10, 8, 16, 64, 1, 0.5, 9, N) == attn.ATTN_ERR_UNSUPPORTED  # dtype
+    assert f(P, P, P, P, P, P, P, 2, 3, 2, 10, 8, 16, 64, 1, 0.5, 0, N) == attn.ATTN_ERR_INVALID_ARG  # Hq % Hkv
+    assert f(P, P, P, P, P, P, P, 2, 2, 2, -1, 8, 16, 64, 1, 0.5, 0, N) == attn.ATTN_ERR_INVALID_ARG  # total_q
+    assert f(P, P, P, P, P, P, P, 2, 2, 2, 10, 8, -1, 64, 1, 0.5, 0, N) == attn.ATTN_ERR_INVALID_ARG  # max_kv
+    assert f(P, P, P, P, P, P, P, 2, 2, 2, 10, 8, 16, 64, 1, -0.5, 0, N) == attn.ATTN_ERR_INVALID_ARG  # scale
+    assert f(P, P, P, P, P, N, P, 2, 2, 2, 10, 8, 16, 64, 1, 0.5, 0, N) == attn.ATTN_ERR_INVALID_ARG  # null cu
+    assert f(P, P, P, P, P, P, ctypes.c_void_p(18), 2, 2, 2, 10, 8, 16, 64, 1, 0.5, 0, N) == attn.ATTN_ERR_INVALID_ARG  # kv_lens misaligned
+    assert f(P, M, P, P, P, P, P, 2, 2, 2, 10, 8, 16, 64, 1, 0.5, 0, N) == attn.ATTN_ERR_INVALID_ARG  # kcache misaligned
+    assert f(N, N, N, N, N, N, N, 0, 2, 2, 10, 8, 16, 64, 1, 0.5, 0, N) == attn.ATTN_OK  # empty batch
+    assert f(N, N, N, N, N, N, N, 3, 2, 2, 0, 0, 16, 64, 1, 0.5, 0, N) == attn.ATTN_OK  # no query rows
+
+
 def test_decode_and_merge_validation(lib):
     f = attn.attn_decode_split
     assert f(P, P, P, P, 1, 28, 4, 96, 10, 0.1, 8, 1, P, P, N) == attn.ATTN_ERR_UNSUPPORTED

@@ -325,6 +325,144 @@ def test_prefill_protocol_one_s_buffer_is_sound(NQ, SUB, SK, SV, n_t):
         simulate(NQ, SK, SV, list(n_t), seed, SUB=SUB, NS=1)
 
 
+def simulate_slices(SK, SV, n, seed, NSL=2, NS=2):
+    """CTA-pair schedule with independent key slices: NSL softmax warpgroups own
+    slice h of every S tile with their own running max, sums and O accumulator;
+    per KV tile j the MMA warp issues S(j+1), then P_h(j).V_h(j) for every slice
+    (waiting for that slice's P barrier of S buffer j % NS), committing each to
+    the slice's O barrier."""
+    rng = random.Random(seed)
+    bars = {}
+
+    def bar(name, count=1):
+        if name not in bars:
+            bars[name] = Bar(name, count)
+        return bars[name]
+
+    now = [0]
+    events = []
+    seq = itertools.count()
+    mma_free = [0]
+
+    def at(time, fn):
+        heapq.heappush(events, (time, next(seq), fn))
+
+    def tma(b):
+        at(now[0] + rng.randint(50, 3000), lambda: b.complete_tx(1))
+
+    def mma(dur):
+        mma_free[0] = max(now[0], mma_free[0]) + dur
+
+    def commit(b):
+        at(mma_free[0], b.arrive)
+
+    def wait(b, parity, use):
+        assert b.done in (use, use + 1), f"{b.name}: waiting for phase {use} with {b.done} done"
+        return ("wait", b, parity)
+
+    def producer():
+        bar("q").expect_tx(1)
+        tma(bar("q"))
+        jk = jv = 0
+        while jv < n:
+            if jk < n and jk <= jv + 1:
+                s, u = jk % SK, jk // SK
+                if u > 0:
+                    yield wait(bar(("eK", s)), (u & 1) ^ 1, u - 1)
+                bar(("fK", s)).expect_tx(1)
+                tma(bar(("fK", s)))
+                jk += 1
+                continue
+            s, u = jv % SV, jv // SV
+            if u > 0:
+                yield wait(bar(("eV", s)), (u & 1) ^ 1, u - 1)
+            bar(("fV", s)).expect_tx(1)
+            tma(bar(("fV", s)))
+            jv += 1
+
+    def issue_s(j):
+        for _ in range(8):
+            mma(rng.randint(20, 80))
+        commit(bar(("S", j % NS)))
+
+    def mma_warp():
+        yield wait(bar("q"), 0, 0)
+        yield wait(bar(("fK", 0)), 0, 0)
+        issue_s(0)
+        commit(bar(("eK", 0)))
+        for j in range(n):
+            if j + 1 < n:
+                s, u = (j + 1) % SK, (j + 1) // SK
+                yield wait(bar(("fK", s)), u & 1, u)
+                issue_s(j + 1)
+                commit(bar(("eK", s)))
+            s, u = j % SV, j // SV
+            yield wait(bar(("fV", s)), u & 1, u)
+            for h in range(NSL):
+                pu = j // NS
+                yield wait(bar(("P", j % NS, h), 8), pu & 1, pu)
+                for _ in range(4):
+                    mma(rng.randint(20, 80))
+                commit(bar(("O", h)))
+            if j == n - 1:
+                commit(bar("Fin"))
+            commit(bar(("eV", s)))
+
+    def softmax(h):
+        for j in range(n):
+            buf, use = j % NS, j // NS
+            yield wait(bar(("S", buf)), use & 1, use)
+            yield ("sleep", rng.randint(20, 600))
+            if j > 0 and rng.random() < 0.3:  # this slice's O rescale needs P_h(j-1).V_h(j-1)
+                yield wait(bar(("O", h)), (j - 1) & 1, j - 1)
+                yield ("sleep", rng.randint(20, 200))
+            for _ in range(8):  # 4 warps in each of the two CTAs
+                bar(("P", buf, h), 8).arrive()
+        if n > 0:
+            yield wait(bar("Fin"), 0, 0)
+
+    procs = [producer()] + [softmax(h) for h in range(NSL)] + [mma_warp()]
+    blocked = {}
+    finished = set()
+
+    def step(i):
+        while True:
+            if i in blocked:
+                _, b, parity = blocked[i]
+                if not b.ready(parity):
+                    return
+                del blocked[i]
+            try:
+                req = next(procs[i])
+            except StopIteration:
+                finished.add(i)
+                return
+            if req[0] == "wait":
+                blocked[i] = req
+            elif req[0] == "sleep":
+                at(now[0] + req[1], lambda i=i: step(i))
+                return
+
+    for i in range(len(procs)):
+        step(i)
+    for _ in range(200000):
+        for i in list(blocked):
+            step(i)
+        if len(finished) == len(procs):
+            break
+        if not events:
+            raise AssertionError(f"deadlock: blocked on {[blocked[i][1].name for i in blocked]}")
+        now[0], _, fn = heapq.heappop(events)
+        fn()
+    assert len(finished) == len(procs), "pipeline did not drain"
+
+
+@pytest.mark.parametrize("SK,SV,n", [(3, 3, 11), (3, 3, 1), (3, 3, 2), (2, 2, 7), (1, 1, 5)])
+def test_prefill_protocol_key_slices_is_sound(SK, SV, n):
+    for seed in range(150):
+        simulate_slices(SK, SV, n, seed)
+
+
 def test_single_p_barrier_with_two_s_buffers_is_unsound():
     """One P barrier shared by both S buffers of a tile: the softmax can publish
     P(j+1) before the MMA warp has waited for P(j), two phases ahead of that

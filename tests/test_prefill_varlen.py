@@ -1,0 +1,99 @@
+"""Packed variable-length prefill against a KV cache (chunked prefill), through
+the C ABI, against the fp64 oracle.
+
+Small batches are compared element by element; the full-size chunked-prefill
+workload is compared on sampled rows of every sequence that the oracle
+computes one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from attn_forward_tcgen05_gb300 import prefill_varlen, sync_check
+from attn_forward_tcgen05_gb300 import workloads as W
+from tests.tolerances import check_lse, check_o
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(q, kc, vc, cu, kv, causal, scale, out_dtype, max_sq=None):
+    if max_sq is None:
+        max_sq = int((cu[1:] - cu[:-1]).max().item()) if kv.numel() else 0
+    o, lse = prefill_varlen(q.cuda(), kc.cuda(), vc.cuda(), cu.cuda(), kv.cuda(), max_sq,
+                            causal=causal, scale=scale, out_dtype=out_dtype)
+    sync_check()
+    return o.float().cpu().numpy(), lse.cpu().numpy()
+
+
+def _case(seqs, Hq, Hkv, d, seed, max_kv=None):
+    sq = torch.tensor([a for a, _ in seqs], dtype=torch.int32)
+    kv = torch.tensor([b for _, b in seqs], dtype=torch.int32)
+    q, kc, vc, cu = W.varlen_inputs(len(seqs), Hq, Hkv, d, sq, kv, seed, max_kv)
+    return q, kc, vc, cu, kv
+
+
+# (new query rows, keys) per sequence: a single new token, a chunk after a
+# history, a chunk that is the whole sequence, several KV tiles, an empty
+# sequence, a sequence with fewer keys than rows (its first rows see no key
+# under the causal mask), and a ragged tail in every dimension
+MIXED = [(1, 1), (77, 300), (128, 128), (300, 1200), (0, 50), (200, 150), (129, 1000)]
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_mixed_batch(d, causal, out_dtype):
+    q, kc, vc, cu, kv = _case(MIXED, 4, 2, d, 60 + d)
+    scale = 1.0 / np.sqrt(d)
+    o, lse = _run(q, kc, vc, cu, kv, causal, scale, out_dtype)
+    ro, rl = oracle.sdpa_varlen(q, kc, vc, cu, kv, causal, scale)
+    check_o(o, ro, out_dtype == torch.bfloat16)
+    check_lse(lse, rl)
+
+
+def test_one_sequence_equals_prefill():
+    """One sequence whose keys are exactly its rows is the fixed-length prefill."""
+    from attn_forward_tcgen05_gb300 import prefill
+    q, kc, vc, cu, kv = _case([(300, 300)], 8, 2, 128, 71)
+    o1, l1 = _run(q, kc, vc, cu, kv, True, 0.1, torch.float32)
+    o2, l2 = prefill(q[None].cuda(), kc.cuda(), vc.cuda(), causal=True, scale=0.1, out_dtype=torch.float32)
+    sync_check()
+    np.testing.assert_array_equal(o1, o2[0].cpu().numpy())
+    np.testing.assert_array_equal(l1, l2[0].cpu().numpy())
+
+
+def test_larger_max_sq_and_cache_than_needed():
+    """max_sq and max_kv larger than every sequence: extra q-blocks do nothing and
+    cache rows past kv_lens are never admitted (filled with large values here)."""
+    q, kc, vc, cu, kv = _case([(90, 200), (33, 40)], 4, 4, 64, 72, max_kv=512)
+    kc[:, 300:] = 30.0
+    vc[:, 300:] = -30.0
+    o, lse = _run(q, kc, vc, cu, kv, True, 0.125, torch.float32, max_sq=700)
+    ro, rl = oracle.sdpa_varlen(q, kc, vc, cu, kv, True, 0.125)
+    check_o(o, ro, False)
+    check_lse(lse, rl)
+
+
+def test_no_keys_anywhere():
+    q, kc, vc, cu, kv = _case([(5, 0), (3, 0)], 2, 2, 64, 73, max_kv=0)
+    o, lse = _run(q, kc, vc, cu, kv, True, 0.125, torch.float32)
+    assert np.all(o == 0) and np.all(np.isneginf(lse))
+
+
+def test_chunked_prefill_workload_sampled():
+    """The full chunked-prefill workload in the benchmark's configuration, checked
+    on sampled rows of every sequence (first, last, around the tile edges)."""
+    s = W.CHUNKED_PREFILL
+    q, kc, vc, cu, kv = W.varlen_inputs_for(s)
+    o, lse = _run(q, kc, vc, cu, kv, s.causal, s.scale, torch.bfloat16)
+    for b in range(s.B):
+        c0, c1 = int(cu[b]), int(cu[b + 1])
+        sq, L = c1 - c0, int(kv[b])
+        picks = sorted({0, 1, 127, 128, sq // 2, sq - 2, sq - 1} & set(range(sq)))
+        rows = [(0, h, i) for h in range(s.Hq) for i in picks]
+        ro, rl = oracle.sdpa_rows(q[None, c0:c1], kc[b:b + 1, :L], vc[b:b + 1, :L], s.causal, s.scale, rows)
+        got_o = np.stack([o[c0 + i, h] for _, h, i in rows])
+        got_l = np.array([lse[h, c0 + i] for _, h, i in rows])
+        check_o(got_o, ro, True, f"O seq {b}")
+        check_lse(got_l, rl, f"LSE seq {b}")
