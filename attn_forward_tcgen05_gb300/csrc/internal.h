@@ -88,9 +88,6 @@ constexpr int kPrefillKVStageRows = 128;
 #ifndef ATTN_PREFILL_PAIR_D128
 #define ATTN_PREFILL_PAIR_D128 0
 #endif
-#ifndef ATTN_PREFILL_PAIR_D128_SLICES
-#define ATTN_PREFILL_PAIR_D128_SLICES 1
-#endif
 constexpr bool prefill_uses_pair(int d) { return d == 256 || (ATTN_PREFILL_PAIR_D128 && d == 128); }
 constexpr int prefill_k_box_rows(int d) { return prefill_uses_pair(d) ? kPrefillKVStageRows / 2 : kPrefillKVStageRows; }
 
