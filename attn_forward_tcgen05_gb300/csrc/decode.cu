@@ -15,7 +15,8 @@
 // one 64-row box per 128-byte panel: 32-row boxes capped the kernel at about
 // 14 bytes per cycle per SM, below the HBM rate.
 //
-// Work mapping: one CTA per split unit (batch, KV head, split), 6 warps.
+// Work mapping: one CTA per split unit (batch, KV head, split), 6 warps; a
+// launch with few units spreads each group's query heads over several CTAs.
 // Consumer warps 0..3 form two pairs; pair p owns ring stage p and takes the
 // stages u = p, p+2, p+4, ... of the unit, warp h of the pair the rows
 // [32h, 32h+32) of each, for all G query heads of the group, so every loaded
@@ -98,18 +99,28 @@ __device__ __forceinline__ void consumer_bar_sync() {
 // barriers: the warp hands the K half back as soon as its scores are done, so
 // the K producer warp refills it with the warp's next K tile while the warp is
 // still in softmax and P.V; the V producer warp refills the V half after P.V.
-template <int D, int GMAX>
+template <int D, int GMAX, bool SPLIT_HEADS>
 __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<D, GMAX>::kMinBlocks)
     decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const uint16_t* __restrict__ q,
                         const int* __restrict__ kv_lens, float* __restrict__ part_o,
                         float* __restrict__ part_lse, int Hq, int Hkv, int max_kv, int n_splits,
-                        int min_rows, float scale, uint32_t* err) {
+                        int min_rows, float scale, int heads_per_cta, uint32_t* err) {
   using C = DecodeCfg<D, GMAX>;
   constexpr int DPL = D / 32;   // output dims per lane in the P.V phase
   constexpr int DP2 = DPL / 2;  // ... as fp32 pairs
-  const int s_idx = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
-  const int G = Hq / Hkv;
+  // CTA = (split, KV head, batch x head group): the query heads [g0, g0 + G) of
+  // the KV head's group (all of them unless a small launch splits the group
+  // across CTAs, which then re-read the same K/V rows from L2)
+  const int Gall = Hq / Hkv;
+  const int s_idx = blockIdx.x, hk = blockIdx.y;
+  int b = blockIdx.z, g0 = 0, G = Gall;
+  if constexpr (SPLIT_HEADS) {
+    const int n_hg = (Gall + heads_per_cta - 1) / heads_per_cta;
+    b = blockIdx.z / n_hg;
+    g0 = (blockIdx.z % n_hg) * heads_per_cta;
+    G = min(heads_per_cta, Gall - g0);
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // ---- split bounds: chunk = max(ceil(L / n_splits), min_rows) ----
@@ -120,7 +131,7 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<D, GMAX>::kMinBlocks
   if (chunk < 1) chunk = 1;
   const long long lo_ll = (long long)s_idx * chunk, hi_ll = lo_ll + chunk;
   const int lo = (int)(lo_ll < L ? lo_ll : L), hi = (int)(hi_ll < L ? hi_ll : L);
-  const size_t row_base = ((size_t)b * Hq + (size_t)hk * G) * n_splits + s_idx;  // head g: + g*n_splits
+  const size_t row_base = ((size_t)b * Hq + (size_t)hk * Gall + g0) * n_splits + s_idx;  // head g: + g*n_splits
 
   if (lo >= hi) {  // empty split: o = 0, lse = -inf; nothing is read
     for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
@@ -158,7 +169,7 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<D, GMAX>::kMinBlocks
   const float qscale = scale * kLog2e;
   for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
     const int g = i / D, t = i % D;
-    qs[g * D + t] = q[((size_t)b * Hq + (size_t)hk * G + g) * D + t];
+    qs[g * D + t] = q[((size_t)b * Hq + (size_t)hk * Gall + g0 + g) * D + t];
   }
   for (int i = threadIdx.x; i < (GMAX - G) * D; i += blockDim.x) qs[G * D + i] = 0;
   __syncthreads();
@@ -440,26 +451,47 @@ __global__ void __launch_bounds__(128)
   if (lane == 0) lse[row] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
 }
 
-template <int D, int GMAX>
-cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
+template <int D, int GMAX, bool SPLIT_HEADS>
+cudaError_t launch_decode_t(const DecodeArgs& a, int heads_per_cta, cudaStream_t stream) {
   using C = DecodeCfg<D, GMAX>;
-  auto kern = decode_split_kernel<D, GMAX>;
+  auto kern = decode_split_kernel<D, GMAX, SPLIT_HEADS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  dim3 grid(a.n_splits, a.Hkv, a.B);
+  const int G = a.Hq / a.Hkv;
+  const int n_hg = (G + heads_per_cta - 1) / heads_per_cta;
+  if ((long long)a.B * n_hg > 65535) return cudaErrorInvalidValue;
+  dim3 grid(a.n_splits, a.Hkv, a.B * n_hg);
   kern<<<grid, kDecodeThreads, C::kSmemBytes, stream>>>(a.tm_k, a.tm_v, a.q, a.kv_lens, a.part_o,
                                                          a.part_lse, a.Hq, a.Hkv, a.max_kv,
-                                                         a.n_splits, a.min_rows, a.scale, a.err);
+                                                         a.n_splits, a.min_rows, a.scale,
+                                                         heads_per_cta, a.err);
   return cudaGetLastError();
 }
+
+// Query heads per CTA.  A launch with fewer than kSmallUnits (batch, KV head,
+// split) units is latency-bound (one sequence of 1641 keys in 8 splits is 32
+// CTAs on 152 SMs), so its head groups are spread over more CTAs.
+constexpr int kSmallUnits = 128;
 
 template <int D>
 cudaError_t launch_decode_g(const DecodeArgs& a, cudaStream_t stream) {
   const int G = a.Hq / a.Hkv;
-  if (G <= 4) return launch_decode_t<D, 4>(a, stream);
-  if (G <= 8) return launch_decode_t<D, 8>(a, stream);
-  return launch_decode_t<D, 16>(a, stream);
+  const long long units = (long long)a.B * a.Hkv * a.n_splits;
+  int hpc = G;
+  if (units < kSmallUnits && G > 1) {
+    const int want = (int)((kSmallUnits + units - 1) / units);  // head groups wanted
+    const int n_hg = want < G ? want : G;
+    hpc = (G + n_hg - 1) / n_hg;
+  }
+  if (hpc < G) {
+    if (hpc <= 4) return launch_decode_t<D, 4, true>(a, hpc, stream);
+    if (hpc <= 8) return launch_decode_t<D, 8, true>(a, hpc, stream);
+    return launch_decode_t<D, 16, true>(a, hpc, stream);
+  }
+  if (hpc <= 4) return launch_decode_t<D, 4, false>(a, hpc, stream);
+  if (hpc <= 8) return launch_decode_t<D, 8, false>(a, hpc, stream);
+  return launch_decode_t<D, 16, false>(a, hpc, stream);
 }
 
 }  // namespace
