@@ -45,13 +45,16 @@ def _bind(lib):
     c_int, c_double = ctypes.c_int, ctypes.c_double
     lib.oracle_sdpa.argtypes = [P, P, P] + [c_int] * 7 + [c_double, P, P, c_int]
     lib.oracle_sdpa_rows.argtypes = [P, P, P] + [c_int] * 7 + [c_double, I, c_int, P, P, c_int]
+    lib.oracle_sdpa_window.argtypes = [P, P, P] + [c_int] * 8 + [c_double, P, P, c_int]
+    lib.oracle_sdpa_window_rows.argtypes = [P, P, P] + [c_int] * 8 + [c_double, I, c_int, P, P, c_int]
     lib.oracle_split_bounds.argtypes = [c_int] * 4 + [I, I]
     lib.oracle_decode_split.argtypes = [P, P, P, I] + [c_int] * 5 + [c_double, c_int, c_int, P, P, c_int]
     lib.oracle_decode.argtypes = [P, P, P, I] + [c_int] * 5 + [c_double, P, P, c_int]
     lib.oracle_merge.argtypes = [P, P] + [c_int] * 4 + [P, P]
     lib.oracle_num_cores.argtypes = []
     for f in ("oracle_sdpa", "oracle_sdpa_rows", "oracle_split_bounds", "oracle_decode_split",
-              "oracle_decode", "oracle_merge", "oracle_num_cores"):
+              "oracle_decode", "oracle_merge", "oracle_num_cores", "oracle_sdpa_window",
+              "oracle_sdpa_window_rows"):
         getattr(lib, f).restype = c_int
     return lib
 
@@ -113,6 +116,40 @@ def sdpa(q, k, v, causal: bool, scale: float, nthreads: int = 0, lib=None):
     rc = (lib or _load()).oracle_sdpa(_dp(q), _dp(k), _dp(v), B, Hq, Hkv, Sq, Skv, d, int(bool(causal)),
                              float(scale), _dp(o), _dp(lse), int(nthreads))
     _check(rc, "oracle_sdpa")
+    return o, lse
+
+
+def sdpa_window(q, k, v, window: int, n_sink: int, scale: float, nthreads: int = 0, lib=None):
+    """Causal attention over a sliding window plus attention sinks: query i (key
+    position p = i + Skv - Sq) admits the keys p - window < j <= p and the first
+    n_sink keys j < n_sink (j <= p).  Same layouts as ``sdpa``.  Follows the
+    sliding-window and sink items (D3-D5) of "STAGE_D.md -- FMHA Kernel
+    Development": their two branches merged through the LSE are exactly the
+    softmax over the union of the two key sets, which this computes directly."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, Sq, Hq, d = q.shape
+    _, Skv, Hkv, _ = k.shape
+    o = np.zeros((B, Sq, Hq, d), np.float64)
+    lse = np.zeros((B, Hq, Sq), np.float64)
+    rc = (lib or _load()).oracle_sdpa_window(_dp(q), _dp(k), _dp(v), B, Hq, Hkv, Sq, Skv, d, int(window),
+                                             int(n_sink), float(scale), _dp(o), _dp(lse), int(nthreads))
+    _check(rc, "oracle_sdpa_window")
+    return o, lse
+
+
+def sdpa_window_rows(q, k, v, window: int, n_sink: int, scale: float, rows, nthreads: int = 0, lib=None):
+    """Selected rows ``rows`` = [(b, hq, i), ...] of ``sdpa_window``: (o [n, d], lse [n])."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, Sq, Hq, d = q.shape
+    _, Skv, Hkv, _ = k.shape
+    r = _i32(np.asarray(rows, dtype=np.int32).reshape(-1, 3))
+    n = r.shape[0]
+    o = np.zeros((n, d), np.float64)
+    lse = np.zeros((n,), np.float64)
+    rc = (lib or _load()).oracle_sdpa_window_rows(_dp(q), _dp(k), _dp(v), B, Hq, Hkv, Sq, Skv, d, int(window),
+                                                  int(n_sink), float(scale), _ip(r), n, _dp(o), _dp(lse),
+                                                  int(nthreads))
+    _check(rc, "oracle_sdpa_window_rows")
     return o, lse
 
 

@@ -10,6 +10,9 @@
  *
  *   S[i][j] = scale * sum_t q[i][t] * k[j][t]                (fp64, full Sq x Skv)
  *   S[i][j] = -inf  if causal and j > i + (Skv - Sq)          (bottom-right alignment)
+ *   S[i][j] = -inf  if a window W > 0 is set and n_sink <= j <= i + (Skv - Sq) - W
+ *                   (sliding window of the last W positions up to the query's
+ *                   own, plus the first n_sink positions always visible)
  *   m_i     = max_j S[i][j]
  *   l_i     = sum_j exp(S[i][j] - m_i)
  *   P[i][j] = exp(S[i][j] - m_i) / l_i
@@ -26,6 +29,12 @@
  *    P = exp(S*scale - row_max), LSE from ln(row_sum) plus the row max; the
  *    page mixes a base-2 max with a natural log, and this oracle takes LSE in
  *    natural units throughout (LSE = ln sum_j exp(S_ij)).
+ *  - "STAGE_D.md -- FMHA Kernel Development", D3-D5: a length mask on the
+ *    sliding-window branch, a causal mask on it, and a merge of the window
+ *    branch with a sink branch through their LSEs.  Here both branches are
+ *    one key set: the window of the last W positions and the first n_sink
+ *    positions, under the causal mask (the merge of two disjoint key sets
+ *    through their LSEs is exactly the softmax over their union).
  *  - "66 . D2: explicit K+V register staging", section 3.2: the decode split
  *    body walks rows [lo, hi) of one sequence for one KV head, with score
  *    s = (q . k) * scale and the running max / running sum / running O update.
@@ -133,13 +142,17 @@ static void run_items(item_fn fn, void* ctx, long n_items, int nthreads) {
  * Writes o_row[d] and returns lse through *lse_out.  s is caller scratch of
  * length (j1 - j0). */
 static void softmax_row(const double* q_row, const double* k_base, const double* v_base,
-                        long kv_row_stride, int d, int j0, int j1, int jmax, double scale,
-                        double* s, double* o_row, double* lse_out) {
+                        long kv_row_stride, int d, int j0, int j1, int jmax, int jlo, int nsink,
+                        double scale, double* s, double* o_row, double* lse_out) {
     int j, t;
     double m = -INFINITY, l = 0.0;
-    /* step 1-2: scores with mask */
+    /* step 1-2: scores with mask (keys past jmax; keys before jlo except sinks) */
     for (j = j0; j < j1; ++j) {
         if (j > jmax) {
+            s[j - j0] = -INFINITY;
+            continue;
+        }
+        if (j < jlo && j >= nsink) {
             s[j - j0] = -INFINITY;
             continue;
         }
@@ -175,6 +188,7 @@ static void softmax_row(const double* q_row, const double* k_base, const double*
 typedef struct {
     const double *q, *k, *v;
     int B, Hq, Hkv, Sq, Skv, d, causal;
+    int window, n_sink; /* window <= 0: no window */
     double scale;
     double *o, *lse;
     int err;
@@ -205,6 +219,8 @@ static void sdpa_item(void* vctx, long item) {
             for (t = 0; t < c->d; ++t) dot += q_row[t] * k_row[t];
             S[(long)i * c->Skv + j] = c->scale * dot;
             if (c->causal && j > i + (c->Skv - c->Sq)) S[(long)i * c->Skv + j] = -INFINITY;
+            if (c->window > 0 && j >= c->n_sink && j <= i + (c->Skv - c->Sq) - c->window)
+                S[(long)i * c->Skv + j] = -INFINITY;
         }
     }
     /* softmax row by row, O = P V, LSE = m + ln l */
@@ -248,6 +264,26 @@ int oracle_sdpa(const double* q, const double* k, const double* v, int B, int Hq
     if (!q || !o || !lse || (Skv > 0 && (!k || !v))) return ORACLE_EINVAL;
     c.q = q; c.k = k; c.v = v;
     c.B = B; c.Hq = Hq; c.Hkv = Hkv; c.Sq = Sq; c.Skv = Skv; c.d = d; c.causal = causal;
+    c.window = 0; c.n_sink = 0;
+    c.scale = scale; c.o = o; c.lse = lse; c.err = ORACLE_OK;
+    run_items(sdpa_item, &c, (long)B * Hq, nthreads);
+    return c.err;
+}
+
+/* Causal attention over a sliding window of the last `window` positions (the
+ * query's own included) plus the first n_sink positions.  window >= 1,
+ * n_sink >= 0.  Returns 0 or a negative error. */
+int oracle_sdpa_window(const double* q, const double* k, const double* v, int B, int Hq, int Hkv,
+                       int Sq, int Skv, int d, int window, int n_sink, double scale, double* o,
+                       double* lse, int nthreads) {
+    sdpa_ctx c;
+    if (!check_dims(B, Hq, Hkv, d) || Sq < 0 || Skv < 0 || window < 1 || n_sink < 0)
+        return ORACLE_EINVAL;
+    if (B == 0 || Sq == 0) return ORACLE_OK;
+    if (!q || !o || !lse || (Skv > 0 && (!k || !v))) return ORACLE_EINVAL;
+    c.q = q; c.k = k; c.v = v;
+    c.B = B; c.Hq = Hq; c.Hkv = Hkv; c.Sq = Sq; c.Skv = Skv; c.d = d; c.causal = 1;
+    c.window = window; c.n_sink = n_sink;
     c.scale = scale; c.o = o; c.lse = lse; c.err = ORACLE_OK;
     run_items(sdpa_item, &c, (long)B * Hq, nthreads);
     return c.err;
@@ -260,6 +296,7 @@ int oracle_sdpa(const double* q, const double* k, const double* v, int B, int Hq
 typedef struct {
     const double *q, *k, *v;
     int B, Hq, Hkv, Sq, Skv, d, causal;
+    int window, n_sink; /* window <= 0: no window */
     double scale;
     const int* rows; /* n x 3: (b, hq, i) */
     double *o, *lse; /* n x d, n */
@@ -272,6 +309,7 @@ static void rows_item(void* vctx, long item) {
     int G = c->Hq / c->Hkv, hk = hq / G;
     long q_row_stride = (long)c->Hq * c->d, kv_row_stride = (long)c->Hkv * c->d;
     int jmax = c->causal ? i + (c->Skv - c->Sq) : c->Skv - 1;
+    int jlo = c->window > 0 ? i + (c->Skv - c->Sq) - c->window + 1 : 0;
     double* s;
     if (b < 0 || b >= c->B || hq < 0 || hq >= c->Hq || i < 0 || i >= c->Sq) {
         c->err = ORACLE_EINVAL;
@@ -285,7 +323,7 @@ static void rows_item(void* vctx, long item) {
     softmax_row(c->q + ((long)b * c->Sq + i) * q_row_stride + (long)hq * c->d,
                 c->k + (long)b * c->Skv * kv_row_stride + (long)hk * c->d,
                 c->v + (long)b * c->Skv * kv_row_stride + (long)hk * c->d, kv_row_stride, c->d, 0,
-                c->Skv, jmax, c->scale, s, c->o + item * c->d, &c->lse[item]);
+                c->Skv, jmax, jlo, c->n_sink, c->scale, s, c->o + item * c->d, &c->lse[item]);
     free(s);
 }
 
@@ -298,6 +336,24 @@ int oracle_sdpa_rows(const double* q, const double* k, const double* v, int B, i
     if (!q || !k || !v || !rows || !o || !lse) return ORACLE_EINVAL;
     c.q = q; c.k = k; c.v = v;
     c.B = B; c.Hq = Hq; c.Hkv = Hkv; c.Sq = Sq; c.Skv = Skv; c.d = d; c.causal = causal;
+    c.window = 0; c.n_sink = 0;
+    c.scale = scale; c.rows = rows; c.o = o; c.lse = lse; c.err = ORACLE_OK;
+    run_items(rows_item, &c, n_rows, nthreads);
+    return c.err;
+}
+
+/* Selected rows of oracle_sdpa_window. */
+int oracle_sdpa_window_rows(const double* q, const double* k, const double* v, int B, int Hq,
+                            int Hkv, int Sq, int Skv, int d, int window, int n_sink, double scale,
+                            const int* rows, int n_rows, double* o, double* lse, int nthreads) {
+    rows_ctx c;
+    if (!check_dims(B, Hq, Hkv, d) || Sq < 0 || Skv < 0 || n_rows < 0 || window < 1 || n_sink < 0)
+        return ORACLE_EINVAL;
+    if (n_rows == 0) return ORACLE_OK;
+    if (!q || !k || !v || !rows || !o || !lse) return ORACLE_EINVAL;
+    c.q = q; c.k = k; c.v = v;
+    c.B = B; c.Hq = Hq; c.Hkv = Hkv; c.Sq = Sq; c.Skv = Skv; c.d = d; c.causal = 1;
+    c.window = window; c.n_sink = n_sink;
     c.scale = scale; c.rows = rows; c.o = o; c.lse = lse; c.err = ORACLE_OK;
     run_items(rows_item, &c, n_rows, nthreads);
     return c.err;
@@ -352,7 +408,7 @@ static void dec_split_item(void* vctx, long item) {
         long idx = ((long)b * c->Hq + hq) * c->n_splits + s;
         oracle_split_bounds(L, c->n_splits, c->min_rows, s, &lo, &hi);
         /* an empty split: lo == hi gives m = -inf -> O = 0, lse = -inf */
-        softmax_row(q_row, kb, vb, kv_row_stride, c->d, lo, hi, hi - 1, c->scale, sc,
+        softmax_row(q_row, kb, vb, kv_row_stride, c->d, lo, hi, hi - 1, lo, 0, c->scale, sc,
                     c->part_o + idx * c->d, &c->part_lse[idx]);
     }
     free(sc);
@@ -371,7 +427,7 @@ static void dec_full_item(void* vctx, long item) {
     softmax_row(c->q + ((long)b * c->Hq + hq) * c->d,
                 c->kc + (long)b * c->Lmax * kv_row_stride + (long)hk * c->d,
                 c->vc + (long)b * c->Lmax * kv_row_stride + (long)hk * c->d, kv_row_stride, c->d,
-                0, L, L - 1, c->scale, sc, c->o + ((long)b * c->Hq + hq) * c->d,
+                0, L, L - 1, 0, 0, c->scale, sc, c->o + ((long)b * c->Hq + hq) * c->d,
                 &c->lse[(long)b * c->Hq + hq]);
     free(sc);
 }

@@ -198,6 +198,96 @@ def pin_varlen_brute_force(lib=None):
             _close(lse[:, cu[b]:cu[b + 1]], el[0], 1e-12, f"varlen b={b} causal={causal} LSE")
 
 
+def _exact_window(q, k, v, window, n_sink, scale):
+    """Brute force of causal attention over a window plus sinks, with the mask as
+    an explicit key set per query (independent of the oracle's predicate)."""
+    getcontext().prec = 50
+    B, Sq, Hq, d = q.shape
+    _, Skv, Hkv, _ = k.shape
+    group = Hq // Hkv
+    o = np.zeros((B, Sq, Hq, d))
+    lse = np.zeros((B, Hq, Sq))
+    for b in range(B):
+        for h in range(Hq):
+            kvh = h // group
+            for i in range(Sq):
+                p = i + (Skv - Sq)
+                keys = set(range(max(0, p - window + 1), min(p, Skv - 1) + 1)) | set(range(min(n_sink, p + 1, Skv)))
+                allowed = sorted(keys)
+                if not allowed:
+                    lse[b, h, i] = -math.inf
+                    continue
+                ex = []
+                for j in allowed:
+                    s_ = Fraction(scale) * sum(Fraction(float(q[b, i, h, t])) * Fraction(float(k[b, j, kvh, t]))
+                                               for t in range(d))
+                    ex.append((Decimal(s_.numerator) / Decimal(s_.denominator)).exp())
+                Z = sum(ex)
+                for t in range(d):
+                    o[b, i, h, t] = float(sum(e * Decimal(float(v[b, j, kvh, t])) for e, j in zip(ex, allowed)) / Z)
+                lse[b, h, i] = float(Z.ln())
+    return o, lse
+
+
+def pin_window_brute_force(lib=None):
+    """Sliding window plus sinks against the exact brute force, including windows of
+    one position, sinks overlapping the window, Sq < Skv and Sq > Skv."""
+    rng = np.random.default_rng(97531)
+    cases = [  # B, Hq, Hkv, Sq, Skv, d, window, n_sink
+        (1, 2, 1, 9, 9, 3, 3, 2),
+        (1, 2, 2, 7, 7, 2, 1, 0),
+        (2, 4, 2, 4, 10, 3, 4, 3),   # new rows after a history
+        (1, 2, 1, 6, 4, 2, 2, 1),    # more rows than keys: early rows see nothing
+        (1, 1, 1, 8, 8, 4, 5, 8),    # sinks cover everything: plain causal
+    ]
+    for B, Hq, Hkv, Sq, Skv, d, W_, ns in cases:
+        q, k, v = _bf16((B, Sq, Hq, d), rng), _bf16((B, Skv, Hkv, d), rng), _bf16((B, Skv, Hkv, d), rng)
+        o, lse = oracle.sdpa_window(q, k, v, W_, ns, 0.5, lib=lib)
+        eo, el = _exact_window(q, k, v, W_, ns, 0.5)
+        tag = f"window {B, Hq, Hkv, Sq, Skv, d, W_, ns}"
+        _close(o, eo, 1e-12, tag + " O")
+        _close(lse, el, 1e-12, tag + " LSE")
+        rows = [(b, h, i) for b in range(B) for h in range(Hq) for i in range(Sq)]
+        ro, rl = oracle.sdpa_window_rows(q, k, v, W_, ns, 0.5, rows, lib=lib)
+        _close(ro, np.stack([eo[b, i, h] for b, h, i in rows]), 1e-12, tag + " rows O")
+        _close(rl, np.array([el[b, h, i] for b, h, i in rows]), 1e-12, tag + " rows LSE")
+
+
+def pin_window_closed_forms(lib=None):
+    """A window of one position returns the query's own value row (LSE = its own
+    score); a window or sink set covering every key is plain causal attention; and
+    the union of a window and disjoint sinks is the LSE merge of the two branches
+    computed separately (the FMHA page's two-pass form)."""
+    rng = np.random.default_rng(8642)
+    B, Hq, Hkv, S, d = 1, 4, 2, 40, 8
+    q, k, v = _bf16((B, S, Hq, d), rng), _bf16((B, S, Hkv, d), rng), _bf16((B, S, Hkv, d), rng)
+    o, lse = oracle.sdpa_window(q, k, v, 1, 0, 0.3, lib=lib)
+    hk = [h // (Hq // Hkv) for h in range(Hq)]
+    _close(o[0], np.stack([v[0, :, hk[h]] for h in range(Hq)], 1), 1e-12, "window 1 O")
+    own = np.stack([[0.3 * float(np.dot(q[0, i, h].astype(np.float64), k[0, i, hk[h]].astype(np.float64)))
+                     for i in range(S)] for h in range(Hq)])
+    _close(lse[0], own, 1e-12, "window 1 LSE")
+    oc, lc = oracle.sdpa(q, k, v, True, 0.3, lib=lib)
+    for W_, ns in ((S, 0), (10 * S, 3), (2, S)):
+        ow, lw = oracle.sdpa_window(q, k, v, W_, ns, 0.3, lib=lib)
+        _close(ow, oc, 1e-12, f"cover W={W_} sinks={ns} O")
+        _close(lw, lc, 1e-12, f"cover W={W_} sinks={ns} LSE")
+    # two branches: rows i >= W_ + ns have disjoint window [i-W_+1, i] and sinks [0, ns)
+    W_, ns = 6, 4
+    ow, lw = oracle.sdpa_window(q, k, v, W_, ns, 0.3, lib=lib)
+    for i in range(W_ + ns, S):
+        for h in range(Hq):
+            lo = i - W_ + 1
+            win = oracle.sdpa(q[:, i:i + 1], k[:, lo:i + 1], v[:, lo:i + 1], False, 0.3, lib=lib)
+            snk = oracle.sdpa(q[:, i:i + 1], k[:, :ns], v[:, :ns], False, 0.3, lib=lib)
+            lw_, ls_ = win[1][0, h, 0], snk[1][0, h, 0]
+            M = max(lw_, ls_)
+            a, b_ = math.exp(lw_ - M), math.exp(ls_ - M)
+            om = (a * win[0][0, 0, h] + b_ * snk[0][0, 0, h]) / (a + b_)
+            _close(ow[0, i, h], om, 1e-12, f"two-branch merge row {i} O")
+            _close(lw[0, h, i], M + math.log(a + b_), 1e-12, f"two-branch merge row {i} LSE")
+
+
 # ---------------------------------------------------------------- library routine
 def pin_torch_sdpa(lib=None):
     from torch.nn.attention.bias import causal_lower_right
@@ -362,5 +452,5 @@ ALL_PINS = [
     pin_golden_split_merge, pin_golden_split_rule, pin_brute_force_exact, pin_torch_sdpa,
     pin_rows_sum_to_one, pin_permutation_invariance, pin_linearity_in_v,
     pin_split_merge_equals_unsplit, pin_merge_identity, pin_decode_equals_prefill, pin_closed_forms,
-    pin_varlen_brute_force,
+    pin_varlen_brute_force, pin_window_brute_force, pin_window_closed_forms,
 ]

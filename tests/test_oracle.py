@@ -44,6 +44,9 @@ MUTANTS = [
     ("split rule floor", "chunk = ((long)L + n_splits - 1) / n_splits;", "chunk = (long)L / n_splits;"),
     ("decode gqa map modulo", "int G = c->Hq / c->Hkv, hk = hq / G, s, L = c->kv_lens[b];", "int G = c->Hq / c->Hkv, hk = hq % c->Hkv, s, L = c->kv_lens[b];"),
     ("rows: causal bound top-left", "int jmax = c->causal ? i + (c->Skv - c->Sq) : c->Skv - 1;", "int jmax = c->causal ? i : c->Skv - 1;"),
+    ("window off by one", "j <= i + (c->Skv - c->Sq) - c->window)", "j < i + (c->Skv - c->Sq) - c->window)"),
+    ("window sinks ignored", "if (c->window > 0 && j >= c->n_sink &&", "if (c->window > 0 && j >= 0 &&"),
+    ("window rows: lower bound off by one", "int jlo = c->window > 0 ? i + (c->Skv - c->Sq) - c->window + 1 : 0;", "int jlo = c->window > 0 ? i + (c->Skv - c->Sq) - c->window : 0;"),
 ]
 
 
