@@ -50,6 +50,7 @@ def load(path: str | None = None):
         vp, i, f, ull = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_ulonglong
         lib.attn_prefill_fwd.argtypes = [vp, vp, vp, vp, vp] + [i] * 7 + [f, i, vp]
         lib.attn_prefill_varlen.argtypes = [vp] * 7 + [i] * 8 + [f, i, vp]
+        lib.attn_prefill_window.argtypes = [vp] * 5 + [i] * 8 + [f, i, vp]
         lib.attn_decode_split.argtypes = [vp, vp, vp, vp] + [i] * 5 + [f, i, i, vp, vp, vp]
         lib.attn_merge.argtypes = [vp, vp, vp, vp] + [i] * 5 + [vp]
         lib.attn_sync_check.argtypes = [vp]
@@ -60,7 +61,8 @@ def load(path: str | None = None):
         lib.attn_decode_noalloc.argtypes = [vp, vp, vp, vp] + [i] * 5 + [f, i, i, vp, vp, i, vp]
         lib.attn_decode_noalloc_scratch_bytes.argtypes = []
         lib.attn_decode_noalloc_scratch_bytes.restype = ull
-        for name in ("attn_prefill_fwd", "attn_prefill_varlen", "attn_decode_split", "attn_merge",
+        for name in ("attn_prefill_fwd", "attn_prefill_varlen", "attn_prefill_window",
+                     "attn_decode_split", "attn_merge",
                      "attn_sync_check",
                      "attn_version", "attn_debug_wait_timeout", "attn_decode_noalloc"):
             getattr(lib, name).restype = i
@@ -72,6 +74,12 @@ def load(path: str | None = None):
 def attn_prefill_fwd(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, d, causal, scale, o_dtype, stream) -> int:
     return load().attn_prefill_fwd(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, d, int(causal),
                                    float(scale), o_dtype, stream)
+
+
+def attn_prefill_window(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, d, window, n_sink, scale, o_dtype,
+                        stream) -> int:
+    return load().attn_prefill_window(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, d, int(window),
+                                      int(n_sink), float(scale), o_dtype, stream)
 
 
 def attn_prefill_varlen(q, kcache, vcache, o, lse, cu_seqlens_q, kv_lens, B, Hq, Hkv, total_q,
@@ -176,6 +184,31 @@ def prefill(q, k, v, causal: bool = True, scale: float | None = None, out_dtype=
                           causal, scale, _out_code(o.dtype), _stream_handle(stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_prefill_fwd")
+    return o, lse
+
+
+def prefill_window(q, k, v, window: int, n_sink: int = 0, scale: float | None = None,
+                   out_dtype=None, stream=None, out=None):
+    """Causal prefill over a sliding window of ``window`` positions plus the first
+    ``n_sink`` positions.  Shapes as ``prefill``; returns (o, lse)."""
+    torch = _torch()
+    out_dtype = out_dtype or torch.bfloat16
+    _check_tensor(q, "q", torch.bfloat16, 4)
+    _check_tensor(k, "k", torch.bfloat16, 4)
+    _check_tensor(v, "v", torch.bfloat16, 4)
+    B, Sq, Hq, d = q.shape
+    _, Skv, Hkv, _ = k.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        o = torch.empty((B, Sq, Hq, d), dtype=out_dtype, device=q.device)
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    else:
+        o, lse = out
+    rc = attn_prefill_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Skv, d,
+                             window, n_sink, scale, _out_code(o.dtype), _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_prefill_window")
     return o, lse
 
 

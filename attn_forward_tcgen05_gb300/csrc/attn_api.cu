@@ -81,6 +81,40 @@ int from_cuda(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA
 
 }  // namespace
 
+static int prefill_impl(const attn_bf16_t* q, const attn_bf16_t* k, const attn_bf16_t* v, void* o,
+                        float* lse, int B, int Hq, int Hkv, int Sq, int Skv, int d, int causal,
+                        int window, int n_sink, float scale, int o_dtype, attn_stream_t stream) {
+  if (B < 0 || Sq < 0 || Skv < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (!ok_scale(scale)) return ATTN_ERR_INVALID_ARG;
+  if (!ok_dim(d) || (o_dtype != ATTN_F32 && o_dtype != ATTN_BF16)) return ATTN_ERR_UNSUPPORTED;
+  if (B == 0 || Sq == 0) return ATTN_OK;
+  if (!q || !o || !lse || !aligned16(q) || !aligned16(o) || !aligned16(lse))
+    return ATTN_ERR_INVALID_ARG;
+  if (Skv > 0 && (!k || !v || !aligned16(k) || !aligned16(v))) return ATTN_ERR_INVALID_ARG;
+  // row counts of every tensor must fit the kernels' 32-bit row indices
+  if ((long long)B * Sq * Hq >= (1LL << 31) || (long long)B * Skv * Hkv >= (1LL << 31))
+    return ATTN_ERR_INVALID_ARG;
+  attn::PrefillArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.o = o;
+  a.lse = lse;
+  a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.Sq = Sq; a.Skv = Skv; a.d = d;
+  a.causal = causal ? 1 : 0;
+  a.o_bf16 = o_dtype == ATTN_BF16 ? 1 : 0;
+  a.scale = scale;
+  a.window = window;
+  a.n_sink = n_sink;
+  a.err = err_word();
+  if (a.err == nullptr) return ATTN_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (Skv == 0) return from_cuda(attn::launch_prefill_empty_kv(a, s));
+  int rc = encode_bf16_4d(&a.tm_q, q, d, Hq, Sq, B, attn::kPrefillTileM);
+  if (rc == ATTN_OK) rc = encode_bf16_4d(&a.tm_k, k, d, Hkv, Skv, B, attn::prefill_k_box_rows(d));
+  if (rc == ATTN_OK) rc = encode_bf16_4d(&a.tm_v, v, d, Hkv, Skv, B, attn::kPrefillKVStageRows);
+  if (rc != ATTN_OK) return rc;
+  return from_cuda(attn::prefill_uses_pair(d) ? attn::launch_prefill_pair(a, s) : attn::launch_prefill(a, s));
+}
+
 extern "C" {
 
 int attn_version(void) { return 10000; }
@@ -100,33 +134,16 @@ const char* attn_strerror(int status) {
 int attn_prefill_fwd(const attn_bf16_t* q, const attn_bf16_t* k, const attn_bf16_t* v, void* o,
                      float* lse, int B, int Hq, int Hkv, int Sq, int Skv, int d, int causal,
                      float scale, int o_dtype, attn_stream_t stream) {
-  if (B < 0 || Sq < 0 || Skv < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
-  if (!ok_scale(scale)) return ATTN_ERR_INVALID_ARG;
-  if (!ok_dim(d) || (o_dtype != ATTN_F32 && o_dtype != ATTN_BF16)) return ATTN_ERR_UNSUPPORTED;
-  if (B == 0 || Sq == 0) return ATTN_OK;
-  if (!q || !o || !lse || !aligned16(q) || !aligned16(o) || !aligned16(lse))
-    return ATTN_ERR_INVALID_ARG;
-  if (Skv > 0 && (!k || !v || !aligned16(k) || !aligned16(v))) return ATTN_ERR_INVALID_ARG;
-  // row counts of every tensor must fit the kernels' 32-bit row indices
-  if ((long long)B * Sq * Hq >= (1LL << 31) || (long long)B * Skv * Hkv >= (1LL << 31))
-    return ATTN_ERR_INVALID_ARG;
-  attn::PrefillArgs a;
-  std::memset(&a, 0, sizeof(a));
-  a.o = o;
-  a.lse = lse;
-  a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.Sq = Sq; a.Skv = Skv; a.d = d;
-  a.causal = causal ? 1 : 0;
-  a.o_bf16 = o_dtype == ATTN_BF16 ? 1 : 0;
-  a.scale = scale;
-  a.err = err_word();
-  if (a.err == nullptr) return ATTN_ERR_CUDA;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (Skv == 0) return from_cuda(attn::launch_prefill_empty_kv(a, s));
-  int rc = encode_bf16_4d(&a.tm_q, q, d, Hq, Sq, B, attn::kPrefillTileM);
-  if (rc == ATTN_OK) rc = encode_bf16_4d(&a.tm_k, k, d, Hkv, Skv, B, attn::prefill_k_box_rows(d));
-  if (rc == ATTN_OK) rc = encode_bf16_4d(&a.tm_v, v, d, Hkv, Skv, B, attn::kPrefillKVStageRows);
-  if (rc != ATTN_OK) return rc;
-  return from_cuda(attn::prefill_uses_pair(d) ? attn::launch_prefill_pair(a, s) : attn::launch_prefill(a, s));
+  return prefill_impl(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, d, causal, 0, 0, scale, o_dtype, stream);
+}
+
+int attn_prefill_window(const attn_bf16_t* q, const attn_bf16_t* k, const attn_bf16_t* v, void* o,
+                        float* lse, int B, int Hq, int Hkv, int Sq, int Skv, int d, int window,
+                        int n_sink, float scale, int o_dtype, attn_stream_t stream) {
+  if (window < 1 || n_sink < 0) return ATTN_ERR_INVALID_ARG;
+  // the experimental d = 128 pair build has no window support
+  if (ATTN_PREFILL_PAIR_D128 && d == 128) return ATTN_ERR_UNSUPPORTED;
+  return prefill_impl(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, d, 1, window, n_sink, scale, o_dtype, stream);
 }
 
 int attn_prefill_varlen(const attn_bf16_t* q, const attn_bf16_t* kcache, const attn_bf16_t* vcache,

@@ -25,6 +25,8 @@ struct PrefillArgs {
   const int* cu_q;               // [B+1] packed query offsets, or nullptr
   const int* kv_lens;            // [B] keys per sequence (varlen only)
   int total_q;                   // rows of the packed q (varlen only)
+  int window;                    // > 0: causal sliding window of this many positions
+  int n_sink;                    // with a window: the first n_sink keys stay admissible
 };
 
 #ifdef __CUDACC__
@@ -51,6 +53,36 @@ __device__ __forceinline__ SeqExtent seq_extent(int b, int Sq, int Skv, const in
   e.Sq = min(c1 - c0, Sq); e.Skv = kl; e.qbase = c0; e.bq = 0; e.rows = total_q;
   return e;
 }
+
+// KV tiles a CTA visits with a sliding window: the sink tiles, then the tiles
+// from the window start of the CTA's first query row up to its causal bound;
+// the tiles in between hold no admissible key for any of its rows.  List entry
+// u holds key tile u for u < gap_at and key tile u + gap after that.
+struct TileList {
+  int gap_at, gap;
+};
+__device__ __forceinline__ TileList tile_list(long long first_row_pos, int n_kv, int window,
+                                              int n_sink, int Skv, int BN) {
+  TileList L;
+  L.gap_at = n_kv;
+  L.gap = 0;
+  if (window <= 0 || n_kv <= 0) return L;
+  const int sink_keys = n_sink < Skv ? n_sink : Skv;
+  int sink_tiles = (sink_keys + BN - 1) / BN;
+  if (sink_tiles > n_kv) sink_tiles = n_kv;
+  const long long lo = first_row_pos - window + 1;  // first key of the first row's window
+  const int w0 = lo <= 0 ? 0 : (int)(lo / BN < n_kv ? lo / BN : n_kv);
+  if (w0 > sink_tiles) {
+    L.gap_at = sink_tiles;
+    L.gap = w0 - sink_tiles;
+  }
+  return L;
+}
+// list entries holding the key tiles [0, n_key_tiles)
+__device__ __forceinline__ int tile_list_len(const TileList& L, int n_key_tiles) {
+  return n_key_tiles <= L.gap_at ? n_key_tiles : (n_key_tiles - L.gap > L.gap_at ? n_key_tiles - L.gap : L.gap_at);
+}
+__device__ __forceinline__ int tile_list_key(const TileList& L, int u) { return u < L.gap_at ? u : u + L.gap; }
 #endif
 
 // Decode-split launch description.

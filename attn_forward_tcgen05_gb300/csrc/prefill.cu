@@ -150,15 +150,19 @@ __device__ __forceinline__ TileInfo tile_info(int q0, int Sq, int Skv, int causa
   return ti;
 }
 
-template <int D>
+// WIN: causal sliding window with attention sinks (window, n_sink); without it
+// both are ignored and the tile list is every KV tile
+template <int D, bool WIN>
 __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
     fmha_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, void* __restrict__ o_ptr,
                     float* __restrict__ lse_ptr, int Hq, int Hkv, int Sq_max, int Skv_max, int causal,
                     int o_bf16, float scale, int n_units_per_head_batch, uint32_t* err,
-                    const int* __restrict__ cu_q, const int* __restrict__ kv_lens, int total_q) {
+                    const int* __restrict__ cu_q, const int* __restrict__ kv_lens, int total_q,
+                    int window, int n_sink) {
   using C = PrefillCfg<D>;
   constexpr int NQ = C::NQ, NS = C::NS, BN = C::BN;
+  static_assert(C::kSub == 1, "a KV stage is one tile (the sliding-window tile list maps tiles, not stages)");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // ---- work unit: longest causal work first ----
@@ -199,6 +203,14 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
   int n_kv = 0;
 #pragma unroll
   for (int t = 0; t < NQ; ++t) n_kv = max(n_kv, ti[t].n_kv);
+  // with a sliding window the loops below run over a list of KV tiles (list index
+  // j, key tile tile_list_key(tl, j)); without one the list is every tile
+  const long long pos_off = (long long)Skv - Sq;  // key position of query row i: i + pos_off
+  const TileList tl = WIN ? tile_list((long long)ti[0].q0 + pos_off, n_kv, window, n_sink, Skv, BN)
+                          : TileList{0x7FFFFFFF, 0};
+#pragma unroll
+  for (int t = 0; t < NQ; ++t) ti[t].n_kv = tile_list_len(tl, ti[t].n_kv);
+  n_kv = tile_list_len(tl, n_kv);
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
@@ -270,7 +282,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
 #pragma unroll
           for (int p = 0; p < C::kPanels; ++p)
             tma_load_4d_e(sK + s * C::kKVStageBytes + p * C::kKVPanelBytes, &tm_k, &bar_fullK[s], p * 64,
-                          hk, jk * C::kStageRows, b);
+                          hk, tile_list_key(tl, jk) * C::kStageRows, b);
           ++jk;
           continue;
         }
@@ -281,7 +293,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
 #pragma unroll
         for (int p = 0; p < C::kPanels; ++p)
           tma_load_4d_e(sV + s * C::kKVStageBytes + p * C::kKVPanelBytes, &tm_v, &bar_fullV[s], p * 64,
-                        hk, jv * C::kStageRows, b);
+                        hk, tile_list_key(tl, jv) * C::kStageRows, b);
         ++jv;
       }
       if (aborted) {
@@ -424,12 +436,19 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
     const int qrow = my.q0 + r;
     const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
     const float sl2 = scale * kLog2e;
-    // admissible keys of this row: [0, row_bound)
+    // admissible keys of this row: [0, row_bound), and with a sliding window only
+    // [row_lo, row_bound) plus the sinks [0, n_sink)
     int row_bound = Skv;
     if (causal) {
-      const long long rb = (long long)qrow + ((long long)Skv - Sq) + 1;
+      const long long rb = (long long)qrow + pos_off + 1;  // causal bound of this row
       row_bound = (int)(rb < 0 ? 0 : (rb > Skv ? Skv : rb));
     }
+    // (32-bit, clamped: key indices are below 2^31; a bound below 0 masks nothing)
+    auto clamp_key = [](long long x) { return (int)(x < -1 ? -1 : (x > 0x7FFFFFFF ? 0x7FFFFFFF : x)); };
+    const int row_lo = WIN ? clamp_key((long long)qrow + pos_off - window + 1) : -1;
+    // the window start of the tile's last existing row: keys below it need the mask
+    const int tile_lo_max =
+        WIN ? clamp_key((long long)min(Sq, my.q0 + kPrefillTileM) - 1 + pos_off - window + 1) : -1;
     float m_used = -INFINITY, l = 0.f, l_rnd = 0.f;
     bool ok = true;
 
@@ -446,12 +465,19 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
 #pragma unroll
       for (int c0 = 0; c0 < BN; c0 += 32) tmem_ld32(s_addr + c0, sr + c0);
       tmem_wait_ld();
-      // mask: keys at or past row_bound (causal bound or Skv)
-      if ((j + 1) * BN > my.kv_lo) {
-        const int lim = row_bound - j * BN;
+      // mask: keys at or past row_bound (causal bound or Skv), and with a window the
+      // keys below the row's window that are not sinks
+      const int key0 = tile_list_key(tl, j) * BN;
+      if (key0 + BN > my.kv_lo) {
+        const int lim = row_bound - key0;
 #pragma unroll
         for (int c = 0; c < BN; ++c)
           if (c >= lim) sr[c] = __float_as_uint(-INFINITY);
+      }
+      if (WIN && key0 < tile_lo_max && key0 + BN > n_sink) {
+#pragma unroll
+        for (int c = 0; c < BN; ++c)
+          if (key0 + c < row_lo && key0 + c >= n_sink) sr[c] = __float_as_uint(-INFINITY);
       }
       // row max: four independent chains of three-input max
       float mx[4];
@@ -598,7 +624,7 @@ __global__ void fill_empty_kernel(void* o, float* lse, size_t n_o, size_t n_lse,
 template <int D>
 cudaError_t launch_prefill_t(const PrefillArgs& a, cudaStream_t stream) {
   using C = PrefillCfg<D>;
-  auto kern = fmha_fwd_kernel<D>;
+  auto kern = a.window > 0 ? fmha_fwd_kernel<D, true> : fmha_fwd_kernel<D, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int n_blocks_q = (a.Sq + C::NQ * kPrefillTileM - 1) / (C::NQ * kPrefillTileM);
@@ -607,7 +633,7 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, cudaStream_t stream) {
   if (units > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
   kern<<<(unsigned)units, C::kThreads, C::kSmemBytes, stream>>>(
       a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, a.Hq, a.Hkv, a.Sq, a.Skv, a.causal, a.o_bf16, a.scale,
-      a.Hq * a.B, a.err, a.cu_q, a.kv_lens, a.total_q);
+      a.Hq * a.B, a.err, a.cu_q, a.kv_lens, a.total_q, a.window, a.n_sink);
   return cudaGetLastError();
 }
 

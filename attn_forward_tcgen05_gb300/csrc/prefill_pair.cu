@@ -123,13 +123,16 @@ __device__ __forceinline__ void softmax_bar_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(NTHREADS) : "memory");  // the softmax warps of this CTA
 }
 
-template <int D>
+// WIN: causal sliding window with attention sinks (window, n_sink); without it
+// both are ignored and the tile list is every KV tile
+template <int D, bool WIN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<D>::kThreads, 1)
     fmha_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, void* __restrict__ o_ptr,
                      float* __restrict__ lse_ptr, int Hq, int Hkv, int Sq_max, int Skv_max, int causal,
                      int o_bf16, float scale, int n_units_per_head_batch, uint32_t* err,
-                     const int* __restrict__ cu_q, const int* __restrict__ kv_lens, int total_q) {
+                     const int* __restrict__ cu_q, const int* __restrict__ kv_lens, int total_q,
+                     int window, int n_sink) {
   using C = PairCfg<D>;
   constexpr int BN = C::BN, NS = C::NS;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -161,6 +164,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<D>::kThreads
     n_kv = (kv_hi + BN - 1) / BN;
     if (q0_pair >= Sq) n_kv = 0;  // a q-block past the end of this sequence (varlen)
   }
+  // with a sliding window the loops run over a list of KV tiles (list index j, key
+  // tile tile_list_key(tl, j)); both CTAs of the pair derive the same list
+  const TileList tl = WIN ? tile_list((long long)q0_pair + off, n_kv, window, n_sink, Skv, BN)
+                          : TileList{0x7FFFFFFF, 0};
+  n_kv = tile_list_len(tl, n_kv);
   // every existing row of this CTA admits keys [0, kv_lo): tiles past it need a mask
   int kv_lo = Skv;
   if (causal) {
@@ -245,7 +253,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<D>::kThreads
 #pragma unroll
           for (int p = 0; p < C::kPanels; ++p)
             tma_load_4d_pair_e(sK + s * C::kKStageBytes + p * C::kKPanelBytes, &tm_k, full_leader, p * 64,
-                               hk, jk * BN + (int)rank * C::kKRows, b);
+                               hk, tile_list_key(tl, jk) * BN + (int)rank * C::kKRows, b);
           ++jk;
           continue;
         }
@@ -257,7 +265,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<D>::kThreads
 #pragma unroll
         for (int p = 0; p < C::kVPanels; ++p)
           tma_load_4d_pair_e(sV + s * C::kVStageBytes + p * C::kVPanelBytes, &tm_v, full_leader,
-                             ((int)rank * C::kVPanels + p) * 64, hk, jv * BN, b);
+                             ((int)rank * C::kVPanels + p) * 64, hk, tile_list_key(tl, jv) * BN, b);
         ++jv;
       }
       if (aborted) {
@@ -352,6 +360,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<D>::kThreads
       const long long rb = (long long)qrow + off + 1;
       row_bound = (int)(rb < 0 ? 0 : (rb > Skv ? Skv : rb));
     }
+    // with a window only [row_lo, row_bound) plus the sinks [0, n_sink); keys below the
+    // window start of the CTA's last existing row need the mask (32-bit, clamped)
+    auto clamp_key = [](long long x) { return (int)(x < -1 ? -1 : (x > 0x7FFFFFFF ? 0x7FFFFFFF : x)); };
+    const int row_lo = WIN ? clamp_key((long long)qrow + off - window + 1) : -1;
+    const int cta_lo_max =
+        WIN ? clamp_key((long long)min(Sq, q0 + kPrefillTileM) - 1 + off - window + 1) : -1;
     float m_used = -INFINITY, l = 0.f, l_rnd = 0.f;
     bool ok = true;  // cleared by a failed wait; the loop still runs to the end so that
                      // both warpgroups meet at every exchange barrier
@@ -371,12 +385,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<D>::kThreads
         for (int c = 0; c < KC; ++c) sr[c] = __float_as_uint(-INFINITY);
       }
       // mask: keys at or past row_bound (causal bound or Skv)
-      const int key0 = j * BN + KC * h;
+      const int key0 = tile_list_key(tl, j) * BN + KC * h;
       if (key0 + KC > kv_lo) {
         const int lim = row_bound - key0;
 #pragma unroll
         for (int c = 0; c < KC; ++c)
           if (c >= lim) sr[c] = __float_as_uint(-INFINITY);
+      }
+      if (WIN && key0 < cta_lo_max && key0 + KC > n_sink) {
+#pragma unroll
+        for (int c = 0; c < KC; ++c)
+          if (key0 + c < row_lo && key0 + c >= n_sink) sr[c] = __float_as_uint(-INFINITY);
       }
       float mx[4];
 #pragma unroll
@@ -975,7 +994,7 @@ cudaError_t launch_pair_slices(const PrefillArgs& a, cudaStream_t stream) {
 template <int D>
 cudaError_t launch_pair_t(const PrefillArgs& a, cudaStream_t stream) {
   using C = PairCfg<D>;
-  auto kern = fmha_pair_kernel<D>;
+  auto kern = a.window > 0 ? fmha_pair_kernel<D, true> : fmha_pair_kernel<D, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int n_blocks_q = (a.Sq + 2 * kPrefillTileM - 1) / (2 * kPrefillTileM);
@@ -984,7 +1003,7 @@ cudaError_t launch_pair_t(const PrefillArgs& a, cudaStream_t stream) {
   if (2 * units > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
   kern<<<(unsigned)(2 * units), C::kThreads, C::kSmemBytes, stream>>>(
       a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, a.Hq, a.Hkv, a.Sq, a.Skv, a.causal, a.o_bf16, a.scale,
-      a.Hq * a.B, a.err, a.cu_q, a.kv_lens, a.total_q);
+      a.Hq * a.B, a.err, a.cu_q, a.kv_lens, a.total_q, a.window, a.n_sink);
   return cudaGetLastError();
 }
 

@@ -16,6 +16,8 @@ Workloads (names used throughout the tests and the benchmark):
 * ``ragged_gqa_decode_b64`` B=64, Hq=32, Hkv=8, d=128, KV lengths ~ U[512, 8192],
                         at most 8 splits of at least 1024 rows each (1 to 8 per
                         sequence, chosen by its length), O bf16 + LSE fp32
+* ``gqa_prefill_3314_window1024_sink4`` the GQA prefill inputs, causal over a
+                        1024-position sliding window plus 4 sink positions
 * ``chunked_prefill_gqa_b8`` packed variable-length prefill against a KV cache:
                         B=8, Hq=28, Hkv=4, d=128, causal, 64-1024 new rows per
                         sequence after 0-3072 cached ones, O bf16 + LSE fp32
@@ -96,6 +98,41 @@ class VarlenShape:
 # tokens each after 0-3072 cached ones
 CHUNKED_PREFILL = VarlenShape("chunked_prefill_gqa_b8", 8, 28, 4, 128, True, 1.0 / math.sqrt(128.0),
                               (64, 1024), (0, 3072), 1006)
+
+
+@dataclass(frozen=True)
+class WindowShape:
+    """Causal prefill over a sliding window of ``window`` positions plus ``n_sink``
+    attention-sink positions, on the inputs of ``base``."""
+    name: str
+    base: PrefillShape
+    window: int
+    n_sink: int
+
+
+# the GQA prefill shape with a 1024-position window and 4 sink positions
+WINDOW_PREFILL = WindowShape("gqa_prefill_3314_window1024_sink4", GQA_PREFILL, 1024, 4)
+
+
+def window_pairs(Sq: int, Skv: int, window: int, n_sink: int) -> int:
+    """Admissible (query, key) pairs of one head of a windowed causal prefill."""
+    total = 0
+    for i in range(Sq):
+        p = i + Skv - Sq
+        if p < 0:
+            continue
+        hi = min(p, Skv - 1)
+        lo = max(0, p - window + 1)
+        win = max(0, hi - lo + 1)
+        sinks = max(0, min(n_sink, hi + 1, lo))  # sink keys below the window
+        total += win + sinks
+    return total
+
+
+def window_flops(s: WindowShape) -> int:
+    """Algorithmic FLOPs: 4*d per admissible (query, key) pair."""
+    b = s.base
+    return 4 * b.d * b.B * b.Hq * window_pairs(b.Sq, b.Skv, s.window, s.n_sink)
 
 
 def _gen(seed: int) -> torch.Generator:

@@ -214,6 +214,8 @@ def run_ours(args, rank, world, local_rank):
 
     # ---- packed variable-length prefill (chunked prefill against a KV cache) ----
     varlen = None if args.only else time_varlen(args, attn, W, dev, stream, flush, peaks, peak_src)
+    # ---- causal sliding window with attention sinks ----
+    window = None if args.only else time_window(args, attn, W, dev, stream, flush, peaks, peak_src)
 
     # ---- end to end through the public API with host buffers ----
     e2e = None if (args.no_e2e or args.only) else run_e2e(args, attn, W, dev, stream, P, dec, flops)
@@ -287,6 +289,7 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": (int(do_prefill) + 4 * int(do_decode)) * args.steps,
         "e2e": e2e,
         "prefill_varlen": varlen,
+        "prefill_window": window,
         "clocks": clocks,
     }
     return line
@@ -326,6 +329,45 @@ def time_varlen(args, attn, W, dev, stream, flush, peaks, peak_src):
             "total_q": int(q.shape[0]), "kv_tokens": int(kv.sum()), "gflop": round(flops / 1e9, 3),
             "us": round(ms * 1e3, 2), "value": round(tf, 2), "unit": "TFLOP/s", "steps": n,
             "roofline": {"bound": "tensor", "kernel": "fmha_fwd_kernel<128>", "achieved": round(tf, 2),
+                         "peak": peak_tc, "unit": "TFLOP/s", "frac": round(tf / peak_tc, 4),
+                         "peak_source": f"bf16_tflops (burst) of {peak_src}"}}
+
+
+def time_window(args, attn, W, dev, stream, flush, peaks, peak_src):
+    """Causal sliding-window prefill with attention sinks: average launch time of
+    attn_prefill_window over the timed iterations, L2 flushed before each.  The
+    FLOPs count only admissible (query, key) pairs."""
+    import torch
+
+    S = W.WINDOW_PREFILL
+    P = S.base
+    q, k, v = (t.to(dev) for t in W.prefill_inputs_for(P))
+    flops = W.window_flops(S)
+    o = torch.empty((P.B, P.Sq, P.Hq, P.d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((P.B, P.Hq, P.Sq), dtype=torch.float32, device=dev)
+
+    def call():
+        attn.prefill_window(q, k, v, S.window, S.n_sink, scale=P.scale, out=(o, lse))
+
+    for _ in range(args.warmup):
+        call()
+    n = max(1, min(args.steps, 50))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for a, b in evs:
+        flush.zero_()
+        a.record(stream)
+        call()
+        b.record(stream)
+    torch.cuda.synchronize()
+    attn.sync_check()
+    ms = sum(a.elapsed_time(b) for a, b in evs) / n
+    tf = flops / (ms * 1e-3) / 1e12
+    peak_tc = float(peaks["bf16_tflops"])
+    kern = f"fmha_pair_kernel<{P.d}>" if P.d == 256 else f"fmha_fwd_kernel<{P.d}>"
+    return {"workload": S.name, "B": P.B, "Hq": P.Hq, "Hkv": P.Hkv, "S": P.Sq, "d": P.d,
+            "window": S.window, "n_sink": S.n_sink, "gflop": round(flops / 1e9, 3),
+            "us": round(ms * 1e3, 2), "value": round(tf, 2), "unit": "TFLOP/s", "steps": n,
+            "roofline": {"bound": "tensor", "kernel": kern, "achieved": round(tf, 2),
                          "peak": peak_tc, "unit": "TFLOP/s", "frac": round(tf / peak_tc, 4),
                          "peak_source": f"bf16_tflops (burst) of {peak_src}"}}
 

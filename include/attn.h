@@ -90,6 +90,29 @@ int attn_prefill_fwd(const attn_bf16_t* q, const attn_bf16_t* k, const attn_bf16
                      float scale, int o_dtype, attn_stream_t stream);
 
 /*
+ * attn_prefill_window -- causal prefill over a sliding window plus attention sinks.
+ *
+ * As attn_prefill_fwd with causal = 1, except that query row i (key position
+ * p = i + Skv - Sq) admits only the keys
+ *   p - window < j <= p     (the last `window` positions, its own included)
+ *   j < n_sink, j <= p      (the first n_sink positions, always visible)
+ * A row with no admissible key gets O = 0 and LSE = -inf.  Only the KV tiles
+ * that hold admissible keys are read: the sink tiles and the tiles of the
+ * window.  This is one launch computing what "STAGE_D.md -- FMHA Kernel
+ * Development", D3-D5, builds from two passes (a sliding-window branch with
+ * its length and causal masks, and a sink branch) merged through their LSEs:
+ * the softmax over the union of the two key sets.
+ *
+ * Arguments: as attn_prefill_fwd, plus
+ *   window   >= 1: positions in the window (window >= Skv is plain causal attention)
+ *   n_sink   >= 0: leading sink positions
+ * Returns ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED or ATTN_ERR_CUDA.
+ */
+int attn_prefill_window(const attn_bf16_t* q, const attn_bf16_t* k, const attn_bf16_t* v, void* o,
+                        float* lse, int B, int Hq, int Hkv, int Sq, int Skv, int d, int window,
+                        int n_sink, float scale, int o_dtype, attn_stream_t stream);
+
+/*
  * attn_prefill_varlen -- prefill of a packed batch of sequences of different
  * lengths against a KV cache (chunked prefill).
  *

@@ -21,7 +21,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 sys.path.insert(0, ROOT)
 
 import oracle  # noqa: E402
-from attn_forward_tcgen05_gb300 import decode, prefill, sync_check  # noqa: E402
+from attn_forward_tcgen05_gb300 import decode, prefill, prefill_window, sync_check  # noqa: E402
 from attn_forward_tcgen05_gb300 import workloads as W  # noqa: E402
 
 REPS = 20
@@ -85,6 +85,22 @@ def prefill_row(label, s, peak_tc):
             f"| {e32:.2e} (fp32 O); {e16:.2e} (bf16 O) | {el:.2e} | {cpu_s:.2f} s ({oracle.num_cores()} cores) |")
 
 
+def window_row(label, s, peak_tc):
+    b = s.base
+    q, k, v = W.prefill_inputs_for(b)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o, lse = prefill_window(qd, kd, vd, s.window, s.n_sink, scale=b.scale, out_dtype=torch.float32)
+    ms = gpu_time_ms(lambda: prefill_window(qd, kd, vd, s.window, s.n_sink, scale=b.scale, out=(o, lse)))
+    t0 = time.perf_counter()
+    ro, rl = oracle.sdpa_window(q, k, v, s.window, s.n_sink, b.scale)
+    cpu_s = time.perf_counter() - t0
+    tf = W.window_flops(s) / (ms * 1e-3) / 1e12
+    eo = max_err(o.cpu().numpy(), ro)
+    el = max_err(lse.cpu().numpy(), rl)
+    return (f"| {label} | {ms * 1e3:.1f} µs | {tf:.1f} TFLOP/s | {tf / peak_tc:.3f} of {peak_tc:.1f} TFLOP/s "
+            f"| {eo:.2e} (fp32 O) | {el:.2e} | {cpu_s:.2f} s ({oracle.num_cores()} cores) |")
+
+
 def decode_row(label, s, peak_hbm):
     q, kc, vc, lens = W.decode_inputs_for(s)
     qd, kd, vd, ld = q.cuda(), kc.cuda(), vc.cuda(), lens.cuda()
@@ -112,6 +128,7 @@ def main():
     for d in (64, 128, 256):
         print(prefill_row(f"C4 non-causal MHA, S = 4096, d = {d}", W.mha_sweep(d), peak_tc), flush=True)
     print(decode_row("C5 ragged GQA decode, B = 64", W.RAGGED_DECODE, peak_hbm), flush=True)
+    print(window_row("GQA prefill S = 3314, window 1024 + 4 sinks", W.WINDOW_PREFILL, peak_tc), flush=True)
 
 
 if __name__ == "__main__":

@@ -57,6 +57,21 @@ def test_prefill_validation(lib):
     assert f(N, N, N, N, N, 2, 2, 2, 0, 4, 64, 1, 0.5, 0, N) == attn.ATTN_OK  # no queries: no-op
 
 
+def test_prefill_window_validation(lib):
+    f = attn.attn_prefill_window
+    #      q  k  v  o  lse B  Hq Hkv Sq Skv d  win sink scale dtype stream
+    assert f(P, P, P, P, P, 1, 2, 2, 4, 4, 96, 8, 0, 0.5, 0, N) == attn.ATTN_ERR_UNSUPPORTED  # d
+    assert f(P, P, P, P, P, 1, 2, 2, 4, 4, 64, 8, 0, 0.5, 5, N) == attn.ATTN_ERR_UNSUPPORTED  # dtype
+    assert f(P, P, P, P, P, 1, 2, 2, 4, 4, 64, 0, 0, 0.5, 0, N) == attn.ATTN_ERR_INVALID_ARG  # window 0
+    assert f(P, P, P, P, P, 1, 2, 2, 4, 4, 64, -3, 0, 0.5, 0, N) == attn.ATTN_ERR_INVALID_ARG  # window < 0
+    assert f(P, P, P, P, P, 1, 2, 2, 4, 4, 64, 8, -1, 0.5, 0, N) == attn.ATTN_ERR_INVALID_ARG  # n_sink < 0
+    assert f(P, P, P, P, P, 1, 3, 2, 4, 4, 64, 8, 0, 0.5, 0, N) == attn.ATTN_ERR_INVALID_ARG  # Hq % Hkv
+    assert f(P, P, P, P, P, 1, 2, 2, 4, 4, 64, 8, 0, -1.0, 0, N) == attn.ATTN_ERR_INVALID_ARG  # scale
+    assert f(P, M, P, P, P, 1, 2, 2, 4, 4, 64, 8, 0, 0.5, 0, N) == attn.ATTN_ERR_INVALID_ARG  # misaligned k
+    assert f(N, N, N, N, N, 0, 2, 2, 4, 4, 64, 8, 4, 0.5, 0, N) == attn.ATTN_OK  # empty batch
+    assert f(N, N, N, N, N, 2, 2, 2, 0, 4, 64, 8, 4, 0.5, 0, N) == attn.ATTN_OK  # no queries
+
+
 def test_prefill_varlen_validation(lib):
     f = attn.attn_prefill_varlen
     #      q  kc vc o  lse cu kv  B  Hq Hkv tot msq mkv d  causal scale dtype stream
