@@ -51,6 +51,7 @@ def load(path: str | None = None):
         lib.attn_prefill_fwd.argtypes = [vp, vp, vp, vp, vp] + [i] * 7 + [f, i, vp]
         lib.attn_prefill_varlen.argtypes = [vp] * 7 + [i] * 8 + [f, i, vp]
         lib.attn_prefill_window.argtypes = [vp] * 5 + [i] * 8 + [f, i, vp]
+        lib.attn_prefill_varlen_window.argtypes = [vp] * 7 + [i] * 9 + [f, i, vp]
         lib.attn_decode_split.argtypes = [vp, vp, vp, vp] + [i] * 5 + [f, i, i, vp, vp, vp]
         lib.attn_merge.argtypes = [vp, vp, vp, vp] + [i] * 5 + [vp]
         lib.attn_sync_check.argtypes = [vp]
@@ -62,6 +63,7 @@ def load(path: str | None = None):
         lib.attn_decode_noalloc_scratch_bytes.argtypes = []
         lib.attn_decode_noalloc_scratch_bytes.restype = ull
         for name in ("attn_prefill_fwd", "attn_prefill_varlen", "attn_prefill_window",
+                     "attn_prefill_varlen_window",
                      "attn_decode_split", "attn_merge",
                      "attn_sync_check",
                      "attn_version", "attn_debug_wait_timeout", "attn_decode_noalloc"):
@@ -87,6 +89,14 @@ def attn_prefill_varlen(q, kcache, vcache, o, lse, cu_seqlens_q, kv_lens, B, Hq,
     return load().attn_prefill_varlen(q, kcache, vcache, o, lse, cu_seqlens_q, kv_lens, B, Hq, Hkv,
                                       total_q, max_sq, max_kv, d, int(causal), float(scale), o_dtype,
                                       stream)
+
+
+def attn_prefill_varlen_window(q, kcache, vcache, o, lse, cu_seqlens_q, kv_lens, B, Hq, Hkv,
+                               total_q, max_sq, max_kv, d, window, n_sink, scale, o_dtype,
+                               stream) -> int:
+    return load().attn_prefill_varlen_window(q, kcache, vcache, o, lse, cu_seqlens_q, kv_lens, B, Hq,
+                                             Hkv, total_q, max_sq, max_kv, d, int(window), int(n_sink),
+                                             float(scale), o_dtype, stream)
 
 
 def attn_decode_split(q, kcache, vcache, kv_lens, B, Hq, Hkv, d, max_kv, scale, n_splits,
@@ -213,12 +223,15 @@ def prefill_window(q, k, v, window: int, n_sink: int = 0, scale: float | None = 
 
 
 def prefill_varlen(q, kcache, vcache, cu_seqlens_q, kv_lens, max_sq: int, causal: bool = True,
-                   scale: float | None = None, out_dtype=None, stream=None, out=None):
+                   scale: float | None = None, out_dtype=None, stream=None, out=None,
+                   window: int = 0, n_sink: int = 0):
     """Packed variable-length prefill against a KV cache (chunked prefill).
 
     q [total_q,Hq,d] bf16 (sequences concatenated), kcache/vcache [B,max_kv,Hkv,d] bf16,
     cu_seqlens_q int32 [B+1] and kv_lens int32 [B] on the GPU; max_sq >= the longest
-    sequence.  Returns (o [total_q,Hq,d] in out_dtype (default bf16), lse [Hq,total_q] fp32)."""
+    sequence.  window > 0 selects the causal sliding window of that many positions
+    plus n_sink sink positions (attn_prefill_varlen_window; causal must be True).
+    Returns (o [total_q,Hq,d] in out_dtype (default bf16), lse [Hq,total_q] fp32)."""
     torch = _torch()
     out_dtype = out_dtype or torch.bfloat16
     _check_tensor(q, "q", torch.bfloat16, 3)
@@ -237,6 +250,16 @@ def prefill_varlen(q, kcache, vcache, cu_seqlens_q, kv_lens, max_sq: int, causal
         lse = torch.empty((Hq, total_q), dtype=torch.float32, device=q.device)
     else:
         o, lse = out
+    if window:
+        if not causal:
+            raise ValueError("a sliding window is causal")
+        rc = attn_prefill_varlen_window(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(o), _ptr(lse),
+                                        _ptr(cu_seqlens_q), _ptr(kv_lens), B, Hq, Hkv, total_q,
+                                        int(max_sq), max_kv, d, window, n_sink, scale,
+                                        _out_code(o.dtype), _stream_handle(stream))
+        if rc != ATTN_OK:
+            raise AttnError(rc, "attn_prefill_varlen_window")
+        return o, lse
     rc = attn_prefill_varlen(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(o), _ptr(lse),
                              _ptr(cu_seqlens_q), _ptr(kv_lens), B, Hq, Hkv, total_q, int(max_sq),
                              max_kv, d, causal, scale, _out_code(o.dtype), _stream_handle(stream))

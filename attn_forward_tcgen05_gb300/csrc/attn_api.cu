@@ -115,6 +115,48 @@ static int prefill_impl(const attn_bf16_t* q, const attn_bf16_t* k, const attn_b
   return from_cuda(attn::prefill_uses_pair(d) ? attn::launch_prefill_pair(a, s) : attn::launch_prefill(a, s));
 }
 
+static int varlen_impl(const attn_bf16_t* q, const attn_bf16_t* kcache, const attn_bf16_t* vcache,
+                       void* o, float* lse, const int* cu_seqlens_q, const int* kv_lens, int B, int Hq,
+                       int Hkv, int total_q, int max_sq, int max_kv, int d, int causal, int window,
+                       int n_sink, float scale, int o_dtype, attn_stream_t stream) {
+  if (B < 0 || total_q < 0 || max_sq < 0 || max_kv < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (!ok_scale(scale)) return ATTN_ERR_INVALID_ARG;
+  if (!ok_dim(d) || (o_dtype != ATTN_F32 && o_dtype != ATTN_BF16)) return ATTN_ERR_UNSUPPORTED;
+  if (B == 0 || total_q == 0 || max_sq == 0) return ATTN_OK;
+  if (!q || !o || !lse || !aligned16(q) || !aligned16(o) || !aligned16(lse)) return ATTN_ERR_INVALID_ARG;
+  if (!cu_seqlens_q || !kv_lens || (reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3) ||
+      (reinterpret_cast<uintptr_t>(kv_lens) & 3))
+    return ATTN_ERR_INVALID_ARG;
+  if (max_kv > 0 && (!kcache || !vcache || !aligned16(kcache) || !aligned16(vcache)))
+    return ATTN_ERR_INVALID_ARG;
+  if ((long long)total_q * Hq >= (1LL << 31) || (long long)B * max_kv * Hkv >= (1LL << 31))
+    return ATTN_ERR_INVALID_ARG;
+  attn::PrefillArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.o = o;
+  a.lse = lse;
+  a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.Sq = max_sq; a.Skv = max_kv; a.d = d;
+  a.causal = causal ? 1 : 0;
+  a.o_bf16 = o_dtype == ATTN_BF16 ? 1 : 0;
+  a.scale = scale;
+  a.window = window;
+  a.n_sink = n_sink;
+  a.cu_q = cu_seqlens_q;
+  a.kv_lens = kv_lens;
+  a.total_q = total_q;
+  a.err = err_word();
+  if (a.err == nullptr) return ATTN_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (max_kv == 0) return from_cuda(attn::launch_prefill_empty_kv(a, s));
+  // packed q is one batch slab of total_q rows; the cache keeps its batch dimension
+  int rc = encode_bf16_4d(&a.tm_q, q, d, Hq, total_q, 1, attn::kPrefillTileM);
+  if (rc == ATTN_OK) rc = encode_bf16_4d(&a.tm_k, kcache, d, Hkv, max_kv, B, attn::prefill_k_box_rows(d));
+  if (rc == ATTN_OK) rc = encode_bf16_4d(&a.tm_v, vcache, d, Hkv, max_kv, B, attn::kPrefillKVStageRows);
+  if (rc != ATTN_OK) return rc;
+  return from_cuda(attn::prefill_uses_pair(d) ? attn::launch_prefill_pair(a, s) : attn::launch_prefill(a, s));
+}
+
 extern "C" {
 
 int attn_version(void) { return 10000; }
@@ -150,40 +192,20 @@ int attn_prefill_varlen(const attn_bf16_t* q, const attn_bf16_t* kcache, const a
                         void* o, float* lse, const int* cu_seqlens_q, const int* kv_lens, int B,
                         int Hq, int Hkv, int total_q, int max_sq, int max_kv, int d, int causal,
                         float scale, int o_dtype, attn_stream_t stream) {
-  if (B < 0 || total_q < 0 || max_sq < 0 || max_kv < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0)
-    return ATTN_ERR_INVALID_ARG;
-  if (!ok_scale(scale)) return ATTN_ERR_INVALID_ARG;
-  if (!ok_dim(d) || (o_dtype != ATTN_F32 && o_dtype != ATTN_BF16)) return ATTN_ERR_UNSUPPORTED;
-  if (B == 0 || total_q == 0 || max_sq == 0) return ATTN_OK;
-  if (!q || !o || !lse || !aligned16(q) || !aligned16(o) || !aligned16(lse)) return ATTN_ERR_INVALID_ARG;
-  if (!cu_seqlens_q || !kv_lens || (reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3) ||
-      (reinterpret_cast<uintptr_t>(kv_lens) & 3))
-    return ATTN_ERR_INVALID_ARG;
-  if (max_kv > 0 && (!kcache || !vcache || !aligned16(kcache) || !aligned16(vcache)))
-    return ATTN_ERR_INVALID_ARG;
-  if ((long long)total_q * Hq >= (1LL << 31) || (long long)B * max_kv * Hkv >= (1LL << 31))
-    return ATTN_ERR_INVALID_ARG;
-  attn::PrefillArgs a;
-  std::memset(&a, 0, sizeof(a));
-  a.o = o;
-  a.lse = lse;
-  a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.Sq = max_sq; a.Skv = max_kv; a.d = d;
-  a.causal = causal ? 1 : 0;
-  a.o_bf16 = o_dtype == ATTN_BF16 ? 1 : 0;
-  a.scale = scale;
-  a.cu_q = cu_seqlens_q;
-  a.kv_lens = kv_lens;
-  a.total_q = total_q;
-  a.err = err_word();
-  if (a.err == nullptr) return ATTN_ERR_CUDA;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (max_kv == 0) return from_cuda(attn::launch_prefill_empty_kv(a, s));
-  // packed q is one batch slab of total_q rows; the cache keeps its batch dimension
-  int rc = encode_bf16_4d(&a.tm_q, q, d, Hq, total_q, 1, attn::kPrefillTileM);
-  if (rc == ATTN_OK) rc = encode_bf16_4d(&a.tm_k, kcache, d, Hkv, max_kv, B, attn::prefill_k_box_rows(d));
-  if (rc == ATTN_OK) rc = encode_bf16_4d(&a.tm_v, vcache, d, Hkv, max_kv, B, attn::kPrefillKVStageRows);
-  if (rc != ATTN_OK) return rc;
-  return from_cuda(attn::prefill_uses_pair(d) ? attn::launch_prefill_pair(a, s) : attn::launch_prefill(a, s));
+  return varlen_impl(q, kcache, vcache, o, lse, cu_seqlens_q, kv_lens, B, Hq, Hkv, total_q, max_sq,
+                     max_kv, d, causal, 0, 0, scale, o_dtype, stream);
+}
+
+int attn_prefill_varlen_window(const attn_bf16_t* q, const attn_bf16_t* kcache,
+                               const attn_bf16_t* vcache, void* o, float* lse,
+                               const int* cu_seqlens_q, const int* kv_lens, int B, int Hq, int Hkv,
+                               int total_q, int max_sq, int max_kv, int d, int window, int n_sink,
+                               float scale, int o_dtype, attn_stream_t stream) {
+  if (window < 1 || n_sink < 0) return ATTN_ERR_INVALID_ARG;
+  // the experimental d = 128 pair build has no window support
+  if (ATTN_PREFILL_PAIR_D128 && d == 128) return ATTN_ERR_UNSUPPORTED;
+  return varlen_impl(q, kcache, vcache, o, lse, cu_seqlens_q, kv_lens, B, Hq, Hkv, total_q, max_sq,
+                     max_kv, d, 1, window, n_sink, scale, o_dtype, stream);
 }
 
 int attn_decode_split(const attn_bf16_t* q, const attn_bf16_t* kcache, const attn_bf16_t* vcache,

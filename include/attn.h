@@ -150,6 +150,27 @@ int attn_prefill_varlen(const attn_bf16_t* q, const attn_bf16_t* kcache, const a
                         float scale, int o_dtype, attn_stream_t stream);
 
 /*
+ * attn_prefill_varlen_window -- packed variable-length prefill against a KV
+ * cache with a causal sliding window and attention sinks.
+ *
+ * As attn_prefill_varlen with causal = 1, except that row i of sequence b (key
+ * position p = i + L_b - Sq_b) admits only the keys p - window < j <= p and the
+ * sinks j < n_sink (j <= p), all below L_b.  kv_lens plays the part of the
+ * per-sequence window length of "STAGE_D.md -- FMHA Kernel Development", D3;
+ * the window and sink sets are those of attn_prefill_window (D4, D5).
+ *
+ * Arguments: as attn_prefill_varlen without `causal`, plus
+ *   window   >= 1: positions in the window
+ *   n_sink   >= 0: leading sink positions
+ * Returns ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED or ATTN_ERR_CUDA.
+ */
+int attn_prefill_varlen_window(const attn_bf16_t* q, const attn_bf16_t* kcache,
+                               const attn_bf16_t* vcache, void* o, float* lse,
+                               const int* cu_seqlens_q, const int* kv_lens, int B, int Hq, int Hkv,
+                               int total_q, int max_sq, int max_kv, int d, int window, int n_sink,
+                               float scale, int o_dtype, attn_stream_t stream);
+
+/*
  * attn_decode_split -- one-token GQA decode, split-KV partials.
  *
  * For every batch b, KV head hk and split s, the rows [lo, hi) of sequence b

@@ -178,6 +178,30 @@ def sdpa_varlen(q, kcache, vcache, cu_seqlens_q, kv_lens, causal: bool, scale: f
     return o, lse
 
 
+def sdpa_varlen_window(q, kcache, vcache, cu_seqlens_q, kv_lens, window: int, n_sink: int,
+                       scale: float, nthreads: int = 0, lib=None):
+    """Packed variable-length causal prefill over a sliding window plus sinks:
+    every sequence b is ``sdpa_window`` of its own rows q[cu[b]:cu[b+1]] against the
+    keys kcache[b, :kv_lens[b]].  Layouts as ``sdpa_varlen``.  kv_lens is the
+    per-sequence window length of the sliding-window items (D3) of "STAGE_D.md --
+    FMHA Kernel Development"; the per-sequence computation is ``sdpa_window``."""
+    q, kc, vc = _f64(q), _f64(kcache), _f64(vcache)
+    cu = [int(x) for x in np.asarray(cu_seqlens_q).reshape(-1)]
+    lens = [int(x) for x in np.asarray(kv_lens).reshape(-1)]
+    total_q, Hq, d = q.shape
+    o = np.zeros((total_q, Hq, d), np.float64)
+    lse = np.full((Hq, total_q), -np.inf, np.float64)
+    for b, L in enumerate(lens):
+        c0, c1 = cu[b], cu[b + 1]
+        if c1 <= c0:
+            continue
+        ob, lb = sdpa_window(q[None, c0:c1], kc[b:b + 1, :L], vc[b:b + 1, :L], window, n_sink, scale,
+                             nthreads, lib)
+        o[c0:c1] = ob[0]
+        lse[:, c0:c1] = lb[0]
+    return o, lse
+
+
 def sdpa_rows(q, k, v, causal: bool, scale: float, rows, nthreads: int = 0, lib=None):
     """Exact attention for selected rows ``rows`` = [(b, hq, i), ...].
 

@@ -253,6 +253,30 @@ def pin_window_brute_force(lib=None):
         _close(rl, np.array([el[b, h, i] for b, h, i in rows]), 1e-12, tag + " rows LSE")
 
 
+def pin_varlen_window_brute_force(lib=None):
+    """Packed sequences with a sliding window and sinks: every sequence against the
+    explicit-key-set brute force of its own rows and keys (offsets, per-sequence key
+    counts, the window measured from each sequence's own bottom-right position)."""
+    rng = np.random.default_rng(1357)
+    Hq, Hkv, d, max_kv = 4, 2, 3, 12
+    seqs = [(3, 9), (0, 4), (5, 5), (2, 12), (4, 2), (1, 0)]  # (new query rows, keys)
+    B = len(seqs)
+    cu = np.cumsum([0] + [sq for sq, _ in seqs]).astype(np.int32)
+    lens = np.array([L for _, L in seqs], np.int32)
+    q = _bf16((int(cu[-1]), Hq, d), rng)
+    kc = _bf16((B, max_kv, Hkv, d), rng)
+    vc = _bf16((B, max_kv, Hkv, d), rng)
+    for W_, ns in ((3, 2), (1, 0), (4, 5)):
+        o, lse = oracle.sdpa_varlen_window(q, kc, vc, cu, lens, W_, ns, 0.5, lib=lib)
+        assert o.shape == (cu[-1], Hq, d) and lse.shape == (Hq, cu[-1])
+        for b, (sq, L) in enumerate(seqs):
+            if sq == 0:
+                continue
+            eo, el = _exact_window(q[None, cu[b]:cu[b + 1]], kc[b:b + 1, :L], vc[b:b + 1, :L], W_, ns, 0.5)
+            _close(o[cu[b]:cu[b + 1]], eo[0], 1e-12, f"varlen window b={b} W={W_} sinks={ns} O")
+            _close(lse[:, cu[b]:cu[b + 1]], el[0], 1e-12, f"varlen window b={b} W={W_} sinks={ns} LSE")
+
+
 def pin_window_closed_forms(lib=None):
     """A window of one position returns the query's own value row (LSE = its own
     score); a window or sink set covering every key is plain causal attention; and
@@ -453,4 +477,5 @@ ALL_PINS = [
     pin_rows_sum_to_one, pin_permutation_invariance, pin_linearity_in_v,
     pin_split_merge_equals_unsplit, pin_merge_identity, pin_decode_equals_prefill, pin_closed_forms,
     pin_varlen_brute_force, pin_window_brute_force, pin_window_closed_forms,
+    pin_varlen_window_brute_force,
 ]

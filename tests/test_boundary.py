@@ -88,6 +88,17 @@ def test_prefill_varlen_validation(lib):
     assert f(N, N, N, N, N, N, N, 3, 2, 2, 0, 0, 16, 64, 1, 0.5, 0, N) == attn.ATTN_OK  # no query rows
 
 
+def test_prefill_varlen_window_validation(lib):
+    f = attn.attn_prefill_varlen_window
+    #      q  kc vc o  lse cu kv  B  Hq Hkv tot msq mkv d  win sink scale dtype stream
+    assert f(P, P, P, P, P, P, P, 2, 2, 2, 10, 8, 16, 96, 4, 0, 0.5, 0, N) == attn.ATTN_ERR_UNSUPPORTED  # d
+    assert f(P, P, P, P, P, P, P, 2, 2, 2, 10, 8, 16, 64, 0, 0, 0.5, 0, N) == attn.ATTN_ERR_INVALID_ARG  # window
+    assert f(P, P, P, P, P, P, P, 2, 2, 2, 10, 8, 16, 64, 4, -2, 0.5, 0, N) == attn.ATTN_ERR_INVALID_ARG  # n_sink
+    assert f(P, P, P, P, P, N, P, 2, 2, 2, 10, 8, 16, 64, 4, 0, 0.5, 0, N) == attn.ATTN_ERR_INVALID_ARG  # null cu
+    assert f(P, P, P, P, P, P, P, 2, 3, 2, 10, 8, 16, 64, 4, 0, 0.5, 0, N) == attn.ATTN_ERR_INVALID_ARG  # Hq % Hkv
+    assert f(N, N, N, N, N, N, N, 0, 2, 2, 10, 8, 16, 64, 4, 0, 0.5, 0, N) == attn.ATTN_OK  # empty batch
+
+
 def test_decode_and_merge_validation(lib):
     f = attn.attn_decode_split
     assert f(P, P, P, P, 1, 28, 4, 96, 10, 0.1, 8, 1, P, P, N) == attn.ATTN_ERR_UNSUPPORTED

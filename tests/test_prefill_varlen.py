@@ -97,3 +97,24 @@ def test_chunked_prefill_workload_sampled():
         got_l = np.array([lse[h, c0 + i] for _, h, i in rows])
         check_o(got_o, ro, True, f"O seq {b}")
         check_lse(got_l, rl, f"LSE seq {b}")
+
+
+# sequences for the windowed packed batch: rows past a long history (the window
+# leaves the sinks behind), a chunk shorter than the window, a single token, an
+# empty sequence, fewer keys than rows, and sinks spanning two KV tiles
+WINDOW_MIXED = [(200, 1500), (90, 90), (1, 700), (0, 64), (150, 100), (300, 600)]
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("window,n_sink", [(1, 0), (100, 4), (256, 130), (2000, 7)])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_mixed_batch_window(d, window, n_sink, out_dtype):
+    q, kc, vc, cu, kv = _case(WINDOW_MIXED, 4, 2, d, 80 + d + window)
+    scale = 1.0 / np.sqrt(d)
+    max_sq = int((cu[1:] - cu[:-1]).max().item())
+    o, lse = prefill_varlen(q.cuda(), kc.cuda(), vc.cuda(), cu.cuda(), kv.cuda(), max_sq, causal=True,
+                            scale=scale, out_dtype=out_dtype, window=window, n_sink=n_sink)
+    sync_check()
+    ro, rl = oracle.sdpa_varlen_window(q, kc, vc, cu, kv, window, n_sink, scale)
+    check_o(o.float().cpu().numpy(), ro, out_dtype == torch.bfloat16)
+    check_lse(lse.cpu().numpy(), rl)
