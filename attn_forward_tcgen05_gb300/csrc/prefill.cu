@@ -521,7 +521,8 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
       const uint64_t sl2x2 = f2pack(sl2, sl2), nmx2 = f2pack(-msub, -msub);
       // two row sums: the exact one (for LSE) and one of the bf16-rounded weights the
       // P.V MMA uses (for O / l: consistent weights, so P rounding cancels for flat V)
-      uint64_t lex2 = f2pack(0.f, 0.f), lrd2 = f2pack(0.f, 0.f);
+      uint64_t lex2 = f2pack(0.f, 0.f);
+      float lrd0 = 0.f, lrd1 = 0.f;
 #pragma unroll
       for (int h = 0; h < BN / 32; ++h) {
         uint32_t pk[16];
@@ -534,16 +535,15 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
           const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
           pk[e] = pack_bf16x2(p0, p1);
           lex2 = add2(lex2, f2pack(p0, p1));
-          lrd2 = add2(lrd2, f2pack(__uint_as_float(pk[e] << 16), __uint_as_float(pk[e] & 0xFFFF0000u)));
+          add_bf16x2_f32(pk[e], lrd0, lrd1);
         }
         tmem_st16(s_addr + 16 * h, pk);  // P: bf16 pairs over the first BN/2 columns of S
       }
       {
-        float a0, a1, b0, b1;
+        float a0, a1;
         f2unpack(lex2, a0, a1);
-        f2unpack(lrd2, b0, b1);
         l += a0 + a1;
-        l_rnd += b0 + b1;
+        l_rnd += lrd0 + lrd1;
       }
       // publish P(j): the MMA warp reads it as the A operand of P.V
       tmem_wait_st();

@@ -447,7 +447,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<D>::kThreads
       const uint64_t sl2x2 = f2pack(sl2, sl2), nmx2 = f2pack(-msub, -msub);
       // two row sums: the exact one (for LSE) and one of the bf16-rounded weights the
       // P.V MMA uses (for O / l: consistent weights, so P rounding cancels for flat V)
-      uint64_t lex2 = f2pack(0.f, 0.f), lrd2 = f2pack(0.f, 0.f);
+      uint64_t lex2 = f2pack(0.f, 0.f);
+      float lrd0 = 0.f, lrd1 = 0.f;
       uint32_t pk[KC / 2];
 #pragma unroll
       for (int e = 0; e < KC / 2; ++e) {
@@ -457,14 +458,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<D>::kThreads
         const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
         pk[e] = pack_bf16x2(p0, p1);
         lex2 = add2(lex2, f2pack(p0, p1));
-        lrd2 = add2(lrd2, f2pack(__uint_as_float(pk[e] << 16), __uint_as_float(pk[e] & 0xFFFF0000u)));
+        add_bf16x2_f32(pk[e], lrd0, lrd1);
       }
       {
-        float a0, a1, b0, b1;
+        float a0, a1;
         f2unpack(lex2, a0, a1);
-        f2unpack(lrd2, b0, b1);
         l += a0 + a1;
-        l_rnd += b0 + b1;
+        l_rnd += lrd0 + lrd1;
       }
       // P over the first KC / 2 of this warpgroup's S columns; then publish it to rank 0
       if (ok) {
@@ -869,7 +869,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(SliceCfg::kThreads, 
       }
       const float msub = (m_used == -INFINITY) ? 0.f : m_used;
       const uint64_t sl2x2 = f2pack(sl2, sl2), nmx2 = f2pack(-msub, -msub);
-      uint64_t lex2 = f2pack(0.f, 0.f), lrd2 = f2pack(0.f, 0.f);
+      uint64_t lex2 = f2pack(0.f, 0.f);
+      float lrd0 = 0.f, lrd1 = 0.f;
       uint32_t pk[KC / 2];
 #pragma unroll
       for (int e = 0; e < KC / 2; ++e) {
@@ -879,14 +880,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(SliceCfg::kThreads, 
         const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
         pk[e] = pack_bf16x2(p0, p1);
         lex2 = add2(lex2, f2pack(p0, p1));
-        lrd2 = add2(lrd2, f2pack(__uint_as_float(pk[e] << 16), __uint_as_float(pk[e] & 0xFFFF0000u)));
+        add_bf16x2_f32(pk[e], lrd0, lrd1);
       }
       {
-        float a0, a1, b0, b1;
+        float a0, a1;
         f2unpack(lex2, a0, a1);
-        f2unpack(lrd2, b0, b1);
         l += a0 + a1;
-        l_rnd += b0 + b1;
+        l_rnd += lrd0 + lrd1;
       }
       tmem_st32(s_addr, pk);  // P_h: bf16 pairs over the first KC/2 columns of the slice
       tmem_wait_st();

@@ -549,6 +549,15 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// acc_lo += bf16 low half of pk, acc_hi += its high half (mixed-precision f32 adds of a
+// bf16 operand: the bf16 value widens exactly, so this is the f32 sum of the rounded values)
+__device__ __forceinline__ void add_bf16x2_f32(uint32_t pk, float& acc_lo, float& acc_hi) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+      : "+f"(acc_lo), "+f"(acc_hi)
+      : "r"(pk));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   // cvt packs its first source into the upper half.
