@@ -52,6 +52,8 @@ def load(path: str | None = None):
         lib.attn_prefill_varlen.argtypes = [vp] * 7 + [i] * 8 + [f, i, vp]
         lib.attn_prefill_window.argtypes = [vp] * 5 + [i] * 8 + [f, i, vp]
         lib.attn_prefill_varlen_window.argtypes = [vp] * 7 + [i] * 9 + [f, i, vp]
+        lib.attn_prefill_packed.argtypes = [vp] * 5 + [i] * 7 + [f, i, vp]
+        lib.attn_decode_packed.argtypes = [vp] * 4 + [i] * 5 + [f, vp, vp, i, vp]
         lib.attn_decode_split.argtypes = [vp, vp, vp, vp] + [i] * 5 + [f, i, i, vp, vp, vp]
         lib.attn_merge.argtypes = [vp, vp, vp, vp] + [i] * 5 + [vp]
         lib.attn_sync_check.argtypes = [vp]
@@ -63,7 +65,7 @@ def load(path: str | None = None):
         lib.attn_decode_noalloc_scratch_bytes.argtypes = []
         lib.attn_decode_noalloc_scratch_bytes.restype = ull
         for name in ("attn_prefill_fwd", "attn_prefill_varlen", "attn_prefill_window",
-                     "attn_prefill_varlen_window",
+                     "attn_prefill_varlen_window", "attn_prefill_packed", "attn_decode_packed",
                      "attn_decode_split", "attn_merge",
                      "attn_sync_check",
                      "attn_version", "attn_debug_wait_timeout", "attn_decode_noalloc"):
@@ -76,6 +78,17 @@ def load(path: str | None = None):
 def attn_prefill_fwd(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, d, causal, scale, o_dtype, stream) -> int:
     return load().attn_prefill_fwd(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, d, int(causal),
                                    float(scale), o_dtype, stream)
+
+
+def attn_prefill_packed(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, d, causal, scale, o_dtype, stream) -> int:
+    return load().attn_prefill_packed(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, d, int(causal),
+                                      float(scale), o_dtype, stream)
+
+
+def attn_decode_packed(q, kcache, vcache, kv_lens, B, Hq, Hkv, d, max_kv, scale, o, lse, o_dtype,
+                       stream) -> int:
+    return load().attn_decode_packed(q, kcache, vcache, kv_lens, B, Hq, Hkv, d, max_kv, float(scale),
+                                     o, lse, o_dtype, stream)
 
 
 def attn_prefill_window(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, d, window, n_sink, scale, o_dtype,
@@ -172,8 +185,10 @@ def _out_code(dtype):
 
 
 def prefill(q, k, v, causal: bool = True, scale: float | None = None, out_dtype=None, stream=None,
-            out=None):
+            out=None, packed: bool = False):
     """Exact attention forward.  q [B,Sq,Hq,d], k/v [B,Skv,Hkv,d] bf16 on the GPU.
+    packed=True folds the Hq/Hkv query heads of each KV head into the MMA tile rows
+    (attn_prefill_packed).
 
     Returns (o [B,Sq,Hq,d] in out_dtype (default bf16), lse [B,Hq,Sq] fp32)."""
     torch = _torch()
@@ -190,10 +205,11 @@ def prefill(q, k, v, causal: bool = True, scale: float | None = None, out_dtype=
         lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
     else:
         o, lse = out
-    rc = attn_prefill_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Skv, d,
-                          causal, scale, _out_code(o.dtype), _stream_handle(stream))
+    fn = attn_prefill_packed if packed else attn_prefill_fwd
+    rc = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Skv, d, causal, scale,
+            _out_code(o.dtype), _stream_handle(stream))
     if rc != ATTN_OK:
-        raise AttnError(rc, "attn_prefill_fwd")
+        raise AttnError(rc, fn.__name__)
     return o, lse
 
 
@@ -319,6 +335,34 @@ def decode(q, kcache, vcache, kv_lens, n_splits: int, min_rows_per_split: int = 
     """Split-KV decode followed by the merge: (o [B,Hq,d], lse [B,Hq])."""
     po, pl = decode_split(q, kcache, vcache, kv_lens, n_splits, min_rows_per_split, scale, stream)
     return merge(po, pl, out_dtype, stream)
+
+
+def decode_packed(q, kcache, vcache, kv_lens, scale: float | None = None, out_dtype=None,
+                  stream=None, out=None):
+    """One-token decode on the tensor cores, heads packed into the tile rows
+    (attn_decode_packed).  q [B,Hq,d], caches [B,max_kv,Hkv,d] bf16, kv_lens int32 [B].
+
+    Returns (o [B,Hq,d] in out_dtype (default bf16), lse [B,Hq] fp32)."""
+    torch = _torch()
+    out_dtype = out_dtype or torch.bfloat16
+    _check_tensor(q, "q", torch.bfloat16, 3)
+    _check_tensor(kcache, "kcache", torch.bfloat16, 4)
+    _check_tensor(vcache, "vcache", torch.bfloat16, 4)
+    _check_tensor(kv_lens, "kv_lens", torch.int32, 1)
+    B, Hq, d = q.shape
+    _, max_kv, Hkv, _ = kcache.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        o = torch.empty((B, Hq, d), dtype=out_dtype, device=q.device)
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    else:
+        o, lse = out
+    rc = attn_decode_packed(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(kv_lens), B, Hq, Hkv, d, max_kv,
+                            scale, _ptr(o), _ptr(lse), _out_code(o.dtype), _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_decode_packed")
+    return o, lse
 
 
 def sync_check(stream=None) -> None:

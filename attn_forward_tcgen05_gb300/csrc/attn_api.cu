@@ -73,6 +73,24 @@ int encode_bf16_4d(CUtensorMap* map, const void* base, uint64_t n0, uint64_t n1,
   return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+// 5-D bf16 tensor map for the query tiles of the single-CTA prefill kernel over a
+// [nb][ns][Hq][d] row-major tensor, viewed as {d, G, Hq/G, ns, nb}: box
+// {64, G, 1, 128/G, 1} holds 128/G positions x the G heads of one group, 128
+// rows of 128 bytes in shared memory (row = position-in-box * G + head-in-group).
+int encode_bf16_q5d(CUtensorMap* map, const void* base, uint64_t d, uint64_t G, uint64_t Hq,
+                    uint64_t ns, uint64_t nb) {
+  EncodeTiledFn enc = encoder();
+  if (enc == nullptr) return ATTN_ERR_CUDA;
+  const cuuint64_t dims[5] = {d, G, Hq / G, ns, nb};
+  const cuuint64_t strides[4] = {d * 2, d * G * 2, d * Hq * 2, d * Hq * ns * 2};
+  const cuuint32_t box[5] = {64, (cuuint32_t)G, 1, (cuuint32_t)(attn::kPrefillTileM / G), 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool ok_dim(int d) { return d == 64 || d == 128 || d == 256; }
 bool ok_scale(float s) { return std::isfinite(s) && s > 0.f; }
@@ -81,9 +99,12 @@ int from_cuda(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA
 
 }  // namespace
 
+// kv_lens (optional): keys per sequence, each sequence's Sq queries being its last
+// positions; pack: query heads folded into the tile rows (single-CTA kernel only).
 static int prefill_impl(const attn_bf16_t* q, const attn_bf16_t* k, const attn_bf16_t* v, void* o,
                         float* lse, int B, int Hq, int Hkv, int Sq, int Skv, int d, int causal,
-                        int window, int n_sink, float scale, int o_dtype, attn_stream_t stream) {
+                        int window, int n_sink, float scale, int o_dtype, attn_stream_t stream,
+                        const int* kv_lens = nullptr, int pack = 1) {
   if (B < 0 || Sq < 0 || Skv < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (!ok_scale(scale)) return ATTN_ERR_INVALID_ARG;
   if (!ok_dim(d) || (o_dtype != ATTN_F32 && o_dtype != ATTN_BF16)) return ATTN_ERR_UNSUPPORTED;
@@ -104,15 +125,20 @@ static int prefill_impl(const attn_bf16_t* q, const attn_bf16_t* k, const attn_b
   a.scale = scale;
   a.window = window;
   a.n_sink = n_sink;
+  a.kv_lens = kv_lens;
+  a.pack = pack;
   a.err = err_word();
   if (a.err == nullptr) return ATTN_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (Skv == 0) return from_cuda(attn::launch_prefill_empty_kv(a, s));
-  int rc = encode_bf16_4d(&a.tm_q, q, d, Hq, Sq, B, attn::kPrefillTileM);
+  const bool pair = attn::prefill_uses_pair(d);
+  if (pair && pack != 1) return ATTN_ERR_UNSUPPORTED;
+  int rc = pair ? encode_bf16_4d(&a.tm_q, q, d, Hq, Sq, B, attn::kPrefillTileM)
+                : encode_bf16_q5d(&a.tm_q, q, d, pack, Hq, Sq, B);
   if (rc == ATTN_OK) rc = encode_bf16_4d(&a.tm_k, k, d, Hkv, Skv, B, attn::prefill_k_box_rows(d));
   if (rc == ATTN_OK) rc = encode_bf16_4d(&a.tm_v, v, d, Hkv, Skv, B, attn::kPrefillKVStageRows);
   if (rc != ATTN_OK) return rc;
-  return from_cuda(attn::prefill_uses_pair(d) ? attn::launch_prefill_pair(a, s) : attn::launch_prefill(a, s));
+  return from_cuda(pair ? attn::launch_prefill_pair(a, s) : attn::launch_prefill(a, s));
 }
 
 static int varlen_impl(const attn_bf16_t* q, const attn_bf16_t* kcache, const attn_bf16_t* vcache,
@@ -144,17 +170,20 @@ static int varlen_impl(const attn_bf16_t* q, const attn_bf16_t* kcache, const at
   a.n_sink = n_sink;
   a.cu_q = cu_seqlens_q;
   a.kv_lens = kv_lens;
+  a.pack = 1;
   a.total_q = total_q;
   a.err = err_word();
   if (a.err == nullptr) return ATTN_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (max_kv == 0) return from_cuda(attn::launch_prefill_empty_kv(a, s));
   // packed q is one batch slab of total_q rows; the cache keeps its batch dimension
-  int rc = encode_bf16_4d(&a.tm_q, q, d, Hq, total_q, 1, attn::kPrefillTileM);
+  const bool pair = attn::prefill_uses_pair(d);
+  int rc = pair ? encode_bf16_4d(&a.tm_q, q, d, Hq, total_q, 1, attn::kPrefillTileM)
+                : encode_bf16_q5d(&a.tm_q, q, d, 1, Hq, total_q, 1);
   if (rc == ATTN_OK) rc = encode_bf16_4d(&a.tm_k, kcache, d, Hkv, max_kv, B, attn::prefill_k_box_rows(d));
   if (rc == ATTN_OK) rc = encode_bf16_4d(&a.tm_v, vcache, d, Hkv, max_kv, B, attn::kPrefillKVStageRows);
   if (rc != ATTN_OK) return rc;
-  return from_cuda(attn::prefill_uses_pair(d) ? attn::launch_prefill_pair(a, s) : attn::launch_prefill(a, s));
+  return from_cuda(pair ? attn::launch_prefill_pair(a, s) : attn::launch_prefill(a, s));
 }
 
 extern "C" {
@@ -186,6 +215,36 @@ int attn_prefill_window(const attn_bf16_t* q, const attn_bf16_t* k, const attn_b
   // the experimental d = 128 pair build has no window support
   if (ATTN_PREFILL_PAIR_D128 && d == 128) return ATTN_ERR_UNSUPPORTED;
   return prefill_impl(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, d, 1, window, n_sink, scale, o_dtype, stream);
+}
+
+// head packing needs the group to tile the 128 rows and the single-CTA kernel
+static bool packable(int Hq, int Hkv, int d) {
+  if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return false;
+  const int G = Hq / Hkv;
+  return (d == 64 || d == 128) && !attn::prefill_uses_pair(d) && G <= attn::kPrefillTileM &&
+         attn::kPrefillTileM % G == 0;
+}
+
+int attn_prefill_packed(const attn_bf16_t* q, const attn_bf16_t* k, const attn_bf16_t* v, void* o,
+                        float* lse, int B, int Hq, int Hkv, int Sq, int Skv, int d, int causal,
+                        float scale, int o_dtype, attn_stream_t stream) {
+  if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (!packable(Hq, Hkv, d)) return ATTN_ERR_UNSUPPORTED;
+  return prefill_impl(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, d, causal, 0, 0, scale, o_dtype, stream,
+                      nullptr, Hq / Hkv);
+}
+
+int attn_decode_packed(const attn_bf16_t* q, const attn_bf16_t* kcache, const attn_bf16_t* vcache,
+                       const int* kv_lens, int B, int Hq, int Hkv, int d, int max_kv, float scale,
+                       void* o, float* lse, int o_dtype, attn_stream_t stream) {
+  if (B < 0 || max_kv < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (!ok_scale(scale)) return ATTN_ERR_INVALID_ARG;
+  if (!packable(Hq, Hkv, d) || (o_dtype != ATTN_F32 && o_dtype != ATTN_BF16)) return ATTN_ERR_UNSUPPORTED;
+  if (B == 0) return ATTN_OK;
+  if (!kv_lens || (reinterpret_cast<uintptr_t>(kv_lens) & 3)) return ATTN_ERR_INVALID_ARG;
+  // one query position per sequence, the last one: causal admits keys [0, kv_lens[b])
+  return prefill_impl(q, kcache, vcache, o, lse, B, Hq, Hkv, 1, max_kv, d, 1, 0, 0, scale, o_dtype,
+                      stream, kv_lens, Hq / Hkv);
 }
 
 int attn_prefill_varlen(const attn_bf16_t* q, const attn_bf16_t* kcache, const attn_bf16_t* vcache,

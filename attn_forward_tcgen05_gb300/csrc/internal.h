@@ -9,14 +9,21 @@ namespace attn {
 
 // Prefill launch description (already validated by the C-ABI layer).
 // Fixed-length batches: cu_q == nullptr, q/o [B][Sq][Hq][d], k/v [B][Skv][Hkv][d],
-// lse [B][Hq][Sq].  Packed variable-length batches (cu_q != nullptr): sequence b
-// has rows [cu_q[b], cu_q[b+1]) of q/o [total_q][Hq][d] and lse [Hq][total_q]; its
-// keys are rows [0, kv_lens[b]) of k/v [B][Skv][Hkv][d] (Skv = the cache's
-// max_kv); Sq is the longest sequence (it sizes the grid).
+// lse [B][Hq][Sq]; with kv_lens != nullptr sequence b has only the keys
+// [0, kv_lens[b]) (its Sq queries are its last positions).  Packed
+// variable-length batches (cu_q != nullptr): sequence b has rows
+// [cu_q[b], cu_q[b+1]) of q/o [total_q][Hq][d] and lse [Hq][total_q]; its keys are
+// rows [0, kv_lens[b]) of k/v [B][Skv][Hkv][d] (Skv = the cache's max_kv); Sq is
+// the longest sequence (it sizes the grid).
+// Head packing (pack = G > 1, single-CTA kernel only): the G query heads of one KV
+// head fill the rows of a query tile, row r = position r / G, head r % G of the
+// group, so a tile holds 128 / G positions.
 struct PrefillArgs {
-  CUtensorMap tm_q, tm_k, tm_v;  // 4-D maps {d, H, S, B}, box {64, 1, rows, 1}, 128B swizzle:
-                                 // rows = kPrefillTileM for Q, prefill_k_box_rows(d) for K,
-                                 // kPrefillKVStageRows for V
+  CUtensorMap tm_q, tm_k, tm_v;  // K, V (and Q of the pair kernel): 4-D maps {d, H, S, B},
+                                 // box {64, 1, rows, 1}, 128B swizzle: rows = kPrefillTileM
+                                 // for Q, prefill_k_box_rows(d) for K, kPrefillKVStageRows
+                                 // for V.  Q of the single-CTA kernel: 5-D map
+                                 // {d, G, Hq/G, S, B}, box {64, G, 1, 128/G, 1}.
   void* o;                       // [B][Sq][Hq][d], fp32 or bf16
   float* lse;                    // [B][Hq][Sq]
   int B, Hq, Hkv, Sq, Skv, d, causal, o_bf16;
@@ -27,6 +34,7 @@ struct PrefillArgs {
   int total_q;                   // rows of the packed q (varlen only)
   int window;                    // > 0: causal sliding window of this many positions
   int n_sink;                    // with a window: the first n_sink keys stay admissible
+  int pack;                      // query rows per position (G); 1 = one head per tile
 };
 
 #ifdef __CUDACC__
@@ -42,6 +50,10 @@ __device__ __forceinline__ SeqExtent seq_extent(int b, int Sq, int Skv, const in
   SeqExtent e;
   if (cu_q == nullptr) {
     e.Sq = Sq; e.Skv = Skv; e.qbase = 0; e.bq = b; e.rows = Sq;
+    if (kv_lens != nullptr) {  // fixed queries, per-sequence keys (decode)
+      const int kl = kv_lens[b];
+      e.Skv = kl < 0 ? 0 : (kl > Skv ? Skv : kl);
+    }
     return e;
   }
   // offsets and lengths are clamped to the buffers the caller described

@@ -128,20 +128,23 @@ struct TileInfo {
   int kv_lo;   // every existing row of the tile admits keys [0, kv_lo): tiles past it need a mask
 };
 
+// q0: first row of the tile; Sr: rows of the sequence (Sq positions x G heads);
+// the causal bound of a row follows its position row / G.
 template <int BN>
-__device__ __forceinline__ TileInfo tile_info(int q0, int Sq, int Skv, int causal) {
+__device__ __forceinline__ TileInfo tile_info(int q0, int Sr, int Sq, int G, int Skv, int causal) {
   TileInfo ti;
   ti.q0 = q0;
-  if (q0 >= Sq) {
+  if (q0 >= Sr) {
     ti.n_kv = 0;
     ti.kv_lo = 0;
     return ti;
   }
-  const int q_last = min(Sq, q0 + kPrefillTileM) - 1;
+  const int q_last = (min(Sr, q0 + kPrefillTileM) - 1) / G;  // positions
+  const int q_first = q0 / G;
   int kv_hi = Skv, kv_lo = Skv;
   if (causal) {
     const long long off = (long long)Skv - Sq;
-    long long hi = (long long)q_last + off + 1, lo = (long long)q0 + off + 1;
+    long long hi = (long long)q_last + off + 1, lo = (long long)q_first + off + 1;
     kv_hi = (int)(hi < 0 ? 0 : (hi > Skv ? Skv : hi));
     kv_lo = (int)(lo < 0 ? 0 : (lo > Skv ? Skv : lo));
   }
@@ -159,23 +162,28 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
                     float* __restrict__ lse_ptr, int Hq, int Hkv, int Sq_max, int Skv_max, int causal,
                     int o_bf16, float scale, int n_units_per_head_batch, uint32_t* err,
                     const int* __restrict__ cu_q, const int* __restrict__ kv_lens, int total_q,
-                    int window, int n_sink) {
+                    int window, int n_sink, int pack) {
   using C = PrefillCfg<D>;
   constexpr int NQ = C::NQ, NS = C::NS, BN = C::BN;
   static_assert(C::kSub == 1, "a KV stage is one tile (the sliding-window tile list maps tiles, not stages)");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // ---- work unit: longest causal work first ----
-  const int HB = n_units_per_head_batch;  // Hq * B
-  const int n_blocks_q = (Sq_max + NQ * kPrefillTileM - 1) / (NQ * kPrefillTileM);
+  // A unit is NQ query tiles of one head group: G = pack query heads (of one KV
+  // head) folded into the tile rows, row r = (position r / G, head r % G).
+  const int G = pack;
+  const int Hu = Hq / G;                  // head groups
+  const int HB = n_units_per_head_batch;  // Hu * B
+  const int n_blocks_q = (Sq_max * G + NQ * kPrefillTileM - 1) / (NQ * kPrefillTileM);
   const int u = blockIdx.x;
   const int qb = causal ? (n_blocks_q - 1 - u / HB) : (u / HB);
   const int hb = u % HB;
-  const int hq = hb % Hq, b = hb / Hq;
-  const int hk = hq / (Hq / Hkv);
-  // this sequence's query rows and keys (fixed-length or packed varlen batch)
+  const int hu = hb % Hu, b = hb / Hu;
+  const int hk = (hu * G) / (Hq / Hkv);
+  // this sequence's query positions and keys (fixed-length or packed varlen batch)
   const SeqExtent ext = seq_extent(b, Sq_max, Skv_max, cu_q, kv_lens, total_q);
   const int Sq = ext.Sq, Skv = ext.Skv;
+  const int Sr = Sq * G;  // tile rows of this sequence
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -199,14 +207,14 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
   TileInfo ti[NQ];
 #pragma unroll
   for (int t = 0; t < NQ; ++t)
-    ti[t] = tile_info<BN>(qb * NQ * kPrefillTileM + t * kPrefillTileM, Sq, Skv, causal);
+    ti[t] = tile_info<BN>(qb * NQ * kPrefillTileM + t * kPrefillTileM, Sr, Sq, G, Skv, causal);
   int n_kv = 0;
 #pragma unroll
   for (int t = 0; t < NQ; ++t) n_kv = max(n_kv, ti[t].n_kv);
   // with a sliding window the loops below run over a list of KV tiles (list index
   // j, key tile tile_list_key(tl, j)); without one the list is every tile
   const long long pos_off = (long long)Skv - Sq;  // key position of query row i: i + pos_off
-  const TileList tl = WIN ? tile_list((long long)ti[0].q0 + pos_off, n_kv, window, n_sink, Skv, BN)
+  const TileList tl = WIN ? tile_list((long long)(ti[0].q0 / G) + pos_off, n_kv, window, n_sink, Skv, BN)
                           : TileList{0x7FFFFFFF, 0};
 #pragma unroll
   for (int t = 0; t < NQ; ++t) ti[t].n_kv = tile_list_len(tl, ti[t].n_kv);
@@ -263,8 +271,8 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
         if (ti[t].n_kv > 0) {
 #pragma unroll
           for (int p = 0; p < C::kPanels; ++p)
-            tma_load_4d_e(sQ + t * C::kQTileBytes + p * C::kQPanelBytes, &tm_q, bar_q, p * 64, hq,
-                          ext.qbase + ti[t].q0, ext.bq);
+            tma_load_5d_e(sQ + t * C::kQTileBytes + p * C::kQPanelBytes, &tm_q, bar_q, p * 64, 0, hu,
+                          ext.qbase + ti[t].q0 / G, ext.bq);
         }
       }
       // Stages of kSub KV tiles.  The MMA warp takes the K stage of tile j+1
@@ -433,22 +441,24 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
     const int wq = warp & 3;         // TMEM lane quarter
     const int r = wq * 32 + lane;    // row within the tile = TMEM lane
     const TileInfo my = ti[t];
-    const int qrow = my.q0 + r;
+    const int qrow = my.q0 + r;       // tile row
+    const int qpos = qrow / G;        // its query position
+    const int qg = qrow - qpos * G;   // its head within the group
     const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
     const float sl2 = scale * kLog2e;
     // admissible keys of this row: [0, row_bound), and with a sliding window only
     // [row_lo, row_bound) plus the sinks [0, n_sink)
     int row_bound = Skv;
     if (causal) {
-      const long long rb = (long long)qrow + pos_off + 1;  // causal bound of this row
+      const long long rb = (long long)qpos + pos_off + 1;  // causal bound of this row
       row_bound = (int)(rb < 0 ? 0 : (rb > Skv ? Skv : rb));
     }
     // (32-bit, clamped: key indices are below 2^31; a bound below 0 masks nothing)
     auto clamp_key = [](long long x) { return (int)(x < -1 ? -1 : (x > 0x7FFFFFFF ? 0x7FFFFFFF : x)); };
-    const int row_lo = WIN ? clamp_key((long long)qrow + pos_off - window + 1) : -1;
+    const int row_lo = WIN ? clamp_key((long long)qpos + pos_off - window + 1) : -1;
     // the window start of the tile's last existing row: keys below it need the mask
     const int tile_lo_max =
-        WIN ? clamp_key((long long)min(Sq, my.q0 + kPrefillTileM) - 1 + pos_off - window + 1) : -1;
+        WIN ? clamp_key((long long)((min(Sr, my.q0 + kPrefillTileM) - 1) / G) + pos_off - window + 1) : -1;
     float m_used = -INFINITY, l = 0.f, l_rnd = 0.f;
     bool ok = true;
 
@@ -561,9 +571,10 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
     const bool load_o = ok && my.n_kv > 0;
     const bool have = load_o && l > 0.f;  // per row: at least one admissible key
     const float inv_l = have ? 1.f / l_rnd : 0.f;
-    const bool row_ok = qrow < Sq;
+    const bool row_ok = qrow < Sr;
     const uint32_t o_addr = lane_addr + C::o_col(t);
-    const size_t orow = ((size_t)ext.bq * ext.rows + ext.qbase + (size_t)(row_ok ? qrow : 0)) * Hq + hq;
+    const int hq = hu * G + qg;  // query head of this row
+    const size_t orow = ((size_t)ext.bq * ext.rows + ext.qbase + (size_t)(row_ok ? qpos : 0)) * Hq + hq;
 #pragma unroll
     for (int c0 = 0; c0 < D; c0 += 32) {
       uint32_t ov[32];
@@ -597,7 +608,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
       }
     }
     if (row_ok && ok) {
-      lse_ptr[((size_t)ext.bq * Hq + hq) * ext.rows + ext.qbase + qrow] = have ? (m_used + log2f(l)) * kLn2 : -INFINITY;
+      lse_ptr[((size_t)ext.bq * Hq + hq) * ext.rows + ext.qbase + qpos] = have ? (m_used + log2f(l)) * kLn2 : -INFINITY;
     }
   }
 
@@ -627,13 +638,15 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, cudaStream_t stream) {
   auto kern = a.window > 0 ? fmha_fwd_kernel<D, true> : fmha_fwd_kernel<D, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  const int n_blocks_q = (a.Sq + C::NQ * kPrefillTileM - 1) / (C::NQ * kPrefillTileM);
-  const long long units = (long long)n_blocks_q * a.Hq * a.B;
+  const int G = a.pack;
+  const long long rows = (long long)a.Sq * G;
+  const long long n_blocks_q = (rows + C::NQ * kPrefillTileM - 1) / (C::NQ * kPrefillTileM);
+  const long long units = n_blocks_q * (a.Hq / G) * a.B;
   if (units <= 0) return cudaSuccess;
-  if (units > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+  if (units > 0x7FFFFFFFLL || rows > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
   kern<<<(unsigned)units, C::kThreads, C::kSmemBytes, stream>>>(
       a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, a.Hq, a.Hkv, a.Sq, a.Skv, a.causal, a.o_bf16, a.scale,
-      a.Hq * a.B, a.err, a.cu_q, a.kv_lens, a.total_q, a.window, a.n_sink);
+      (a.Hq / G) * a.B, a.err, a.cu_q, a.kv_lens, a.total_q, a.window, a.n_sink, G);
   return cudaGetLastError();
 }
 

@@ -18,6 +18,8 @@ Workloads (names used throughout the tests and the benchmark):
                         sequence, chosen by its length), O bf16 + LSE fp32
 * ``gqa_prefill_3314_window1024_sink4`` the GQA prefill inputs, causal over a
                         1024-position sliding window plus 4 sink positions
+* ``mqa_decode_b128_h128``  one-token decode, 128 query heads sharing one KV head
+                        (B = 128, d = 128, lengths U[512, 8192])
 * ``chunked_prefill_gqa_b8`` packed variable-length prefill against a KV cache:
                         B=8, Hq=28, Hkv=4, d=128, causal, 64-1024 new rows per
                         sequence after 0-3072 cached ones, O bf16 + LSE fp32
@@ -75,6 +77,17 @@ def mha_sweep(d: int) -> PrefillShape:
 
 RAGGED_DECODE = DecodeShape("ragged_gqa_decode_b64", 64, 32, 8, 128, 1.0 / math.sqrt(128.0), 8,
                             1024, 1005, len_range=(512, 8192))
+
+# multi-query decode (one KV head for 128 query heads, the head count of the
+# FMHA page's D2 workload), head dimension 128, ragged lengths as the GQA batch
+MQA_DECODE = DecodeShape("mqa_decode_b128_h128", 128, 128, 1, 128, 1.0 / math.sqrt(128.0), 1,
+                         1, 1008, len_range=(512, 8192))
+
+
+def decode_flops(kv_lens, Hq, d) -> int:
+    """Algorithmic decode FLOPs: 4*d per (query head, cached key) pair."""
+    total = int(torch.as_tensor(kv_lens).to(torch.int64).sum().item())
+    return 4 * d * Hq * total
 
 
 @dataclass(frozen=True)

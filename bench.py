@@ -216,6 +216,8 @@ def run_ours(args, rank, world, local_rank):
     varlen = None if args.only else time_varlen(args, attn, W, dev, stream, flush, peaks, peak_src)
     # ---- causal sliding window with attention sinks ----
     window = None if args.only else time_window(args, attn, W, dev, stream, flush, peaks, peak_src)
+    # ---- multi-query decode on the tensor cores (heads packed into the tile rows) ----
+    mqa = None if args.only else time_mqa_decode(args, attn, W, dev, stream, flush, peaks, peak_src)
 
     # ---- end to end through the public API with host buffers ----
     e2e = None if (args.no_e2e or args.only) else run_e2e(args, attn, W, dev, stream, P, dec, flops)
@@ -290,6 +292,7 @@ def run_ours(args, rank, world, local_rank):
         "e2e": e2e,
         "prefill_varlen": varlen,
         "prefill_window": window,
+        "decode_packed": mqa,
         "clocks": clocks,
     }
     return line
@@ -370,6 +373,49 @@ def time_window(args, attn, W, dev, stream, flush, peaks, peak_src):
             "roofline": {"bound": "tensor", "kernel": kern, "achieved": round(tf, 2),
                          "peak": peak_tc, "unit": "TFLOP/s", "frac": round(tf / peak_tc, 4),
                          "peak_source": f"bf16_tflops (burst) of {peak_src}"}}
+
+
+def time_mqa_decode(args, attn, W, dev, stream, flush, peaks, peak_src):
+    """One-token decode with 128 query heads per KV head through attn_decode_packed:
+    average launch time over the timed iterations, L2 flushed before each.  Both
+    rooflines are reported: FLOPs on the tensor cores and K/V bytes from HBM."""
+    import torch
+
+    S = W.MQA_DECODE
+    q, kc, vc, lens = W.decode_inputs_for(S)
+    flops = W.decode_flops(lens, S.Hq, S.d)
+    kvb = W.decode_kv_bytes(lens, S.Hkv, S.d)
+    qd, kd, vd, ld = (t.to(dev) for t in (q, kc, vc, lens))
+    o = torch.empty((S.B, S.Hq, S.d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((S.B, S.Hq), dtype=torch.float32, device=dev)
+
+    def call():
+        attn.decode_packed(qd, kd, vd, ld, S.scale, out=(o, lse))
+
+    for _ in range(args.warmup):
+        call()
+    n = max(1, min(args.steps, 50))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for a, b in evs:
+        flush.zero_()
+        a.record(stream)
+        call()
+        b.record(stream)
+    torch.cuda.synchronize()
+    attn.sync_check()
+    ms = sum(a.elapsed_time(b) for a, b in evs) / n
+    tf = flops / (ms * 1e-3) / 1e12
+    gbs = kvb / (ms * 1e-3) / 1e9
+    peak_tc, peak_hbm = float(peaks["bf16_tflops"]), float(peaks["hbm_gbs"])
+    return {"workload": S.name, "B": S.B, "Hq": S.Hq, "Hkv": S.Hkv, "d": S.d,
+            "kv_tokens": int(lens.sum()), "gflop": round(flops / 1e9, 3), "kv_mb": round(kvb / 1e6, 1),
+            "us": round(ms * 1e3, 2), "value": round(tf, 2), "unit": "TFLOP/s", "gbs": round(gbs, 1),
+            "steps": n,
+            "roofline": {"bound": "tensor", "kernel": f"fmha_fwd_kernel<{S.d}>", "achieved": round(tf, 2),
+                         "peak": peak_tc, "unit": "TFLOP/s", "frac": round(tf / peak_tc, 4),
+                         "peak_source": f"bf16_tflops (burst) of {peak_src}"},
+            "roofline_hbm": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak_hbm, "unit": "GB/s",
+                             "frac": round(gbs / peak_hbm, 4), "peak_source": f"hbm_gbs of {peak_src}"}}
 
 
 def run_e2e(args, attn, W, dev, stream, P, dec, flops):

@@ -113,6 +113,50 @@ int attn_prefill_window(const attn_bf16_t* q, const attn_bf16_t* k, const attn_b
                         int n_sink, float scale, int o_dtype, attn_stream_t stream);
 
 /*
+ * attn_prefill_packed -- attn_prefill_fwd with the query heads of each KV head
+ * folded into the rows of the MMA tiles (head packing).
+ *
+ * Same arguments, layouts and results as attn_prefill_fwd (up to summation
+ * order).  The G = Hq / Hkv query heads that share a KV head fill the 128 rows of
+ * a query tile together: row r of a tile is position r / G, head r % G of the
+ * group, so each K/V tile is streamed once per group of G heads instead of once
+ * per head, and a short sequence (a decode step, a small chunk) still fills the
+ * tile.  Follows "STAGE_D.md -- FMHA Kernel Development", D2 (the multi-query
+ * grid: query blocks x batch, the head axis folded into the M dimension).
+ * Requires d in {64, 128} and G dividing 128 (MQA: Hkv = 1, Hq <= 128 a power of
+ * two); otherwise returns ATTN_ERR_UNSUPPORTED.
+ */
+int attn_prefill_packed(const attn_bf16_t* q, const attn_bf16_t* k, const attn_bf16_t* v, void* o,
+                        float* lse, int B, int Hq, int Hkv, int Sq, int Skv, int d, int causal,
+                        float scale, int o_dtype, attn_stream_t stream);
+
+/*
+ * attn_decode_packed -- one-token decode on the tensor cores with head packing.
+ *
+ * For every sequence b and query head hq (hk = hq / (Hq/Hkv)):
+ *   o[b,hq,:] = sum_{j < L_b} exp(s_j - lse[b,hq]) vcache[b,j,hk,:],
+ *   s_j = scale * q[b,hq,:] . kcache[b,j,hk,:],   lse[b,hq] = ln sum_{j < L_b} exp(s_j),
+ * L_b = kv_lens[b] -- the merged result of attn_decode_split + attn_merge, in one
+ * launch and without split partials.  The G = Hq/Hkv heads of a KV head form the
+ * rows of one MMA tile (the FMHA page's D2), so a decode step of G >= 8 heads per
+ * KV head runs on tcgen05 instead of CUDA cores; one unit of work per (sequence,
+ * KV head) streams that sequence's keys once.  Requires d in {64, 128} and G
+ * dividing 128 (any G up to 128, so also MQA groups larger than attn_decode_split's 16).
+ *
+ * Arguments
+ *   q         bf16 [B][Hq][d]
+ *   kcache    bf16 [B][max_kv][Hkv][d]   keys; rows >= kv_lens[b] are never admitted
+ *   vcache    bf16 [B][max_kv][Hkv][d]
+ *   kv_lens   int32 [B] (device)         0 <= L_b <= max_kv (clamped on the device)
+ *   o         [B][Hq][d], fp32 (ATTN_F32) or bf16 (ATTN_BF16); L_b = 0 gives o = 0
+ *   lse       fp32 [B][Hq]; L_b = 0 gives -inf
+ * Returns ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED or ATTN_ERR_CUDA.
+ */
+int attn_decode_packed(const attn_bf16_t* q, const attn_bf16_t* kcache, const attn_bf16_t* vcache,
+                       const int* kv_lens, int B, int Hq, int Hkv, int d, int max_kv, float scale,
+                       void* o, float* lse, int o_dtype, attn_stream_t stream);
+
+/*
  * attn_prefill_varlen -- prefill of a packed batch of sequences of different
  * lengths against a KV cache (chunked prefill).
  *

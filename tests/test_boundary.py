@@ -99,6 +99,25 @@ def test_prefill_varlen_window_validation(lib):
     assert f(N, N, N, N, N, N, N, 0, 2, 2, 10, 8, 16, 64, 4, 0, 0.5, 0, N) == attn.ATTN_OK  # empty batch
 
 
+def test_packed_validation(lib):
+    f = attn.attn_prefill_packed
+    #      q  k  v  o  lse B  Hq Hkv Sq Skv d    causal scale dtype stream
+    assert f(P, P, P, P, P, 1, 8, 1, 4, 4, 256, 1, 0.5, 0, N) == attn.ATTN_ERR_UNSUPPORTED  # d = 256
+    assert f(P, P, P, P, P, 1, 6, 2, 4, 4, 64, 1, 0.5, 0, N) == attn.ATTN_ERR_UNSUPPORTED  # G = 3
+    assert f(P, P, P, P, P, 1, 256, 1, 4, 4, 64, 1, 0.5, 0, N) == attn.ATTN_ERR_UNSUPPORTED  # G = 256
+    assert f(P, P, P, P, P, 1, 6, 4, 4, 4, 64, 1, 0.5, 0, N) == attn.ATTN_ERR_INVALID_ARG  # Hq % Hkv
+    assert f(N, N, N, N, N, 0, 8, 1, 4, 4, 64, 1, 0.5, 0, N) == attn.ATTN_OK  # empty batch
+    g = attn.attn_decode_packed
+    #      q  kc vc kv  B  Hq Hkv d   mkv scale o  lse dtype stream
+    assert g(P, P, P, P, 2, 8, 1, 96, 16, 0.5, P, P, 0, N) == attn.ATTN_ERR_UNSUPPORTED  # d
+    assert g(P, P, P, P, 2, 8, 1, 64, 16, 0.5, P, P, 3, N) == attn.ATTN_ERR_UNSUPPORTED  # dtype
+    assert g(P, P, P, N, 2, 8, 1, 64, 16, 0.5, P, P, 0, N) == attn.ATTN_ERR_INVALID_ARG  # null kv_lens
+    assert g(P, P, P, M, 2, 8, 1, 64, 16, 0.5, P, P, 0, N) == attn.ATTN_ERR_INVALID_ARG  # misaligned kv_lens
+    assert g(P, P, P, P, 2, 8, 1, 64, -1, 0.5, P, P, 0, N) == attn.ATTN_ERR_INVALID_ARG  # max_kv
+    assert g(P, P, P, P, 2, 8, 1, 64, 16, 0.0, P, P, 0, N) == attn.ATTN_ERR_INVALID_ARG  # scale
+    assert g(N, N, N, N, 0, 8, 1, 64, 16, 0.5, N, N, 0, N) == attn.ATTN_OK  # empty batch
+
+
 def test_decode_and_merge_validation(lib):
     f = attn.attn_decode_split
     assert f(P, P, P, P, 1, 28, 4, 96, 10, 0.1, 8, 1, P, P, N) == attn.ATTN_ERR_UNSUPPORTED

@@ -1,0 +1,94 @@
+"""Head packing (the query heads of one KV head folded into the MMA tile rows),
+through the C ABI: attn_prefill_packed against the fp64 oracle and bit for bit
+against the unpacked kernel, attn_decode_packed against the oracle's decode.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from attn_forward_tcgen05_gb300 import decode_packed, prefill, sync_check
+from attn_forward_tcgen05_gb300 import workloads as W
+from tests.tolerances import check_lse, check_o
+
+pytestmark = pytest.mark.gpu
+
+
+def _prefill_inputs(B, Sq, Skv, Hq, Hkv, d, seed):
+    s = W.PrefillShape("packed_case", B, Hq, Hkv, Sq, Skv, d, True, 1.0 / np.sqrt(d), "f32", seed)
+    return W.prefill_inputs_for(s)
+
+
+# (Hq, Hkv): MQA groups of 2..128 heads and a GQA group of 8
+GROUPS = [(128, 1), (16, 1), (2, 1), (32, 4), (8, 4)]
+# (Sq, Skv): single token, a few positions (a tile holds 128/G of them), a ragged
+# tail across several tiles, more keys than queries, more queries than keys
+LENGTHS = [(1, 300), (5, 5), (77, 640), (300, 300), (40, 23)]
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("Hq,Hkv", GROUPS)
+@pytest.mark.parametrize("Sq,Skv", LENGTHS)
+@pytest.mark.parametrize("causal", [True, False])
+def test_packed_prefill(d, Hq, Hkv, Sq, Skv, causal):
+    q, k, v = _prefill_inputs(2, Sq, Skv, Hq, Hkv, d, 500 + d + Hq + Sq)
+    scale = 1.0 / np.sqrt(d)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o, lse = prefill(qd, kd, vd, causal=causal, scale=scale, out_dtype=torch.float32, packed=True)
+    o2, lse2 = prefill(qd, kd, vd, causal=causal, scale=scale, out_dtype=torch.float32)
+    sync_check()
+    o, lse = o.cpu().numpy(), lse.cpu().numpy()
+    # the same rows, keys, masks and per-row arithmetic as the unpacked kernel
+    np.testing.assert_array_equal(o, o2.cpu().numpy())
+    np.testing.assert_array_equal(lse, lse2.cpu().numpy())
+    ro, rl = oracle.sdpa(q, k, v, causal, scale)
+    check_o(o, ro, False)
+    check_lse(lse, rl)
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_packed_prefill_bf16_output(out_dtype):
+    q, k, v = _prefill_inputs(1, 200, 200, 64, 1, 128, 777)
+    o, lse = prefill(q.cuda(), k.cuda(), v.cuda(), causal=True, scale=0.09, out_dtype=out_dtype, packed=True)
+    sync_check()
+    ro, rl = oracle.sdpa(q, k, v, True, 0.09)
+    check_o(o.float().cpu().numpy(), ro, out_dtype == torch.bfloat16)
+    check_lse(lse.cpu().numpy(), rl)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("Hq,Hkv", [(128, 1), (64, 2), (32, 1), (16, 2), (8, 1)])
+def test_packed_decode(d, Hq, Hkv):
+    lens = torch.tensor([0, 1, 29, 128, 129, 1000, 2500, 77], dtype=torch.int32)
+    q, kc, vc = W.decode_inputs(len(lens), Hq, Hkv, d, lens, 600 + d + Hq)
+    scale = 1.0 / np.sqrt(d)
+    o, lse = decode_packed(q.cuda(), kc.cuda(), vc.cuda(), lens.cuda(), scale, out_dtype=torch.float32)
+    sync_check()
+    ro, rl = oracle.decode(q, kc, vc, lens, scale)
+    check_o(o.cpu().numpy(), ro, False)
+    check_lse(lse.cpu().numpy(), rl)
+
+
+def test_packed_decode_cache_rows_past_length_ignored():
+    lens = torch.tensor([100, 3], dtype=torch.int32)
+    q, kc, vc = W.decode_inputs(2, 16, 1, 128, lens, 611, Lmax=400)
+    kc[:, 100:] = 40.0
+    vc[:, 100:] = -40.0
+    o, lse = decode_packed(q.cuda(), kc.cuda(), vc.cuda(), lens.cuda(), 0.1, out_dtype=torch.float32)
+    sync_check()
+    ro, rl = oracle.decode(q, kc, vc, lens, 0.1)
+    check_o(o.cpu().numpy(), ro, False)
+    check_lse(lse.cpu().numpy(), rl)
+
+
+def test_mqa_decode_workload_sampled():
+    """The full multi-query decode workload in the benchmark's configuration
+    (bf16 output), checked on sampled sequences against the oracle."""
+    s = W.MQA_DECODE
+    q, kc, vc, lens = W.decode_inputs_for(s)
+    o, lse = decode_packed(q.cuda(), kc.cuda(), vc.cuda(), lens.cuda(), s.scale)
+    sync_check()
+    pick = [0, 1, 17, 63, 64, 100, s.B - 1]
+    ro, rl = oracle.decode(q[pick], kc[pick], vc[pick], lens[pick], s.scale)
+    check_o(o[pick].float().cpu().numpy(), ro, True)
+    check_lse(lse[pick].cpu().numpy(), rl)
