@@ -54,6 +54,7 @@ def load(path: str | None = None):
         lib.attn_prefill_varlen_window.argtypes = [vp] * 7 + [i] * 9 + [f, i, vp]
         lib.attn_prefill_packed.argtypes = [vp] * 5 + [i] * 7 + [f, i, vp]
         lib.attn_decode_packed.argtypes = [vp] * 4 + [i] * 5 + [f, vp, vp, i, vp]
+        lib.attn_decode_split_packed.argtypes = [vp] * 4 + [i] * 5 + [f, i, i, vp, vp, vp]
         lib.attn_decode_split.argtypes = [vp, vp, vp, vp] + [i] * 5 + [f, i, i, vp, vp, vp]
         lib.attn_merge.argtypes = [vp, vp, vp, vp] + [i] * 5 + [vp]
         lib.attn_sync_check.argtypes = [vp]
@@ -66,6 +67,7 @@ def load(path: str | None = None):
         lib.attn_decode_noalloc_scratch_bytes.restype = ull
         for name in ("attn_prefill_fwd", "attn_prefill_varlen", "attn_prefill_window",
                      "attn_prefill_varlen_window", "attn_prefill_packed", "attn_decode_packed",
+                     "attn_decode_split_packed",
                      "attn_decode_split", "attn_merge",
                      "attn_sync_check",
                      "attn_version", "attn_debug_wait_timeout", "attn_decode_noalloc"):
@@ -89,6 +91,13 @@ def attn_decode_packed(q, kcache, vcache, kv_lens, B, Hq, Hkv, d, max_kv, scale,
                        stream) -> int:
     return load().attn_decode_packed(q, kcache, vcache, kv_lens, B, Hq, Hkv, d, max_kv, float(scale),
                                      o, lse, o_dtype, stream)
+
+
+def attn_decode_split_packed(q, kcache, vcache, kv_lens, B, Hq, Hkv, d, max_kv, scale, n_splits,
+                             min_rows_per_split, part_o, part_lse, stream) -> int:
+    return load().attn_decode_split_packed(q, kcache, vcache, kv_lens, B, Hq, Hkv, d, max_kv,
+                                           float(scale), n_splits, min_rows_per_split, part_o, part_lse,
+                                           stream)
 
 
 def attn_prefill_window(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, d, window, n_sink, scale, o_dtype,
@@ -337,12 +346,44 @@ def decode(q, kcache, vcache, kv_lens, n_splits: int, min_rows_per_split: int = 
     return merge(po, pl, out_dtype, stream)
 
 
+def decode_split_packed(q, kcache, vcache, kv_lens, n_splits: int, min_rows_per_split: int = 1,
+                        scale: float | None = None, stream=None, out=None):
+    """Split-KV decode partials on the tensor cores (attn_decode_split_packed); same
+    contract as decode_split.  Returns (part_o [B,Hq,n_splits,d], part_lse [B,Hq,n_splits])."""
+    torch = _torch()
+    _check_tensor(q, "q", torch.bfloat16, 3)
+    _check_tensor(kcache, "kcache", torch.bfloat16, 4)
+    _check_tensor(vcache, "vcache", torch.bfloat16, 4)
+    _check_tensor(kv_lens, "kv_lens", torch.int32, 1)
+    B, Hq, d = q.shape
+    _, max_kv, Hkv, _ = kcache.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        part_o = torch.empty((B, Hq, n_splits, d), dtype=torch.float32, device=q.device)
+        part_lse = torch.empty((B, Hq, n_splits), dtype=torch.float32, device=q.device)
+    else:
+        part_o, part_lse = out
+    rc = attn_decode_split_packed(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(kv_lens), B, Hq, Hkv, d,
+                                  max_kv, scale, n_splits, min_rows_per_split, _ptr(part_o),
+                                  _ptr(part_lse), _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_decode_split_packed")
+    return part_o, part_lse
+
+
 def decode_packed(q, kcache, vcache, kv_lens, scale: float | None = None, out_dtype=None,
-                  stream=None, out=None):
-    """One-token decode on the tensor cores, heads packed into the tile rows
-    (attn_decode_packed).  q [B,Hq,d], caches [B,max_kv,Hkv,d] bf16, kv_lens int32 [B].
+                  stream=None, out=None, n_splits: int = 1, min_rows_per_split: int = 1):
+    """One-token decode on the tensor cores, heads packed into the tile rows.
+    q [B,Hq,d], caches [B,max_kv,Hkv,d] bf16, kv_lens int32 [B].  n_splits > 1 splits
+    each sequence's keys (attn_decode_split_packed) and merges the partials
+    (attn_merge); n_splits = 1 is one launch (attn_decode_packed).
 
     Returns (o [B,Hq,d] in out_dtype (default bf16), lse [B,Hq] fp32)."""
+    if n_splits > 1:
+        po, pl = decode_split_packed(q, kcache, vcache, kv_lens, n_splits, min_rows_per_split, scale,
+                                     stream)
+        return merge(po, pl, out_dtype, stream, out)
     torch = _torch()
     out_dtype = out_dtype or torch.bfloat16
     _check_tensor(q, "q", torch.bfloat16, 3)

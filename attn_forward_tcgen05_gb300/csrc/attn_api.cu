@@ -104,7 +104,8 @@ int from_cuda(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA
 static int prefill_impl(const attn_bf16_t* q, const attn_bf16_t* k, const attn_bf16_t* v, void* o,
                         float* lse, int B, int Hq, int Hkv, int Sq, int Skv, int d, int causal,
                         int window, int n_sink, float scale, int o_dtype, attn_stream_t stream,
-                        const int* kv_lens = nullptr, int pack = 1) {
+                        const int* kv_lens = nullptr, int pack = 1, int n_splits = 1,
+                        int split_min = 0, float* part_o = nullptr, float* part_lse = nullptr) {
   if (B < 0 || Sq < 0 || Skv < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (!ok_scale(scale)) return ATTN_ERR_INVALID_ARG;
   if (!ok_dim(d) || (o_dtype != ATTN_F32 && o_dtype != ATTN_BF16)) return ATTN_ERR_UNSUPPORTED;
@@ -127,6 +128,10 @@ static int prefill_impl(const attn_bf16_t* q, const attn_bf16_t* k, const attn_b
   a.n_sink = n_sink;
   a.kv_lens = kv_lens;
   a.pack = pack;
+  a.n_splits = n_splits;
+  a.split_min = split_min;
+  a.part_o = part_o;
+  a.part_lse = part_lse;
   a.err = err_word();
   if (a.err == nullptr) return ATTN_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -245,6 +250,28 @@ int attn_decode_packed(const attn_bf16_t* q, const attn_bf16_t* kcache, const at
   // one query position per sequence, the last one: causal admits keys [0, kv_lens[b])
   return prefill_impl(q, kcache, vcache, o, lse, B, Hq, Hkv, 1, max_kv, d, 1, 0, 0, scale, o_dtype,
                       stream, kv_lens, Hq / Hkv);
+}
+
+int attn_decode_split_packed(const attn_bf16_t* q, const attn_bf16_t* kcache,
+                             const attn_bf16_t* vcache, const int* kv_lens, int B, int Hq, int Hkv,
+                             int d, int max_kv, float scale, int n_splits, int min_rows_per_split,
+                             float* part_o, float* part_lse, attn_stream_t stream) {
+  if (B < 0 || max_kv < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (n_splits < 1 || n_splits > 1024 || min_rows_per_split < 0 || !ok_scale(scale))
+    return ATTN_ERR_INVALID_ARG;
+  if (!packable(Hq, Hkv, d)) return ATTN_ERR_UNSUPPORTED;
+  if (B == 0) return ATTN_OK;
+  if (!kv_lens || (reinterpret_cast<uintptr_t>(kv_lens) & 3)) return ATTN_ERR_INVALID_ARG;
+  if (!part_o || !part_lse || !aligned16(part_o) || !aligned16(part_lse)) return ATTN_ERR_INVALID_ARG;
+  if ((long long)B * Hq * n_splits >= (1LL << 31)) return ATTN_ERR_INVALID_ARG;
+  if (max_kv == 0) {
+    // no keys anywhere: every partial is empty (o = 0, lse = -inf)
+    return prefill_impl(q, kcache, vcache, part_o, part_lse, B * n_splits, Hq, Hkv, 1, 0, d, 1, 0, 0,
+                        scale, ATTN_F32, stream);
+  }
+  return prefill_impl(q, kcache, vcache, part_o, part_lse, B, Hq, Hkv, 1, max_kv, d, 1, 0, 0, scale,
+                      ATTN_F32, stream, kv_lens, Hq / Hkv, n_splits, min_rows_per_split, part_o,
+                      part_lse);
 }
 
 int attn_prefill_varlen(const attn_bf16_t* q, const attn_bf16_t* kcache, const attn_bf16_t* vcache,

@@ -35,6 +35,14 @@ struct PrefillArgs {
   int window;                    // > 0: causal sliding window of this many positions
   int n_sink;                    // with a window: the first n_sink keys stay admissible
   int pack;                      // query rows per position (G); 1 = one head per tile
+  // key splits (one-token decode with kv_lens, single-CTA kernel): n_splits > 1
+  // writes per-split partials part_o [B][Hq][n_splits][d] (fp32, normalised within
+  // the split) and part_lse [B][Hq][n_splits] instead of o / lse; split s of a
+  // sequence with L keys covers [s*chunk, min(L, (s+1)*chunk)),
+  // chunk = max(ceil(L / n_splits), split_min)
+  int n_splits, split_min;
+  float* part_o;
+  float* part_lse;
 };
 
 #ifdef __CUDACC__

@@ -129,9 +129,11 @@ struct TileInfo {
 };
 
 // q0: first row of the tile; Sr: rows of the sequence (Sq positions x G heads);
-// the causal bound of a row follows its position row / G.
+// the causal bound of a row follows its position row / G.  Keys at or past kend
+// (the end of a key split; Skv without one) are not admitted.
 template <int BN>
-__device__ __forceinline__ TileInfo tile_info(int q0, int Sr, int Sq, int G, int Skv, int causal) {
+__device__ __forceinline__ TileInfo tile_info(int q0, int Sr, int Sq, int G, int Skv, int causal,
+                                              int kend) {
   TileInfo ti;
   ti.q0 = q0;
   if (q0 >= Sr) {
@@ -148,21 +150,24 @@ __device__ __forceinline__ TileInfo tile_info(int q0, int Sr, int Sq, int G, int
     kv_hi = (int)(hi < 0 ? 0 : (hi > Skv ? Skv : hi));
     kv_lo = (int)(lo < 0 ? 0 : (lo > Skv ? Skv : lo));
   }
+  kv_hi = min(kv_hi, kend);
   ti.n_kv = (kv_hi + BN - 1) / BN;
-  ti.kv_lo = kv_lo;
+  ti.kv_lo = min(kv_lo, kend);
   return ti;
 }
 
 // WIN: causal sliding window with attention sinks (window, n_sink); without it
-// both are ignored and the tile list is every KV tile
-template <int D, bool WIN>
+// both are ignored and the tile list is every KV tile.  SPLIT: key splits with
+// decode partials (n_splits, split_min, part_o, part_lse); without it they are ignored.
+template <int D, bool WIN, bool SPLIT>
 __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
     fmha_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, void* __restrict__ o_ptr,
                     float* __restrict__ lse_ptr, int Hq, int Hkv, int Sq_max, int Skv_max, int causal,
                     int o_bf16, float scale, int n_units_per_head_batch, uint32_t* err,
                     const int* __restrict__ cu_q, const int* __restrict__ kv_lens, int total_q,
-                    int window, int n_sink, int pack) {
+                    int window, int n_sink, int pack, int n_splits, int split_min,
+                    float* __restrict__ part_o, float* __restrict__ part_lse) {
   using C = PrefillCfg<D>;
   constexpr int NQ = C::NQ, NS = C::NS, BN = C::BN;
   static_assert(C::kSub == 1, "a KV stage is one tile (the sliding-window tile list maps tiles, not stages)");
@@ -175,8 +180,11 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
   const int Hu = Hq / G;                  // head groups
   const int HB = n_units_per_head_batch;  // Hu * B
   const int n_blocks_q = (Sq_max * G + NQ * kPrefillTileM - 1) / (NQ * kPrefillTileM);
+  // key splits (one-token decode only): unit = (query block, split, head group, batch)
+  const int NSPL = SPLIT ? n_splits : 1;
   const int u = blockIdx.x;
-  const int qb = causal ? (n_blocks_q - 1 - u / HB) : (u / HB);
+  const int qb = causal ? (n_blocks_q - 1 - u / (HB * NSPL)) : (u / (HB * NSPL));
+  const int sp = (u % (HB * NSPL)) / HB;
   const int hb = u % HB;
   const int hu = hb % Hu, b = hb / Hu;
   const int hk = (hu * G) / (Hq / Hkv);
@@ -184,6 +192,15 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
   const SeqExtent ext = seq_extent(b, Sq_max, Skv_max, cu_q, kv_lens, total_q);
   const int Sq = ext.Sq, Skv = ext.Skv;
   const int Sr = Sq * G;  // tile rows of this sequence
+  // keys [klo, khi) of this unit: split sp of the sequence's keys (the split rule of
+  // the decode partials: chunk = max(ceil(Skv / n_splits), split_min)), or all of them
+  int klo = 0, khi = Skv;
+  if (SPLIT) {
+    const int chunk = max((Skv + NSPL - 1) / NSPL, split_min);
+    const long long lo = (long long)sp * chunk;
+    klo = (int)min((long long)Skv, lo);
+    khi = (int)min((long long)Skv, lo + chunk);
+  }
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -207,18 +224,19 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
   TileInfo ti[NQ];
 #pragma unroll
   for (int t = 0; t < NQ; ++t)
-    ti[t] = tile_info<BN>(qb * NQ * kPrefillTileM + t * kPrefillTileM, Sr, Sq, G, Skv, causal);
+    ti[t] = tile_info<BN>(qb * NQ * kPrefillTileM + t * kPrefillTileM, Sr, Sq, G, Skv, causal, khi);
   int n_kv = 0;
 #pragma unroll
   for (int t = 0; t < NQ; ++t) n_kv = max(n_kv, ti[t].n_kv);
-  // with a sliding window the loops below run over a list of KV tiles (list index
-  // j, key tile tile_list_key(tl, j)); without one the list is every tile
+  // the loops below run over a list of KV tiles (list index j, key tile
+  // tile_list_key(tl, j)): with a sliding window the sink tiles and the window's
+  // tiles, with a key split the tiles from the split's first one, else every tile
   const long long pos_off = (long long)Skv - Sq;  // key position of query row i: i + pos_off
   const TileList tl = WIN ? tile_list((long long)(ti[0].q0 / G) + pos_off, n_kv, window, n_sink, Skv, BN)
-                          : TileList{0x7FFFFFFF, 0};
+                          : (SPLIT ? TileList{0, klo / BN} : TileList{0x7FFFFFFF, 0});
 #pragma unroll
-  for (int t = 0; t < NQ; ++t) ti[t].n_kv = tile_list_len(tl, ti[t].n_kv);
-  n_kv = tile_list_len(tl, n_kv);
+  for (int t = 0; t < NQ; ++t) ti[t].n_kv = klo < khi ? tile_list_len(tl, ti[t].n_kv) : 0;
+  n_kv = klo < khi ? tile_list_len(tl, n_kv) : 0;
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
@@ -448,10 +466,10 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
     const float sl2 = scale * kLog2e;
     // admissible keys of this row: [0, row_bound), and with a sliding window only
     // [row_lo, row_bound) plus the sinks [0, n_sink)
-    int row_bound = Skv;
+    int row_bound = khi;
     if (causal) {
       const long long rb = (long long)qpos + pos_off + 1;  // causal bound of this row
-      row_bound = (int)(rb < 0 ? 0 : (rb > Skv ? Skv : rb));
+      row_bound = (int)(rb < 0 ? 0 : (rb > khi ? khi : rb));
     }
     // (32-bit, clamped: key indices are below 2^31; a bound below 0 masks nothing)
     auto clamp_key = [](long long x) { return (int)(x < -1 ? -1 : (x > 0x7FFFFFFF ? 0x7FFFFFFF : x)); };
@@ -478,11 +496,11 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
       // mask: keys at or past row_bound (causal bound or Skv), and with a window the
       // keys below the row's window that are not sinks
       const int key0 = tile_list_key(tl, j) * BN;
-      if (key0 + BN > my.kv_lo) {
-        const int lim = row_bound - key0;
+      if (key0 + BN > my.kv_lo || (SPLIT && key0 < klo)) {
+        const int lim = row_bound - key0, low = klo - key0;  // and keys below the split
 #pragma unroll
         for (int c = 0; c < BN; ++c)
-          if (c >= lim) sr[c] = __float_as_uint(-INFINITY);
+          if (c >= lim || (SPLIT && c < low)) sr[c] = __float_as_uint(-INFINITY);
       }
       if (WIN && key0 < tile_lo_max && key0 + BN > n_sink) {
 #pragma unroll
@@ -574,7 +592,12 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
     const bool row_ok = qrow < Sr;
     const uint32_t o_addr = lane_addr + C::o_col(t);
     const int hq = hu * G + qg;  // query head of this row
-    const size_t orow = ((size_t)ext.bq * ext.rows + ext.qbase + (size_t)(row_ok ? qpos : 0)) * Hq + hq;
+    // with key splits the row is a decode partial: part_o / part_lse [B][Hq][n_splits]
+    const bool partial = SPLIT;
+    const size_t prow = ((size_t)b * Hq + hq) * NSPL + sp;
+    const size_t orow = partial ? prow
+                                : ((size_t)ext.bq * ext.rows + ext.qbase + (size_t)(row_ok ? qpos : 0)) * Hq + hq;
+    void* const out = partial ? static_cast<void*>(part_o) : o_ptr;
 #pragma unroll
     for (int c0 = 0; c0 < D; c0 += 32) {
       uint32_t ov[32];
@@ -586,7 +609,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
         for (int e = 0; e < 32; ++e) ov[e] = 0u;
       }
       if (row_ok && ok) {
-        if (o_bf16) {
+        if (o_bf16 && !partial) {
           uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(o_ptr) + orow * D + c0);
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
@@ -598,7 +621,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
             dst[q4] = w;
           }
         } else {
-          float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(o_ptr) + orow * D + c0);
+          float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + orow * D + c0);
 #pragma unroll
           for (int q4 = 0; q4 < 8; ++q4) {
             dst[q4] = make_float4(__uint_as_float(ov[4 * q4 + 0]) * inv_l, __uint_as_float(ov[4 * q4 + 1]) * inv_l,
@@ -608,7 +631,9 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
       }
     }
     if (row_ok && ok) {
-      lse_ptr[((size_t)ext.bq * Hq + hq) * ext.rows + ext.qbase + qpos] = have ? (m_used + log2f(l)) * kLn2 : -INFINITY;
+      const float lse_v = have ? (m_used + log2f(l)) * kLn2 : -INFINITY;
+      if (partial) part_lse[prow] = lse_v;
+      else lse_ptr[((size_t)ext.bq * Hq + hq) * ext.rows + ext.qbase + qpos] = lse_v;
     }
   }
 
@@ -635,18 +660,22 @@ __global__ void fill_empty_kernel(void* o, float* lse, size_t n_o, size_t n_lse,
 template <int D>
 cudaError_t launch_prefill_t(const PrefillArgs& a, cudaStream_t stream) {
   using C = PrefillCfg<D>;
-  auto kern = a.window > 0 ? fmha_fwd_kernel<D, true> : fmha_fwd_kernel<D, false>;
+  const bool split = a.n_splits > 1;
+  auto kern = a.window > 0 ? fmha_fwd_kernel<D, true, false>
+                           : (split ? fmha_fwd_kernel<D, false, true> : fmha_fwd_kernel<D, false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int G = a.pack;
   const long long rows = (long long)a.Sq * G;
   const long long n_blocks_q = (rows + C::NQ * kPrefillTileM - 1) / (C::NQ * kPrefillTileM);
-  const long long units = n_blocks_q * (a.Hq / G) * a.B;
+  const int n_splits = a.n_splits > 1 ? a.n_splits : 1;
+  const long long units = n_blocks_q * (a.Hq / G) * a.B * n_splits;
   if (units <= 0) return cudaSuccess;
   if (units > 0x7FFFFFFFLL || rows > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
   kern<<<(unsigned)units, C::kThreads, C::kSmemBytes, stream>>>(
       a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, a.Hq, a.Hkv, a.Sq, a.Skv, a.causal, a.o_bf16, a.scale,
-      (a.Hq / G) * a.B, a.err, a.cu_q, a.kv_lens, a.total_q, a.window, a.n_sink, G);
+      (a.Hq / G) * a.B, a.err, a.cu_q, a.kv_lens, a.total_q, a.window, a.n_sink, G, n_splits,
+      a.split_min, a.part_o, a.part_lse);
   return cudaGetLastError();
 }
 

@@ -84,6 +84,11 @@ MQA_DECODE = DecodeShape("mqa_decode_b128_h128", 128, 128, 1, 128, 1.0 / math.sq
                          1, 1008, len_range=(512, 8192))
 
 
+# key splits of the multi-query decode on the tensor cores: (n_splits, min rows per
+# split), 128-key multiples so a split is whole KV tiles
+MQA_DECODE_SPLITS = (16, 512)
+
+
 def decode_flops(kv_lens, Hq, d) -> int:
     """Algorithmic decode FLOPs: 4*d per (query head, cached key) pair."""
     total = int(torch.as_tensor(kv_lens).to(torch.int64).sum().item())

@@ -157,6 +157,24 @@ int attn_decode_packed(const attn_bf16_t* q, const attn_bf16_t* kcache, const at
                        void* o, float* lse, int o_dtype, attn_stream_t stream);
 
 /*
+ * attn_decode_split_packed -- attn_decode_split on the tensor cores with head
+ * packing: the same partials (part_o, part_lse), split rule, layouts and empty-split
+ * convention, to be combined by attn_merge.
+ *
+ * Each (sequence, split, KV head) is one unit of work whose G = Hq/Hkv query
+ * heads fill the rows of an MMA tile (the FMHA page's D2); splits spread a long
+ * sequence's keys over several SMs ("66 . D2: explicit K+V register staging",
+ * section 3.2: rows [lo, hi) of one sequence).  Requires d in {64, 128} and G
+ * dividing 128; part_o and part_lse 16-byte aligned.  Arguments as for
+ * attn_decode_split (n_splits in [1, 1024], min_rows_per_split >= 0).
+ * Returns ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED or ATTN_ERR_CUDA.
+ */
+int attn_decode_split_packed(const attn_bf16_t* q, const attn_bf16_t* kcache,
+                             const attn_bf16_t* vcache, const int* kv_lens, int B, int Hq, int Hkv,
+                             int d, int max_kv, float scale, int n_splits, int min_rows_per_split,
+                             float* part_o, float* part_lse, attn_stream_t stream);
+
+/*
  * attn_prefill_varlen -- prefill of a packed batch of sequences of different
  * lengths against a KV cache (chunked prefill).
  *

@@ -118,6 +118,18 @@ def test_packed_validation(lib):
     assert g(N, N, N, N, 0, 8, 1, 64, 16, 0.5, N, N, 0, N) == attn.ATTN_OK  # empty batch
 
 
+def test_split_packed_validation(lib):
+    f = attn.attn_decode_split_packed
+    #      q  kc vc kv  B  Hq Hkv d   mkv scale ns mr po pl stream
+    assert f(P, P, P, P, 2, 8, 1, 256, 16, 0.5, 4, 1, P, P, N) == attn.ATTN_ERR_UNSUPPORTED  # d
+    assert f(P, P, P, P, 2, 12, 4, 64, 16, 0.5, 4, 1, P, P, N) == attn.ATTN_ERR_UNSUPPORTED  # G = 3
+    assert f(P, P, P, P, 2, 8, 1, 64, 16, 0.5, 0, 1, P, P, N) == attn.ATTN_ERR_INVALID_ARG  # n_splits
+    assert f(P, P, P, P, 2, 8, 1, 64, 16, 0.5, 4, -1, P, P, N) == attn.ATTN_ERR_INVALID_ARG  # min rows
+    assert f(P, P, P, P, 2, 8, 1, 64, 16, 0.5, 4, 1, N, P, N) == attn.ATTN_ERR_INVALID_ARG  # null part_o
+    assert f(P, P, P, P, 2, 8, 1, 64, 16, 0.5, 4, 1, P, M, N) == attn.ATTN_ERR_INVALID_ARG  # part_lse align
+    assert f(N, N, N, N, 0, 8, 1, 64, 16, 0.5, 4, 1, N, N, N) == attn.ATTN_OK  # empty batch
+
+
 def test_decode_and_merge_validation(lib):
     f = attn.attn_decode_split
     assert f(P, P, P, P, 1, 28, 4, 96, 10, 0.1, 8, 1, P, P, N) == attn.ATTN_ERR_UNSUPPORTED

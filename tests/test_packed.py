@@ -92,3 +92,53 @@ def test_mqa_decode_workload_sampled():
     ro, rl = oracle.decode(q[pick], kc[pick], vc[pick], lens[pick], s.scale)
     check_o(o[pick].float().cpu().numpy(), ro, True)
     check_lse(lse[pick].cpu().numpy(), rl)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("Hq,Hkv", [(128, 1), (16, 2)])
+@pytest.mark.parametrize("n_splits,min_rows", [(1, 1), (3, 1), (8, 256), (16, 64)])
+def test_packed_decode_split_partials(d, Hq, Hkv, n_splits, min_rows):
+    """Partials with the decode split rule (empty splits included) against the
+    oracle's split partials, then merged against the oracle's decode."""
+    from attn_forward_tcgen05_gb300 import decode_split_packed, merge
+    lens = torch.tensor([0, 1, 29, 300, 1000, 2049, 5], dtype=torch.int32)
+    q, kc, vc = W.decode_inputs(len(lens), Hq, Hkv, d, lens, 700 + d + n_splits)
+    scale = 1.0 / np.sqrt(d)
+    po, pl = decode_split_packed(q.cuda(), kc.cuda(), vc.cuda(), lens.cuda(), n_splits, min_rows, scale)
+    o, lse = merge(po, pl, torch.float32)
+    sync_check()
+    ro, rl = oracle.decode_split(q, kc, vc, lens, scale, n_splits, min_rows)
+    got_o, got_l = po.cpu().numpy(), pl.cpu().numpy()
+    assert np.array_equal(np.isneginf(got_l), np.isneginf(rl))
+    assert np.all(got_o[np.isneginf(rl)] == 0)
+    check_o(got_o, ro, False)
+    check_lse(got_l, rl)
+    fo, fl = oracle.decode(q, kc, vc, lens, scale)
+    check_o(o.cpu().numpy(), fo, False)
+    check_lse(lse.cpu().numpy(), fl)
+
+
+def test_packed_decode_no_keys_with_splits():
+    from attn_forward_tcgen05_gb300 import decode_split_packed
+    lens = torch.zeros(3, dtype=torch.int32)
+    q, kc, vc = W.decode_inputs(3, 8, 1, 64, lens, 721, Lmax=0)
+    po, pl = decode_split_packed(q.cuda(), kc.cuda(), vc.cuda(), lens.cuda(), 4, 1, 0.125)
+    sync_check()
+    assert np.all(po.cpu().numpy() == 0) and np.all(np.isneginf(pl.cpu().numpy()))
+
+
+def test_mqa_decode_workload_split_sampled():
+    """The multi-query decode workload as the benchmark runs it (split partials +
+    merge), sampled sequences against the oracle."""
+    s = W.MQA_DECODE
+    q, kc, vc, lens = W.decode_inputs_for(s)
+    o, lse = decode_packed(q.cuda(), kc.cuda(), vc.cuda(), lens.cuda(), s.scale,
+                           n_splits=MQA_SPLITS, min_rows_per_split=MQA_MIN_ROWS)
+    sync_check()
+    pick = [0, 5, 31, 64, 127]
+    ro, rl = oracle.decode(q[pick], kc[pick], vc[pick], lens[pick], s.scale)
+    check_o(o[pick].float().cpu().numpy(), ro, True)
+    check_lse(lse[pick].cpu().numpy(), rl)
+
+
+MQA_SPLITS, MQA_MIN_ROWS = W.MQA_DECODE_SPLITS
