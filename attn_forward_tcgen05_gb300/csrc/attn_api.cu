@@ -140,6 +140,9 @@ static int prefill_impl(const attn_bf16_t* q, const attn_bf16_t* k, const attn_b
   if (pair && pack != 1) return ATTN_ERR_UNSUPPORTED;
   int rc = pair ? encode_bf16_4d(&a.tm_q, q, d, Hq, Sq, B, attn::kPrefillTileM)
                 : encode_bf16_q5d(&a.tm_q, q, d, pack, Hq, Sq, B);
+  // bf16 O of the single-CTA kernel leaves through TMA stores (same shape as Q)
+  a.o_tma = (!pair && o_dtype == ATTN_BF16 && n_splits <= 1) ? 1 : 0;
+  if (rc == ATTN_OK && a.o_tma) rc = encode_bf16_q5d(&a.tm_o, o, d, pack, Hq, Sq, B);
   if (rc == ATTN_OK) rc = encode_bf16_4d(&a.tm_k, k, d, Hkv, Skv, B, attn::prefill_k_box_rows(d));
   if (rc == ATTN_OK) rc = encode_bf16_4d(&a.tm_v, v, d, Hkv, Skv, B, attn::kPrefillKVStageRows);
   if (rc != ATTN_OK) return rc;

@@ -19,6 +19,8 @@ namespace attn {
 // head fill the rows of a query tile, row r = position r / G, head r % G of the
 // group, so a tile holds 128 / G positions.
 struct PrefillArgs {
+  CUtensorMap tm_o;              // bf16 O of the single-CTA kernel when o_tma: the Q map's shape
+  int o_tma;                     // 1: O leaves through shared memory and TMA stores
   CUtensorMap tm_q, tm_k, tm_v;  // K, V (and Q of the pair kernel): 4-D maps {d, H, S, B},
                                  // box {64, 1, rows, 1}, 128B swizzle: rows = kPrefillTileM
                                  // for Q, prefill_k_box_rows(d) for K, kPrefillKVStageRows

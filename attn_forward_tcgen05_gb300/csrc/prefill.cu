@@ -162,7 +162,8 @@ __device__ __forceinline__ TileInfo tile_info(int q0, int Sr, int Sq, int G, int
 template <int D, bool WIN, bool SPLIT>
 __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
     fmha_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, void* __restrict__ o_ptr,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                    int o_tma, void* __restrict__ o_ptr,
                     float* __restrict__ lse_ptr, int Hq, int Hkv, int Sq_max, int Skv_max, int causal,
                     int o_bf16, float scale, int n_units_per_head_batch, uint32_t* err,
                     const int* __restrict__ cu_q, const int* __restrict__ kv_lens, int total_q,
@@ -598,34 +599,73 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
     const size_t orow = partial ? prow
                                 : ((size_t)ext.bq * ext.rows + ext.qbase + (size_t)(row_ok ? qpos : 0)) * Hq + hq;
     void* const out = partial ? static_cast<void*>(part_o) : o_ptr;
+    if (!SPLIT && o_tma) {
+      // bf16 O through shared memory: every S MMA of this tile has completed (its
+      // last P.V has), so the tile's Q buffer takes O in the same 128-byte-swizzled
+      // layout and one TMA store per panel writes it (rows past Sq are clipped)
+      uint8_t* const stile = sQ + t * C::kQTileBytes;
 #pragma unroll
-    for (int c0 = 0; c0 < D; c0 += 32) {
-      uint32_t ov[32];
-      if (load_o) {
-        tmem_ld32(o_addr + c0, ov);
-        tmem_wait_ld();
-      } else {
-#pragma unroll
-        for (int e = 0; e < 32; ++e) ov[e] = 0u;
-      }
-      if (row_ok && ok) {
-        if (o_bf16 && !partial) {
-          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(o_ptr) + orow * D + c0);
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(ov[8 * q4 + 0]) * inv_l, __uint_as_float(ov[8 * q4 + 1]) * inv_l);
-            w.y = pack_bf16x2(__uint_as_float(ov[8 * q4 + 2]) * inv_l, __uint_as_float(ov[8 * q4 + 3]) * inv_l);
-            w.z = pack_bf16x2(__uint_as_float(ov[8 * q4 + 4]) * inv_l, __uint_as_float(ov[8 * q4 + 5]) * inv_l);
-            w.w = pack_bf16x2(__uint_as_float(ov[8 * q4 + 6]) * inv_l, __uint_as_float(ov[8 * q4 + 7]) * inv_l);
-            dst[q4] = w;
-          }
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t ov[32];
+        if (load_o) {
+          tmem_ld32(o_addr + c0, ov);
+          tmem_wait_ld();
         } else {
-          float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + orow * D + c0);
 #pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4) {
-            dst[q4] = make_float4(__uint_as_float(ov[4 * q4 + 0]) * inv_l, __uint_as_float(ov[4 * q4 + 1]) * inv_l,
-                                  __uint_as_float(ov[4 * q4 + 2]) * inv_l, __uint_as_float(ov[4 * q4 + 3]) * inv_l);
+          for (int e = 0; e < 32; ++e) ov[e] = 0u;
+        }
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint4 w;
+          w.x = pack_bf16x2(__uint_as_float(ov[8 * q4 + 0]) * inv_l, __uint_as_float(ov[8 * q4 + 1]) * inv_l);
+          w.y = pack_bf16x2(__uint_as_float(ov[8 * q4 + 2]) * inv_l, __uint_as_float(ov[8 * q4 + 3]) * inv_l);
+          w.z = pack_bf16x2(__uint_as_float(ov[8 * q4 + 4]) * inv_l, __uint_as_float(ov[8 * q4 + 5]) * inv_l);
+          w.w = pack_bf16x2(__uint_as_float(ov[8 * q4 + 6]) * inv_l, __uint_as_float(ov[8 * q4 + 7]) * inv_l);
+          const int chunk = (c0 >> 3) + q4;  // 16-byte chunk of the row
+          const int pnl = chunk >> 3, cc = chunk & 7;
+          *reinterpret_cast<uint4*>(stile + pnl * C::kQPanelBytes + r * 128 + ((cc ^ (r & 7)) << 4)) = w;
+        }
+      }
+      fence_proxy_async_smem();
+      // the warpgroup's rows are all in place (and every wait of theirs succeeded)
+      const bool all_ok = bar_sync_and(1 + t, 128, ok);
+      if (all_ok && my.q0 < Sr && (threadIdx.x & 127) == 0) {  // a tile past the end stores nothing
+#pragma unroll
+        for (int pnl = 0; pnl < C::kPanels; ++pnl)
+          tma_store_5d(&tm_o, stile + pnl * C::kQPanelBytes, pnl * 64, 0, hu, ext.qbase + my.q0 / G, ext.bq);
+        tma_store_commit();
+        tma_store_wait_read();  // shared memory stays valid until the store has read it
+      }
+    } else {
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t ov[32];
+        if (load_o) {
+          tmem_ld32(o_addr + c0, ov);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) ov[e] = 0u;
+        }
+        if (row_ok && ok) {
+          if (o_bf16 && !partial) {
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(o_ptr) + orow * D + c0);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(ov[8 * q4 + 0]) * inv_l, __uint_as_float(ov[8 * q4 + 1]) * inv_l);
+              w.y = pack_bf16x2(__uint_as_float(ov[8 * q4 + 2]) * inv_l, __uint_as_float(ov[8 * q4 + 3]) * inv_l);
+              w.z = pack_bf16x2(__uint_as_float(ov[8 * q4 + 4]) * inv_l, __uint_as_float(ov[8 * q4 + 5]) * inv_l);
+              w.w = pack_bf16x2(__uint_as_float(ov[8 * q4 + 6]) * inv_l, __uint_as_float(ov[8 * q4 + 7]) * inv_l);
+              dst[q4] = w;
+            }
+          } else {
+            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + orow * D + c0);
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) {
+              dst[q4] = make_float4(__uint_as_float(ov[4 * q4 + 0]) * inv_l, __uint_as_float(ov[4 * q4 + 1]) * inv_l,
+                                    __uint_as_float(ov[4 * q4 + 2]) * inv_l, __uint_as_float(ov[4 * q4 + 3]) * inv_l);
+            }
           }
         }
       }
@@ -673,7 +713,7 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, cudaStream_t stream) {
   if (units <= 0) return cudaSuccess;
   if (units > 0x7FFFFFFFLL || rows > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
   kern<<<(unsigned)units, C::kThreads, C::kSmemBytes, stream>>>(
-      a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, a.Hq, a.Hkv, a.Sq, a.Skv, a.causal, a.o_bf16, a.scale,
+      a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.o_tma, a.o, a.lse, a.Hq, a.Hkv, a.Sq, a.Skv, a.causal, a.o_bf16, a.scale,
       (a.Hq / G) * a.B, a.err, a.cu_q, a.kv_lens, a.total_q, a.window, a.n_sink, G, n_splits,
       a.split_min, a.part_o, a.part_lse);
   return cudaGetLastError();
