@@ -107,6 +107,23 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------- ours
+def run_line(args):
+    """One extra workload line alone (--line), for profiling its kernel."""
+    import torch
+
+    import attn_forward_tcgen05_gb300 as attn
+    from attn_forward_tcgen05_gb300 import workloads as W
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    attn.load()
+    peaks, peak_src = load_peaks()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    fn = {"varlen": time_varlen, "window": time_window, "mqa": time_mqa_decode}[args.line]
+    return fn(args, attn, W, dev, stream, flush, peaks, peak_src)
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
 
@@ -372,6 +389,7 @@ def time_window(args, attn, W, dev, stream, flush, peaks, peak_src):
             "us": round(ms * 1e3, 2), "value": round(tf, 2), "unit": "TFLOP/s", "steps": n,
             "roofline": {"bound": "tensor", "kernel": kern, "achieved": round(tf, 2),
                          "peak": peak_tc, "unit": "TFLOP/s", "frac": round(tf / peak_tc, 4),
+                         "traffic": load_traffic().get(f"{kern} window {S.name}"),
                          "peak_source": f"bf16_tflops (burst) of {peak_src}"}}
 
 
@@ -415,7 +433,9 @@ def time_mqa_decode(args, attn, W, dev, stream, flush, peaks, peak_src):
                          "peak": peak_tc, "unit": "TFLOP/s", "frac": round(tf / peak_tc, 4),
                          "peak_source": f"bf16_tflops (burst) of {peak_src}"},
             "roofline_hbm": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak_hbm, "unit": "GB/s",
-                             "frac": round(gbs / peak_hbm, 4), "peak_source": f"hbm_gbs of {peak_src}"}}
+                             "frac": round(gbs / peak_hbm, 4),
+                             "traffic": load_traffic().get(f"fmha_fwd_kernel<{S.d}> packed {S.name}"),
+                             "peak_source": f"hbm_gbs of {peak_src}"}}
 
 
 def run_e2e(args, attn, W, dev, stream, P, dec, flops):
@@ -575,6 +595,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--only", choices=("prefill", "decode"), default=None,
                     help="time only one part of the step (profiling runs)")
+    ap.add_argument("--line", choices=("varlen", "window", "mqa"), default=None,
+                    help="time only one of the extra workload lines and print it (profiling runs)")
     ap.add_argument("--prefill-workload", default="gqa_prefill_3314",
                     help="prefill workload of the step (the head-dim sweep shapes are for profiling)")
     args = ap.parse_args()
@@ -592,6 +614,10 @@ def main():
             return
         line = run_reference(args, rank, world)
         print(json.dumps(line))
+        return
+    if args.line:
+        if rank == 0:
+            print(json.dumps(run_line(args)))
         return
     if world > 1:
         import torch
