@@ -184,9 +184,11 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
   // key splits (one-token decode only): unit = (query block, split, head group, batch)
   const int NSPL = SPLIT ? n_splits : 1;
   const int u = blockIdx.x;
-  const int qb = causal ? (n_blocks_q - 1 - u / (HB * NSPL)) : (u / (HB * NSPL));
-  const int sp = (u % (HB * NSPL)) / HB;
-  const int hb = u % HB;
+  // causal: heaviest query blocks first; non-causal: the query blocks of one head
+  // are neighbours, so that head's K/V stay in L2 while they run
+  const int qb = causal ? (n_blocks_q - 1 - u / (HB * NSPL)) : (u % n_blocks_q);
+  const int sp = causal ? (u % (HB * NSPL)) / HB : 0;
+  const int hb = causal ? u % HB : u / n_blocks_q;
   const int hu = hb % Hu, b = hb / Hu;
   const int hk = (hu * G) / (Hq / Hkv);
   // this sequence's query positions and keys (fixed-length or packed varlen batch)

@@ -142,8 +142,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<D>::kThreads
   const int HB = n_units_per_head_batch;  // Hq * B
   const int n_blocks_q = (Sq_max + 2 * kPrefillTileM - 1) / (2 * kPrefillTileM);
   const int pair = blockIdx.x >> 1;
-  const int qb = causal ? (n_blocks_q - 1 - pair / HB) : (pair / HB);
-  const int hb = pair % HB;
+  // causal: heaviest query blocks first; non-causal: the query blocks of one head
+  // are neighbours, so that head's K/V stay in L2 while they run
+  const int qb = causal ? (n_blocks_q - 1 - pair / HB) : (pair % n_blocks_q);
+  const int hb = causal ? pair % HB : pair / n_blocks_q;
   const int hq = hb % Hq, b = hb / Hq;
   const int hk = hq / (Hq / Hkv);
   // this sequence's query rows and keys (fixed-length or packed varlen batch)
@@ -613,8 +615,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(SliceCfg::kThreads, 
   const int HB = n_units_per_head_batch;
   const int n_blocks_q = (Sq_max + 2 * kPrefillTileM - 1) / (2 * kPrefillTileM);
   const int pair = blockIdx.x >> 1;
-  const int qb = causal ? (n_blocks_q - 1 - pair / HB) : (pair / HB);
-  const int hb = pair % HB;
+  // causal: heaviest query blocks first; non-causal: the query blocks of one head
+  // are neighbours, so that head's K/V stay in L2 while they run
+  const int qb = causal ? (n_blocks_q - 1 - pair / HB) : (pair % n_blocks_q);
+  const int hb = causal ? pair % HB : pair / n_blocks_q;
   const int hq = hb % Hq, b = hb / Hq;
   const int hk = hq / (Hq / Hkv);
   // this sequence's query rows and keys (fixed-length or packed varlen batch)
