@@ -43,6 +43,9 @@ struct PrefillArgs {
   // sequence with L keys covers [s*chunk, min(L, (s+1)*chunk)),
   // chunk = max(ceil(L / n_splits), split_min)
   int n_splits, split_min;
+  // one query position per sequence with its G <= 128 rows in the first query tile:
+  // the second tile takes the second half of the keys (merged in the epilogue)
+  int halves;
   float* part_o;
   float* part_lse;
 };

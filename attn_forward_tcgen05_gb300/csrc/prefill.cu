@@ -96,7 +96,10 @@ struct PrefillCfg {
   // P[NQ][NS], O[NQ], Fin[NQ].  S and P have one barrier per S buffer, so each
   // is at most one phase ahead of the warp that waits on it.
   static constexpr int kNumBars = 1 + 2 * kStagesK + 2 * kStagesV + 2 * NQ * NS + 2 * NQ;
-  static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;
+  // merge of the two key halves of a decode unit: per row (m, l, l_rnd, ok), fp32
+  static constexpr int kMergeOff = kBarOff + kNumBars * 8 + 16;
+  static constexpr int kMergeBytes = 128 * 4 * 4;
+  static constexpr int kSmemBytes = kMergeOff + kMergeBytes + 1024;
   // NQ softmax warpgroups + one control warpgroup (MMA warp, TMA warp, two spare warps).
   static constexpr int kThreads = (4 * NQ + 4) * 32;
   static constexpr int kMmaWarp = 4 * NQ;
@@ -159,7 +162,10 @@ __device__ __forceinline__ TileInfo tile_info(int q0, int Sr, int Sq, int G, int
 // WIN: causal sliding window with attention sinks (window, n_sink); without it
 // both are ignored and the tile list is every KV tile.  SPLIT: key splits with
 // decode partials (n_splits, split_min, part_o, part_lse); without it they are ignored.
-template <int D, bool WIN, bool SPLIT>
+// HALVES (one query position per sequence, its G <= 128 head rows in one tile):
+// both query tiles hold the same rows and take the two halves of the unit's keys,
+// so their S -> softmax -> P.V chains overlap; the halves merge in the epilogue.
+template <int D, bool WIN, bool SPLIT, bool HALVES>
 __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
     fmha_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -172,6 +178,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
   using C = PrefillCfg<D>;
   constexpr int NQ = C::NQ, NS = C::NS, BN = C::BN;
   static_assert(C::kSub == 1, "a KV stage is one tile (the sliding-window tile list maps tiles, not stages)");
+  static_assert(!HALVES || (NQ == 2 && NS == 1 && !WIN && !SPLIT), "key halves: two query tiles, plain keys");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // ---- work unit: longest causal work first ----
@@ -240,6 +247,23 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
 #pragma unroll
   for (int t = 0; t < NQ; ++t) ti[t].n_kv = klo < khi ? tile_list_len(tl, ti[t].n_kv) : 0;
   n_kv = klo < khi ? tile_list_len(tl, n_kv) : 0;
+  // key halves: tile 0 takes key tiles [0, n0), tile 1 (the same rows) [n0, n);
+  // the K/V rings run over items i = (step i / 2, tile i % 2)
+  int n_items = n_kv, n0 = n_kv;
+  if constexpr (HALVES) {
+    const int n = ti[0].n_kv;
+    n0 = (n + 1) / 2;
+    ti[1] = ti[0];
+    ti[1].n_kv = n - n0;
+    ti[0].n_kv = n0;
+    n_kv = n0;
+    n_items = n;
+  }
+  // key tile of ring item i (the TMA order) and of list entry j of query tile t
+  auto item_key = [&](int i) -> int {
+    if constexpr (HALVES) return (i & 1) ? n0 + (i >> 1) : (i >> 1);
+    return tile_list_key(tl, i);
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
@@ -299,7 +323,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
       // Stages of kSub KV tiles.  The MMA warp takes the K stage of tile j+1
       // before the V stage of tile j, so K stage uk goes out before V stage uv
       // while uk*kSub - 1 <= uv*kSub.
-      const int n_st = (n_kv + C::kSub - 1) / C::kSub;
+      const int n_st = (n_items + C::kSub - 1) / C::kSub;
       int jk = 0, jv = 0;  // next K / V stage
       bool aborted = false;
       while (jv < n_st) {
@@ -311,7 +335,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
 #pragma unroll
           for (int p = 0; p < C::kPanels; ++p)
             tma_load_4d_e(sK + s * C::kKVStageBytes + p * C::kKVPanelBytes, &tm_k, &bar_fullK[s], p * 64,
-                          hk, tile_list_key(tl, jk) * C::kStageRows, b);
+                          hk, item_key(jk) * C::kStageRows, b);
           ++jk;
           continue;
         }
@@ -322,7 +346,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
 #pragma unroll
         for (int p = 0; p < C::kPanels; ++p)
           tma_load_4d_e(sV + s * C::kKVStageBytes + p * C::kKVPanelBytes, &tm_v, &bar_fullV[s], p * 64,
-                        hk, tile_list_key(tl, jv) * C::kStageRows, b);
+                        hk, item_key(jv) * C::kStageRows, b);
         ++jv;
       }
       if (aborted) {
@@ -356,8 +380,9 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
       tc_fence_after();
 
       // S_t(j) = Q_t K_j^T into S buffer j % NS of tile t
-      auto issue_s = [&](int t, int j) {
-        const uint64_t dk = kv_tile_desc(dk0, j, C::kStagesK);
+      // g: ring position of the K / V tile (= j except with key halves)
+      auto issue_s = [&](int t, int j, int g) {
+        const uint64_t dk = kv_tile_desc(dk0, g, C::kStagesK);
         const uint32_t d_tmem = tmem + C::s_col(t, j % NS);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -370,11 +395,11 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
       };
       // O_t += P_t(j) V_j, P read from TMEM over S buffer j % NS; tile j is the
       // (j / NS)-th use of that buffer
-      auto issue_pv = [&](int t, int j) -> bool {
+      auto issue_pv = [&](int t, int j, int g) -> bool {
         const int buf = j % NS;
         if (!mbar_wait_warp(&bar_P[t * NS + buf], (uint32_t)(j / NS) & 1u, err, abort_flag)) return false;
         tc_fence_after();
-        const uint64_t dv = kv_tile_desc(dv0, j, C::kStagesV);
+        const uint64_t dv = kv_tile_desc(dv0, g, C::kStagesV);
         const uint32_t p_tmem = tmem + C::s_col(t, buf);
         const uint32_t d_tmem = tmem + C::o_col(t);
 #pragma unroll
@@ -386,6 +411,47 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
         return true;
       };
 
+      if constexpr (HALVES) {
+        // ring items in order (step 0, tile 0), (step 0, tile 1), (step 1, tile 0), ...:
+        // S of both tiles' first items, then per step and tile P.V of the item and
+        // S of the tile's next item -- the order the TMA producer loads them in
+        int ik = 0, iv = 0;  // next K / V item
+#pragma unroll
+        for (int t = 0; t < NQ; ++t) {
+          if (ok && ti[t].n_kv > 0) {
+            ok = mbar_wait_warp(&bar_fullK[ik % C::kStagesK], (uint32_t)(ik / C::kStagesK) & 1u, err, abort_flag);
+            tc_fence_after();
+            if (ok) {
+              issue_s(t, 0, ik);
+              mma_commit_e(&bar_emptyK[ik % C::kStagesK]);
+              ++ik;
+            }
+          }
+        }
+        for (int j = 0; ok && j < n_kv; ++j) {
+#pragma unroll
+          for (int t = 0; t < NQ; ++t) {
+            if (ok && j < ti[t].n_kv) {
+              ok = mbar_wait_warp(&bar_fullV[iv % C::kStagesV], (uint32_t)(iv / C::kStagesV) & 1u, err, abort_flag);
+              tc_fence_after();
+              if (ok) ok = issue_pv(t, j, iv);
+              if (ok) {
+                mma_commit_e(&bar_emptyV[iv % C::kStagesV]);
+                ++iv;
+              }
+            }
+            if (ok && j + 1 < ti[t].n_kv) {
+              ok = mbar_wait_warp(&bar_fullK[ik % C::kStagesK], (uint32_t)(ik / C::kStagesK) & 1u, err, abort_flag);
+              tc_fence_after();
+              if (ok) {
+                issue_s(t, j + 1, ik);
+                mma_commit_e(&bar_emptyK[ik % C::kStagesK]);
+                ++ik;
+              }
+            }
+          }
+        }
+      } else {
       if (ok) {
         // prologue: S of the first KV tile
         ok = mbar_wait_warp(&bar_fullK[0], 0, err, abort_flag);
@@ -393,7 +459,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
         if (ok) {
 #pragma unroll
           for (int t = 0; t < NQ; ++t)
-            if (ti[t].n_kv > 0) issue_s(t, 0);
+            if (ti[t].n_kv > 0) issue_s(t, 0, 0);
           if (C::kSub == 1 || n_kv == 1) mma_commit_e(&bar_emptyK[0]);
         }
       }
@@ -414,14 +480,14 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
           bool k_ready = false;
 #pragma unroll
           for (int t = 0; t < NQ; ++t) {
-            if (ok && j < ti[t].n_kv) ok = issue_pv(t, j);
+            if (ok && j < ti[t].n_kv) ok = issue_pv(t, j, j);
             if (ok && jn < ti[t].n_kv) {
               if (!k_ready && first_of_stage(jn)) {
                 ok = mbar_wait_warp(&bar_fullK[sn], (uint32_t)(un / C::kStagesK) & 1u, err, abort_flag);
                 tc_fence_after();
               }
               k_ready = true;
-              if (ok) issue_s(t, jn);
+              if (ok) issue_s(t, jn, jn);
             }
           }
           if (!ok) break;
@@ -438,7 +504,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
           }
 #pragma unroll
           for (int t = 0; t < NQ; ++t)
-            if (jn < ti[t].n_kv) issue_s(t, jn);
+            if (jn < ti[t].n_kv) issue_s(t, jn, jn);
           if (last_of_stage(jn)) mma_commit_e(&bar_emptyK[sn]);
         }
         const int u = j / C::kSub, s = u % C::kStagesV;
@@ -448,11 +514,12 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
         }
 #pragma unroll
         for (int t = 0; t < NQ; ++t) {
-          if (ok && j < ti[t].n_kv) ok = issue_pv(t, j);
+          if (ok && j < ti[t].n_kv) ok = issue_pv(t, j, j);
         }
         if (!ok) break;
         if (last_of_stage(j)) mma_commit_e(&bar_emptyV[s]);
       }
+      }  // HALVES
     }
   }
   } else {
@@ -498,7 +565,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
       tmem_wait_ld();
       // mask: keys at or past row_bound (causal bound or Skv), and with a window the
       // keys below the row's window that are not sinks
-      const int key0 = tile_list_key(tl, j) * BN;
+      const int key0 = (HALVES ? (t == 1 ? n0 + j : j) : tile_list_key(tl, j)) * BN;
       if (key0 + BN > my.kv_lo || (SPLIT && key0 < klo)) {
         const int lim = row_bound - key0, low = klo - key0;  // and keys below the split
 #pragma unroll
@@ -588,6 +655,36 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bar_Fin[t], 0, err, abort_flag))) ok = false;
       tc_fence_after();
     }
+    // key halves: tile 1 hands its rows' (m, l, l_rnd) to tile 0, which merges the
+    // two halves (O = f0 O_0 + f1 O_1 against the larger max) and writes the rows
+    float f0 = 1.f, f1 = 0.f;
+    bool have1 = false;  // warp-uniform: tile 1 held keys
+    if constexpr (HALVES) {
+      float* mg = reinterpret_cast<float*>(smem + C::kMergeOff) + r * 4;
+      if (t == 1) {
+        mg[0] = m_used;
+        mg[1] = l;
+        mg[2] = l_rnd;
+        mg[3] = ok ? 1.f : 0.f;
+        named_bar_arrive(3, 256);  // always, so tile 0 never waits for a failed tile 1
+      } else {
+        named_bar_sync(3, 256);
+        const float m1 = mg[0], l1 = mg[1], lr1 = mg[2];
+        ok = ok && mg[3] != 0.f;
+        have1 = ti[1].n_kv > 0;
+        if (ok && have1) {  // O_1 complete: its last P.V is done
+          if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bar_Fin[1], 0, err, abort_flag))) ok = false;
+          tc_fence_after();
+        }
+        const float m = fmaxf(m_used, m1);
+        f0 = (m_used == -INFINITY) ? 0.f : ex2_approx(m_used - m);
+        f1 = (m1 == -INFINITY) ? 0.f : ex2_approx(m1 - m);
+        l = l * f0 + l1 * f1;
+        l_rnd = l_rnd * f0 + lr1 * f1;
+        m_used = m;
+      }
+    }
+    if (!(HALVES && t == 1)) {
     // warp-uniform: tcgen05.ld below is a warp-collective instruction
     const bool load_o = ok && my.n_kv > 0;
     const bool have = load_o && l > 0.f;  // per row: at least one admissible key
@@ -601,6 +698,25 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
     const size_t orow = partial ? prow
                                 : ((size_t)ext.bq * ext.rows + ext.qbase + (size_t)(row_ok ? qpos : 0)) * Hq + hq;
     void* const out = partial ? static_cast<void*>(part_o) : o_ptr;
+    // 32 columns of this row's O (merged over the key halves), or zeros
+    const uint32_t o_addr1 = lane_addr + C::o_col(NQ - 1);
+    auto load_o32 = [&](int c0, uint32_t* ov) {
+      if (load_o) {
+        tmem_ld32(o_addr + c0, ov);
+        tmem_wait_ld();
+        if (HALVES && have1) {
+          uint32_t o1[32];
+          tmem_ld32(o_addr1 + c0, o1);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            ov[e] = __float_as_uint(fmaf(__uint_as_float(ov[e]), f0, __uint_as_float(o1[e]) * f1));
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) ov[e] = 0u;
+      }
+    };
     if (!SPLIT && o_tma) {
       // bf16 O through shared memory: every S MMA of this tile has completed (its
       // last P.V has), so the tile's Q buffer takes O in the same 128-byte-swizzled
@@ -609,13 +725,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t ov[32];
-        if (load_o) {
-          tmem_ld32(o_addr + c0, ov);
-          tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) ov[e] = 0u;
-        }
+        load_o32(c0, ov);
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
           uint4 w;
@@ -642,13 +752,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t ov[32];
-        if (load_o) {
-          tmem_ld32(o_addr + c0, ov);
-          tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) ov[e] = 0u;
-        }
+        load_o32(c0, ov);
         if (row_ok && ok) {
           if (o_bf16 && !partial) {
             uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(o_ptr) + orow * D + c0);
@@ -677,6 +781,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
       if (partial) part_lse[prow] = lse_v;
       else lse_ptr[((size_t)ext.bq * Hq + hq) * ext.rows + ext.qbase + qpos] = lse_v;
     }
+    }  // rows written by this warpgroup
   }
 
   // ---- teardown: every role has finished with TMEM ----
@@ -703,8 +808,10 @@ template <int D>
 cudaError_t launch_prefill_t(const PrefillArgs& a, cudaStream_t stream) {
   using C = PrefillCfg<D>;
   const bool split = a.n_splits > 1;
-  auto kern = a.window > 0 ? fmha_fwd_kernel<D, true, false>
-                           : (split ? fmha_fwd_kernel<D, false, true> : fmha_fwd_kernel<D, false, false>);
+  auto kern = a.window > 0 ? fmha_fwd_kernel<D, true, false, false>
+              : split      ? fmha_fwd_kernel<D, false, true, false>
+              : a.halves   ? fmha_fwd_kernel<D, false, false, true>
+                           : fmha_fwd_kernel<D, false, false, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int G = a.pack;

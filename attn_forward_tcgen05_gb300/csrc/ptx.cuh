@@ -171,6 +171,15 @@ __device__ __forceinline__ void tma_store_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// Named barrier `id` over `count` threads: arrive without waiting / arrive and wait.
+// Memory written before the arrive is visible to the threads after their sync.
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // Named barrier over `count` threads that also returns the AND of `pred` over them.
 __device__ __forceinline__ bool bar_sync_and(uint32_t id, uint32_t count, bool pred) {
   uint32_t r;

@@ -59,7 +59,9 @@ def test_packed_prefill_bf16_output(out_dtype):
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("Hq,Hkv", [(128, 1), (64, 2), (32, 1), (16, 2), (8, 1)])
 def test_packed_decode(d, Hq, Hkv):
-    lens = torch.tensor([0, 1, 29, 128, 129, 1000, 2500, 77], dtype=torch.int32)
+    # one KV tile (the second key half empty), two, odd counts (unequal halves),
+    # ragged tails, an empty sequence
+    lens = torch.tensor([0, 1, 29, 128, 129, 300, 640, 1000, 2500, 77], dtype=torch.int32)
     q, kc, vc = W.decode_inputs(len(lens), Hq, Hkv, d, lens, 600 + d + Hq)
     scale = 1.0 / np.sqrt(d)
     o, lse = decode_packed(q.cuda(), kc.cuda(), vc.cuda(), lens.cuda(), scale, out_dtype=torch.float32)
