@@ -194,6 +194,10 @@ static int varlen_impl(const attn_bf16_t* q, const attn_bf16_t* kcache, const at
                 : encode_bf16_q5d(&a.tm_q, q, d, 1, Hq, total_q, 1);
   if (rc == ATTN_OK) rc = encode_bf16_4d(&a.tm_k, kcache, d, Hkv, max_kv, B, attn::prefill_k_box_rows(d));
   if (rc == ATTN_OK) rc = encode_bf16_4d(&a.tm_v, vcache, d, Hkv, max_kv, B, attn::kPrefillKVStageRows);
+  // bf16 O of whole tiles leaves through TMA stores (the kernel keeps per-row stores
+  // for a sequence's last, partial tile)
+  a.o_tma = (!pair && o_dtype == ATTN_BF16) ? 1 : 0;
+  if (rc == ATTN_OK && a.o_tma) rc = encode_bf16_q5d(&a.tm_o, o, d, 1, Hq, total_q, 1);
   if (rc != ATTN_OK) return rc;
   return from_cuda(pair ? attn::launch_prefill_pair(a, s) : attn::launch_prefill(a, s));
 }

@@ -59,7 +59,9 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when m grows by > 2^8
 
-template <int D>
+// H: the key-halves layout (both query tiles read one Q tile, the freed Q space
+// deepens the K ring for keys streamed from HBM)
+template <int D, bool H = false>
 struct PrefillCfg {
   static constexpr int NQ = (D <= 128) ? 2 : 1;            // query tiles per CTA
 #ifndef ATTN_PREFILL_NS
@@ -79,7 +81,7 @@ struct PrefillCfg {
   static constexpr int kQTileBytes = kPanels * kQPanelBytes;
   static constexpr int kKVStageBytes = kPanels * kKVPanelBytes;
 #ifndef ATTN_PREFILL_KSTAGES
-  static constexpr int kStagesK = (D == 64) ? 4 : (D == 128 ? 2 : 1);  // K ring depth
+  static constexpr int kStagesK = (D == 64) ? (H ? 5 : 4) : (D == 128 ? (H ? 3 : 2) : 1);  // K ring depth
 #else
   static constexpr int kStagesK = ATTN_PREFILL_KSTAGES;
 #endif
@@ -88,8 +90,12 @@ struct PrefillCfg {
 #else
   static constexpr int kStagesV = ATTN_PREFILL_VSTAGES;
 #endif
+  static constexpr int kQTiles = H ? 1 : NQ;               // Q tiles in shared memory
+  // K tiles the producer may issue ahead of V: the MMA warp needs K of the next
+  // tile (item) before V of the current one; key halves stream from HBM and run further
+  static constexpr int kLookK = H ? 2 : 1;
   static constexpr int kQOff = 0;
-  static constexpr int kKOff = NQ * kQTileBytes;
+  static constexpr int kKOff = kQTiles * kQTileBytes;
   static constexpr int kVOff = kKOff + kStagesK * kKVStageBytes;
   static constexpr int kBarOff = kVOff + kStagesV * kKVStageBytes;
   // barriers: fullQ, fullK[SK], emptyK[SK], fullV[SV], emptyV[SV], S[NQ][NS],
@@ -166,7 +172,7 @@ __device__ __forceinline__ TileInfo tile_info(int q0, int Sr, int Sq, int G, int
 // both query tiles hold the same rows and take the two halves of the unit's keys,
 // so their S -> softmax -> P.V chains overlap; the halves merge in the epilogue.
 template <int D, bool WIN, bool SPLIT, bool HALVES>
-__global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
+__global__ void __launch_bounds__(PrefillCfg<D, HALVES>::kThreads, 1)
     fmha_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                     int o_tma, void* __restrict__ o_ptr,
@@ -175,7 +181,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
                     const int* __restrict__ cu_q, const int* __restrict__ kv_lens, int total_q,
                     int window, int n_sink, int pack, int n_splits, int split_min,
                     float* __restrict__ part_o, float* __restrict__ part_lse) {
-  using C = PrefillCfg<D>;
+  using C = PrefillCfg<D, HALVES>;
   constexpr int NQ = C::NQ, NS = C::NS, BN = C::BN;
   static_assert(C::kSub == 1, "a KV stage is one tile (the sliding-window tile list maps tiles, not stages)");
   static_assert(!HALVES || (NQ == 2 && NS == 1 && !WIN && !SPLIT), "key halves: two query tiles, plain keys");
@@ -308,11 +314,11 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
       }
       uint32_t qbytes = 0;
 #pragma unroll
-      for (int t = 0; t < NQ; ++t)
+      for (int t = 0; t < C::kQTiles; ++t)
         if (ti[t].n_kv > 0) qbytes += C::kQTileBytes;
       mbar_arrive_expect_tx_e(bar_q, qbytes);
 #pragma unroll
-      for (int t = 0; t < NQ; ++t) {
+      for (int t = 0; t < C::kQTiles; ++t) {
         if (ti[t].n_kv > 0) {
 #pragma unroll
           for (int p = 0; p < C::kPanels; ++p)
@@ -327,7 +333,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
       int jk = 0, jv = 0;  // next K / V stage
       bool aborted = false;
       while (jv < n_st) {
-        if (jk < n_st && jk * C::kSub <= jv * C::kSub + 1) {
+        if (jk < n_st && jk * C::kSub <= jv * C::kSub + C::kLookK) {
           const int s = jk % C::kStagesK;
           const uint32_t ph = (uint32_t)(jk / C::kStagesK) & 1u;
           if (!mbar_wait_warp(&bar_emptyK[s], ph ^ 1u, err, abort_flag)) { aborted = true; break; }
@@ -372,7 +378,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
       uint64_t dq[NQ];
 #pragma unroll
       for (int t = 0; t < NQ; ++t)
-        dq[t] = smem_desc(smem_u32(sQ + t * C::kQTileBytes), 16, 1024, kSwizzle128B);
+        dq[t] = smem_desc(smem_u32(sQ + (t < C::kQTiles ? t : 0) * C::kQTileBytes), 16, 1024, kSwizzle128B);
       const uint64_t dk0 = smem_desc(smem_u32(sK), 16, 1024, kSwizzle128B);
       // V as the MN-major B operand: consecutive 64-column panels are kKVPanelBytes apart
       const uint64_t dv0 = smem_desc(smem_u32(sV), C::kKVPanelBytes, 1024, kSwizzle128B);
@@ -717,7 +723,10 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
         for (int e = 0; e < 32; ++e) ov[e] = 0u;
       }
     };
-    if (!SPLIT && o_tma) {
+    // (a packed varlen tile that runs past its sequence's rows would overwrite the
+    // next sequence's: it keeps the per-row stores; the choice is per tile, so the
+    // whole warpgroup takes the same branch)
+    if (!SPLIT && o_tma && (cu_q == nullptr || my.q0 + kPrefillTileM <= Sr)) {
       // bf16 O through shared memory: every S MMA of this tile has completed (its
       // last P.V has), so the tile's Q buffer takes O in the same 128-byte-swizzled
       // layout and one TMA store per panel writes it (rows past Sq are clipped)
@@ -804,13 +813,13 @@ __global__ void fill_empty_kernel(void* o, float* lse, size_t n_o, size_t n_lse,
     lse[i] = -INFINITY;
 }
 
-template <int D>
+template <int D, bool H>
 cudaError_t launch_prefill_t(const PrefillArgs& a, cudaStream_t stream) {
-  using C = PrefillCfg<D>;
+  using C = PrefillCfg<D, H>;
   const bool split = a.n_splits > 1;
-  auto kern = a.window > 0 ? fmha_fwd_kernel<D, true, false, false>
+  auto kern = H            ? fmha_fwd_kernel<D, false, false, true>
+              : a.window > 0 ? fmha_fwd_kernel<D, true, false, false>
               : split      ? fmha_fwd_kernel<D, false, true, false>
-              : a.halves   ? fmha_fwd_kernel<D, false, false, true>
                            : fmha_fwd_kernel<D, false, false, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -832,8 +841,8 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, cudaStream_t stream) {
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   switch (a.d) {
-    case 64: return launch_prefill_t<64>(a, stream);
-    case 128: return launch_prefill_t<128>(a, stream);
+    case 64: return a.halves ? launch_prefill_t<64, true>(a, stream) : launch_prefill_t<64, false>(a, stream);
+    case 128: return a.halves ? launch_prefill_t<128, true>(a, stream) : launch_prefill_t<128, false>(a, stream);
     default: return cudaErrorInvalidValue;
   }
 }
