@@ -107,6 +107,18 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------- ours
+def max_over_ranks(values, world):
+    """Element-wise maximum of per-rank timings over all ranks (the slowest replica
+    sets the job's time); the identity with one process."""
+    if world <= 1:
+        return [float(x) for x in values]
+    import torch
+    import torch.distributed as dist
+    tt = torch.tensor([float(x) for x in values], dtype=torch.float64)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return [float(x) for x in tt]
+
+
 def run_line(args):
     """One extra workload line alone (--line), for profiling its kernel."""
     import torch
@@ -221,13 +233,8 @@ def run_ours(args, rank, world, local_rank):
     ms_step = t_prefill + t_split3 + t_merge3 + t_split5 + t_merge5
     wall_ms = t_start.elapsed_time(t_end)
 
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([ms_step, t_prefill, t_split5 + t_merge5, wall_ms], dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_step, t_prefill_max, t_dec5_max, wall_ms = [float(x) for x in tt]
-    else:
-        t_prefill_max, t_dec5_max = t_prefill, t_split5 + t_merge5
+    ms_step, t_prefill_max, t_dec5_max, wall_ms = max_over_ranks(
+        [ms_step, t_prefill, t_split5 + t_merge5, wall_ms], world)
 
     # ---- packed variable-length prefill (chunked prefill against a KV cache) ----
     varlen = None if args.only else time_varlen(args, attn, W, dev, stream, flush, peaks, peak_src)
