@@ -357,6 +357,7 @@ def time_varlen(args, attn, W, dev, stream, flush, peaks, peak_src):
             "us": round(ms * 1e3, 2), "value": round(tf, 2), "unit": "TFLOP/s", "steps": n,
             "roofline": {"bound": "tensor", "kernel": "fmha_fwd_kernel<128>", "achieved": round(tf, 2),
                          "peak": peak_tc, "unit": "TFLOP/s", "frac": round(tf / peak_tc, 4),
+                         "traffic": load_traffic().get(f"fmha_fwd_kernel<128> varlen {V.name}"),
                          "peak_source": f"bf16_tflops (burst) of {peak_src}"}}
 
 
