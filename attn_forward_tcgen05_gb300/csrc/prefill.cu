@@ -180,7 +180,8 @@ __global__ void __launch_bounds__(PrefillCfg<D, HALVES>::kThreads, 1)
                     int o_bf16, float scale, int n_units_per_head_batch, uint32_t* err,
                     const int* __restrict__ cu_q, const int* __restrict__ kv_lens, int total_q,
                     int window, int n_sink, int pack, int n_splits, int split_min,
-                    float* __restrict__ part_o, float* __restrict__ part_lse) {
+                    float* __restrict__ part_o, float* __restrict__ part_lse, int unit0,
+                    int row_halves) {
   using C = PrefillCfg<D, HALVES>;
   constexpr int NQ = C::NQ, NS = C::NS, BN = C::BN;
   static_assert(C::kSub == 1, "a KV stage is one tile (the sliding-window tile list maps tiles, not stages)");
@@ -196,7 +197,10 @@ __global__ void __launch_bounds__(PrefillCfg<D, HALVES>::kThreads, 1)
   const int n_blocks_q = (Sq_max * G + NQ * kPrefillTileM - 1) / (NQ * kPrefillTileM);
   // key splits (one-token decode only): unit = (query block, split, head group, batch)
   const int NSPL = SPLIT ? n_splits : 1;
-  const int u = blockIdx.x;
+  // CTA -> unit: this launch covers units [unit0, ...); with row halves (key-halves
+  // kernel) CTA pairs share a unit, each taking 128 rows of its query block
+  const int u = unit0 + ((HALVES && row_halves) ? (int)(blockIdx.x >> 1) : (int)blockIdx.x);
+  const int rh = (HALVES && row_halves) ? (int)(blockIdx.x & 1) : 0;
   // causal: heaviest query blocks first; non-causal: the query blocks of one head
   // are neighbours, so that head's K/V stay in L2 while they run
   const int qb = causal ? (n_blocks_q - 1 - u / (HB * NSPL)) : (u % n_blocks_q);
@@ -240,7 +244,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, HALVES>::kThreads, 1)
   TileInfo ti[NQ];
 #pragma unroll
   for (int t = 0; t < NQ; ++t)
-    ti[t] = tile_info<BN>(qb * NQ * kPrefillTileM + t * kPrefillTileM, Sr, Sq, G, Skv, causal, khi);
+    ti[t] = tile_info<BN>(qb * NQ * kPrefillTileM + (t + rh) * kPrefillTileM, Sr, Sq, G, Skv, causal, khi);
   int n_kv = 0;
 #pragma unroll
   for (int t = 0; t < NQ; ++t) n_kv = max(n_kv, ti[t].n_kv);
@@ -813,36 +817,70 @@ __global__ void fill_empty_kernel(void* o, float* lse, size_t n_o, size_t n_lse,
     lse[i] = -INFINITY;
 }
 
+// SMs of the current device
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+// One launch of grid CTAs over units [unit0, ...) with configuration H.
 template <int D, bool H>
-cudaError_t launch_prefill_t(const PrefillArgs& a, cudaStream_t stream) {
+cudaError_t launch_prefill_grid(const PrefillArgs& a, cudaStream_t stream, long long unit0, long long grid,
+                                int row_halves) {
   using C = PrefillCfg<D, H>;
-  const bool split = a.n_splits > 1;
-  auto kern = H            ? fmha_fwd_kernel<D, false, false, true>
-              : a.window > 0 ? fmha_fwd_kernel<D, true, false, false>
-              : split      ? fmha_fwd_kernel<D, false, true, false>
-                           : fmha_fwd_kernel<D, false, false, false>;
+  auto kern = fmha_fwd_kernel<D, false, false, false>;
+  if constexpr (H) {
+    kern = fmha_fwd_kernel<D, false, false, true>;
+  } else {
+    if (a.window > 0) kern = fmha_fwd_kernel<D, true, false, false>;
+    else if (a.n_splits > 1) kern = fmha_fwd_kernel<D, false, true, false>;
+  }
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
+  if (grid <= 0) return cudaSuccess;
+  const int G = a.pack;
+  const int n_splits = a.n_splits > 1 ? a.n_splits : 1;
+  kern<<<(unsigned)grid, C::kThreads, C::kSmemBytes, stream>>>(
+      a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.o_tma, a.o, a.lse, a.Hq, a.Hkv, a.Sq, a.Skv, a.causal, a.o_bf16, a.scale,
+      (a.Hq / G) * a.B, a.err, a.cu_q, a.kv_lens, a.total_q, a.window, a.n_sink, G, n_splits,
+      a.split_min, a.part_o, a.part_lse, (int)unit0, row_halves);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_prefill_t(const PrefillArgs& a, cudaStream_t stream) {
+  using C = PrefillCfg<D, false>;
   const int G = a.pack;
   const long long rows = (long long)a.Sq * G;
   const long long n_blocks_q = (rows + C::NQ * kPrefillTileM - 1) / (C::NQ * kPrefillTileM);
   const int n_splits = a.n_splits > 1 ? a.n_splits : 1;
   const long long units = n_blocks_q * (a.Hq / G) * a.B * n_splits;
   if (units <= 0) return cudaSuccess;
-  if (units > 0x7FFFFFFFLL || rows > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-  kern<<<(unsigned)units, C::kThreads, C::kSmemBytes, stream>>>(
-      a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.o_tma, a.o, a.lse, a.Hq, a.Hkv, a.Sq, a.Skv, a.causal, a.o_bf16, a.scale,
-      (a.Hq / G) * a.B, a.err, a.cu_q, a.kv_lens, a.total_q, a.window, a.n_sink, G, n_splits,
-      a.split_min, a.part_o, a.part_lse);
-  return cudaGetLastError();
+  if (2 * units > 0x7FFFFFFFLL || rows > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+  if (a.halves) return launch_prefill_grid<D, true>(a, stream, 0, units, 0);
+  // A non-causal fixed-length launch whose last wave is at most half full: that
+  // wave's units run as two 128-row halves each, whose two query tiles take the
+  // two halves of the keys (the key-halves kernel), in about half a unit's time.
+  const bool plain = !a.causal && a.window == 0 && n_splits == 1 && a.cu_q == nullptr &&
+                     a.kv_lens == nullptr && G == 1;
+  const long long n_sm = sm_count();
+  const long long tail = n_sm > 0 ? units % n_sm : 0;
+  if (plain && units > n_sm && tail > 0 && 2 * tail <= n_sm) {
+    cudaError_t e = launch_prefill_grid<D, false>(a, stream, 0, units - tail, 0);
+    if (e != cudaSuccess) return e;
+    return launch_prefill_grid<D, true>(a, stream, units - tail, 2 * tail, 1);
+  }
+  return launch_prefill_grid<D, false>(a, stream, 0, units, 0);
 }
 
 }  // namespace
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   switch (a.d) {
-    case 64: return a.halves ? launch_prefill_t<64, true>(a, stream) : launch_prefill_t<64, false>(a, stream);
-    case 128: return a.halves ? launch_prefill_t<128, true>(a, stream) : launch_prefill_t<128, false>(a, stream);
+    case 64: return launch_prefill_t<64>(a, stream);
+    case 128: return launch_prefill_t<128>(a, stream);
     default: return cudaErrorInvalidValue;
   }
 }

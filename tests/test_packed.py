@@ -38,9 +38,15 @@ def test_packed_prefill(d, Hq, Hkv, Sq, Skv, causal):
     o2, lse2 = prefill(qd, kd, vd, causal=causal, scale=scale, out_dtype=torch.float32)
     sync_check()
     o, lse = o.cpu().numpy(), lse.cpu().numpy()
-    # the same rows, keys, masks and per-row arithmetic as the unpacked kernel
-    np.testing.assert_array_equal(o, o2.cpu().numpy())
-    np.testing.assert_array_equal(lse, lse2.cpu().numpy())
+    # the same rows, keys, masks and per-row arithmetic as the unpacked kernel --
+    # unless the unpacked launch ran its last wave as key halves (a non-causal
+    # launch over more units than SMs with a last wave at most half full)
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    units = -(-Sq // 256) * Hq * 2
+    halves_tail = (not causal) and units > n_sm and 0 < units % n_sm <= n_sm // 2
+    if not halves_tail:
+        np.testing.assert_array_equal(o, o2.cpu().numpy())
+        np.testing.assert_array_equal(lse, lse2.cpu().numpy())
     ro, rl = oracle.sdpa(q, k, v, causal, scale)
     check_o(o, ro, False)
     check_lse(lse, rl)

@@ -122,3 +122,35 @@ def test_many_heads_long_kv_d256():
     shape = W.PrefillShape("d256_h148_kv8192", 1, 148, 148, 128, 8192, 256, False,
                            1.0 / 16.0, "bf16", 77)
     _full_size(shape, torch.bfloat16, n_random=16)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_noncausal_last_wave_as_key_halves(d):
+    """A non-causal launch whose last wave is at most half full runs that wave's
+    units as 128-row halves whose two query tiles take the two key halves (merged
+    in the epilogue).  The shape is chosen from the SM count so that the launch
+    has a few more units than SMs; rows of the last units (the last head's upper
+    query blocks, on both sides of each 128-row split) and of the first wave are
+    compared with the oracle."""
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    S = 4096
+    H = n_sm // 16 + 1                     # 16 query blocks per head: 16*H units
+    units = 16 * H
+    assert units > n_sm and 0 < units % n_sm <= n_sm // 2
+    q, k, v = W.prefill_inputs(1, H, H, S, S, d, 90 + d)
+    scale = 1.0 / math.sqrt(d)
+    for out_dtype in (torch.float32, torch.bfloat16):
+        o, lse = prefill(q.cuda(), k.cuda(), v.cuda(), causal=False, scale=scale, out_dtype=out_dtype)
+        torch.cuda.synchronize()
+        sync_check()
+        last = H - 1
+        first_tail_block = 16 - units % n_sm  # query blocks of the last head run as halves from here
+        r0 = first_tail_block * 256
+        picks = sorted({0, 1, 127, 128, r0 - 1, r0, r0 + 1, r0 + 127, r0 + 128, r0 + 129, r0 + 255,
+                        r0 + 256, 3000, S - 129, S - 128, S - 2, S - 1} & set(range(S)))
+        rows = [(0, last, i) for i in picks] + [(0, 0, 0), (0, 0, S - 1), (0, H // 2, 2100)]
+        ro, rl = oracle.sdpa_rows(q, k, v, False, scale, rows)
+        got_o = np.stack([o[0, i, h].float().cpu().numpy() for _, h, i in rows])
+        got_l = np.array([lse[0, h, i].item() for _, h, i in rows])
+        check_o(got_o, ro, out_dtype == torch.bfloat16, f"O {out_dtype}")
+        check_lse(got_l, rl, f"LSE {out_dtype}")
