@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, HALVES>::kThreads, 1)
   static_assert(!HALVES || (NQ == 2 && NS == 1 && !WIN && !SPLIT), "key halves: two query tiles, plain keys");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // ---- work unit: longest causal work first ----
+  // ---- work unit ----
   // A unit is NQ query tiles of one head group: G = pack query heads (of one KV
   // head) folded into the tile rows, row r = (position r / G, head r % G).
   const int G = pack;
@@ -330,9 +330,10 @@ __global__ void __launch_bounds__(PrefillCfg<D, HALVES>::kThreads, 1)
                           ext.qbase + ti[t].q0 / G, ext.bq);
         }
       }
-      // Stages of kSub KV tiles.  The MMA warp takes the K stage of tile j+1
-      // before the V stage of tile j, so K stage uk goes out before V stage uv
-      // while uk*kSub - 1 <= uv*kSub.
+      // Stages of kSub KV tiles (ring items with key halves).  The MMA warp takes
+      // K of tile (item) j+1 before V of tile j, so K stage uk goes out before V
+      // stage uv while uk*kSub <= uv*kSub + kLookK (kLookK = 1; 2 with key halves,
+      // whose deeper K ring streams from HBM).
       const int n_st = (n_items + C::kSub - 1) / C::kSub;
       int jk = 0, jv = 0;  // next K / V stage
       bool aborted = false;
