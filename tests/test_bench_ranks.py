@@ -66,3 +66,21 @@ def test_gpus_flag_without_launcher_is_an_error():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--steps", "1",
                         "--warmup", "3"], env=env, capture_output=True, text=True, timeout=300)
     assert r.returncode != 0 and "torchrun" in (r.stderr + r.stdout)
+
+
+def test_reference_arm_line_has_the_contract_keys(monkeypatch):
+    """The reference arm (the fp64 oracle on the host cores) prints the bench
+    contract's line: metric, unit, a positive value, the CPU baseline it measured
+    and an e2e entry without host-device copies."""
+    import argparse
+    sys.path.insert(0, ROOT)
+    import bench
+    monkeypatch.setattr(bench, "REFERENCE_BUDGET_S", 1.0)
+    line = bench.run_reference(argparse.Namespace(steps=2, warmup=3), 0, 1)
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "higher_is_better", "scaling",
+                "vs_baseline", "dtype", "data", "config", "impl", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "TFLOP/s"
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    assert bench.run_reference(argparse.Namespace(steps=2, warmup=3), 1, 2) is None  # other ranks: no work
