@@ -125,7 +125,8 @@ def test_many_heads_long_kv_d256():
 
 
 @pytest.mark.parametrize("d", [64, 128])
-def test_noncausal_last_wave_as_key_halves(d):
+@pytest.mark.parametrize("Sq,Skv", [(4096, 4096), (4000, 1400), (4096, 100)], ids=["4096", "4000x1400", "4096x100"])
+def test_noncausal_last_wave_as_key_halves(d, Sq, Skv):
     """A non-causal launch whose last wave is at most half full runs that wave's
     units as 128-row halves whose two query tiles take the two key halves (merged
     in the epilogue).  The shape is chosen from the SM count so that the launch
@@ -133,11 +134,14 @@ def test_noncausal_last_wave_as_key_halves(d):
     query blocks, on both sides of each 128-row split) and of the first wave are
     compared with the oracle."""
     n_sm = torch.cuda.get_device_properties(0).multi_processor_count
-    S = 4096
+    S = Sq
     H = n_sm // 16 + 1                     # 16 query blocks per head: 16*H units
     units = 16 * H
-    assert units > n_sm and 0 < units % n_sm <= n_sm // 2
-    q, k, v = W.prefill_inputs(1, H, H, S, S, d, 90 + d)
+    assert -(-Sq // 256) == 16 and units > n_sm and 0 < units % n_sm <= n_sm // 2
+    # Sq = 4000: the last query block's second 128-row half is partial;
+    # Skv = 1400: 11 key tiles, halves of 6 and 5 ending in a partial tile;
+    # Skv = 100: one key tile, so the second half holds no keys
+    q, k, v = W.prefill_inputs(1, H, H, Sq, Skv, d, 90 + d if Skv == Sq else 90 + d + Skv)
     scale = 1.0 / math.sqrt(d)
     for out_dtype in (torch.float32, torch.bfloat16):
         o, lse = prefill(q.cuda(), k.cuda(), v.cuda(), causal=False, scale=scale, out_dtype=out_dtype)
