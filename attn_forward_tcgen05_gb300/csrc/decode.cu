@@ -29,7 +29,12 @@
 // an fp32 copy), scaled by scale * log2(e) once per score, warp-shuffle max,
 // exp2 on the MUFU, then P.V with lane = d/32 dims and each row's weights
 // broadcast from shared memory (a shuffle per row and head instead was about
-// 1.5x slower).  Both products run on packed fp32 pairs (fma.f32x2).  At the end the four warps' partial
+// 1.5x slower).  The score products take q and k as bf16 straight from shared
+// memory into a mixed-precision fma (bf16 x bf16 + fp32, exact products, one
+// rounding per step, the same result as fp32 fmas of the widened values); the
+// bf16 -> fp32 conversions this removes were most of the score loop's
+// instructions (0.73 -> 0.83 of the copy bandwidth on a ragged 64-sequence
+// batch).  P.V runs on packed fp32 pairs (fma.f32x2).  At the end the four warps' partial
 // (m, l, O) are merged through shared memory and the split's normalised O
 // and LSE are written.  Everything is fp32 on CUDA cores; no tensor cores.
 #include <cmath>
@@ -71,11 +76,6 @@ __device__ __forceinline__ float bf16lo(uint32_t x) { return __uint_as_float(x <
 __device__ __forceinline__ float bf16hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
 // two bf16 (low, high half of x) as an fp32 pair
 __device__ __forceinline__ uint64_t bf16x2_to_f2(uint32_t x) { return f2pack(bf16lo(x), bf16hi(x)); }
-__device__ __forceinline__ float f2sum(uint64_t a) {
-  float lo, hi;
-  f2unpack(a, lo, hi);
-  return lo + hi;
-}
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -87,6 +87,118 @@ __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
   return v;
+}
+
+// ---- launch order of the split units ----
+// Unit (b, s) holds clamp(L_b - s*chunk_b, 0, chunk_b) rows.  CTAs start in index
+// order and an SM takes the next one when a slot frees, so a ragged batch ends
+// soonest when the long units start first and the short ones fill the end (the
+// longest-first list-scheduling rule).  Every unit of a sequence but its last
+// non-empty one is full, so the order is: all full units, then the partial last
+// units by size (kOrderBuckets buckets of chunk / kOrderBuckets rows, largest
+// first, batch order within a bucket), then the empty units.  Each CTA derives
+// its unit from kv_lens with two warp-wide passes over the batch.  Batches above
+// kOrderMaxBatch take the batch-major order instead (the passes would cost more
+// than the tail they save).
+constexpr int kOrderBuckets = 16;
+constexpr int kOrderMaxBatch = 1024;
+
+struct SplitShape {
+  int nf;  // full units (chunk rows each)
+  int hp;  // 1 if a partial unit follows them
+  int bk;  // size bucket of the partial unit, or -1
+  int ne;  // empty units
+};
+
+// the split rule of the kernel: chunk = max(ceil(L / n_splits), min_rows, 1)
+__device__ __forceinline__ SplitShape split_shape(int L, int max_kv, int n_splits, int min_rows) {
+  L = L < 0 ? 0 : (L > max_kv ? max_kv : L);
+  int chunk = L / n_splits + (L % n_splits != 0 ? 1 : 0);
+  chunk = max(max(chunk, min_rows), 1);
+  SplitShape r;
+  r.nf = L / chunk;
+  const int rem = L - r.nf * chunk;
+  r.hp = rem > 0 ? 1 : 0;
+  r.bk = r.hp ? (int)((long long)rem * kOrderBuckets / chunk) : -1;
+  r.ne = n_splits - r.nf - r.hp;
+  return r;
+}
+
+__device__ __forceinline__ int warp_incl_scan(int v, int lane) {
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int x = __shfl_up_sync(0xFFFFFFFFu, v, off);
+    if (lane >= off) v += x;
+  }
+  return v;
+}
+
+// (b, s) of the unit at position p of the launch order, for every lane of the
+// calling warp; (-1, -1) if p is past the last unit.
+__device__ __noinline__ int2 unit_at(int p, const int* __restrict__ kv_lens, int B, int max_kv, int n_splits,
+                                      int min_rows, int lane) {
+  auto shape_of = [&](int b) {
+    return b < B ? split_shape(kv_lens[b], max_kv, n_splits, min_rows) : SplitShape{0, 0, -1, 0};
+  };
+  int F = 0, P = 0;  // full and partial units of the batch
+  for (int b0 = 0; b0 < B; b0 += 32) {
+    const SplitShape sh = shape_of(b0 + lane);
+    F += (int)__reduce_add_sync(0xFFFFFFFFu, (unsigned)sh.nf);
+    P += __popc(__ballot_sync(0xFFFFFFFFu, sh.hp != 0));
+  }
+  if (p < F || p >= F + P) {
+    // a full unit (the p-th, batch-major) or an empty one (the (p-F-P)-th)
+    const bool full = p < F;
+    const int q = full ? p : p - F - P;
+    int carry = 0;
+    for (int b0 = 0; b0 < B; b0 += 32) {
+      const SplitShape sh = shape_of(b0 + lane);
+      const int n = full ? sh.nf : sh.ne;
+      const int incl = warp_incl_scan(n, lane) + carry, excl = incl - n;
+      const unsigned hit = __ballot_sync(0xFFFFFFFFu, excl <= q && q < incl);
+      if (hit) {
+        const int src = __ffs(hit) - 1;
+        const int first = full ? 0 : sh.nf + sh.hp;  // first unit of the class in the sequence
+        const int s = __shfl_sync(0xFFFFFFFFu, first + q - excl, src);
+        return make_int2(b0 + src, s);
+      }
+      carry = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    }
+    return make_int2(-1, -1);
+  }
+  // a partial unit: count the buckets (lane k < kOrderBuckets holds bucket k)
+  int cnt = 0;
+  for (int b0 = 0; b0 < B; b0 += 32) {
+    const SplitShape sh = shape_of(b0 + lane);
+#pragma unroll
+    for (int k = 0; k < kOrderBuckets; ++k) {
+      const int c = __popc(__ballot_sync(0xFFFFFFFFu, sh.bk == k));
+      if (lane == k) cnt += c;
+    }
+  }
+  int j = p - F, K = -1;
+  for (int k = kOrderBuckets - 1; k >= 0; --k) {  // largest bucket first
+    const int c = __shfl_sync(0xFFFFFFFFu, cnt, k);
+    if (j < c) {
+      K = k;
+      break;
+    }
+    j -= c;
+  }
+  if (K < 0) return make_int2(-1, -1);
+  for (int b0 = 0; b0 < B; b0 += 32) {  // the j-th sequence of bucket K, in batch order
+    const SplitShape sh = shape_of(b0 + lane);
+    const unsigned m = __ballot_sync(0xFFFFFFFFu, sh.bk == K);
+    const int c = __popc(m);
+    if (j < c) {
+      const unsigned below = (1u << lane) - 1u;
+      const unsigned hit = __ballot_sync(0xFFFFFFFFu, ((m >> lane) & 1u) && __popc(m & below) == j);
+      const int src = __ffs(hit) - 1;
+      return make_int2(b0 + src, __shfl_sync(0xFFFFFFFFu, sh.nf, src));
+    }
+    j -= c;
+  }
+  return make_int2(-1, -1);
 }
 
 __device__ __forceinline__ void consumer_bar_sync() {
@@ -105,23 +217,41 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<D, GMAX>::kMinBlocks
                         const __grid_constant__ CUtensorMap tm_v, const uint16_t* __restrict__ q,
                         const int* __restrict__ kv_lens, float* __restrict__ part_o,
                         float* __restrict__ part_lse, int Hq, int Hkv, int max_kv, int n_splits,
-                        int min_rows, float scale, int heads_per_cta, uint32_t* err) {
+                        int min_rows, float scale, int heads_per_cta, int ordered, int B,
+                        uint32_t* err) {
   using C = DecodeCfg<D, GMAX>;
   constexpr int DPL = D / 32;   // output dims per lane in the P.V phase
   constexpr int DP2 = DPL / 2;  // ... as fp32 pairs
-  // CTA = (split, KV head, batch x head group): the query heads [g0, g0 + G) of
-  // the KV head's group (all of them unless a small launch splits the group
-  // across CTAs, which then re-read the same K/V rows from L2)
+  // CTA = (unit, KV head, head group): the query heads [g0, g0 + G) of the KV
+  // head's group (all of them unless a small launch splits the group across
+  // CTAs, which then re-read the same K/V rows from L2).  The CTAs of one unit
+  // are adjacent, so the KV heads of the same rows are read together.
   const int Gall = Hq / Hkv;
-  const int s_idx = blockIdx.x, hk = blockIdx.y;
-  int b = blockIdx.z, g0 = 0, G = Gall;
+  const int n_hg = SPLIT_HEADS ? (Gall + heads_per_cta - 1) / heads_per_cta : 1;
+  const int per_unit = Hkv * n_hg;
+  const int pos = (int)(blockIdx.x / per_unit), w_in = (int)(blockIdx.x % per_unit);
+  const int hk = w_in / n_hg;
+  int g0 = 0, G = Gall;
   if constexpr (SPLIT_HEADS) {
-    const int n_hg = (Gall + heads_per_cta - 1) / heads_per_cta;
-    b = blockIdx.z / n_hg;
-    g0 = (blockIdx.z % n_hg) * heads_per_cta;
+    g0 = (w_in % n_hg) * heads_per_cta;
     G = min(heads_per_cta, Gall - g0);
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int b, s_idx;
+  if (ordered) {
+    __shared__ int2 unit_sh;
+    if (warp == 0) {
+      const int2 u = unit_at(pos, kv_lens, B, max_kv, n_splits, min_rows, lane);
+      if (lane == 0) unit_sh = u;
+    }
+    __syncthreads();
+    b = unit_sh.x;
+    s_idx = unit_sh.y;
+    if (b < 0) return;  // not reached while kv_lens is unchanged during the launch
+  } else {
+    b = pos / n_splits;
+    s_idx = pos % n_splits;
+  }
 
   // ---- split bounds: chunk = max(ceil(L / n_splits), min_rows) ----
   int L = kv_lens[b];
@@ -244,26 +374,22 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<D, GMAX>::kMinBlocks
     }
 
     // ---- scores: lane = row; fp32 pairs along the head dim ----
-    uint64_t acc[GMAX];
+    float acl[GMAX], ach[GMAX];
 #pragma unroll
-    for (int g = 0; g < GMAX; ++g) acc[g] = f2pack(0.f, 0.f);
+    for (int g = 0; g < GMAX; ++g) acl[g] = ach[g] = 0.f;
 #pragma unroll
     for (int c = 0; c < D / 8; ++c) {
       const int p = c >> 3, cc = c & 7;
       const uint4 kv = *reinterpret_cast<const uint4*>(kt + p * C::kPanelBytes + lane * 128 +
                                                        ((cc ^ (lane & 7)) << 4));
-      const uint64_t k01 = bf16x2_to_f2(kv.x), k23 = bf16x2_to_f2(kv.y);
-      const uint64_t k45 = bf16x2_to_f2(kv.z), k67 = bf16x2_to_f2(kv.w);
 #pragma unroll
       for (int g = 0; g < GMAX; ++g) {
         if (g < G) {
           const uint4 qv = *reinterpret_cast<const uint4*>(qs + g * D + c * 8);  // 8 bf16, broadcast
-          uint64_t a = acc[g];
-          a = fma2(bf16x2_to_f2(qv.x), k01, a);
-          a = fma2(bf16x2_to_f2(qv.y), k23, a);
-          a = fma2(bf16x2_to_f2(qv.z), k45, a);
-          a = fma2(bf16x2_to_f2(qv.w), k67, a);
-          acc[g] = a;
+          fma_bf16x2_f32(qv.x, kv.x, acl[g], ach[g]);
+          fma_bf16x2_f32(qv.y, kv.y, acl[g], ach[g]);
+          fma_bf16x2_f32(qv.z, kv.z, acl[g], ach[g]);
+          fma_bf16x2_f32(qv.w, kv.w, acl[g], ach[g]);
         }
       }
     }
@@ -277,7 +403,7 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<D, GMAX>::kMinBlocks
 #pragma unroll
     for (int g = 0; g < GMAX; ++g) {
       if (g < G) {
-        const float sv = valid ? f2sum(acc[g]) * qscale : -INFINITY;
+        const float sv = valid ? (acl[g] + ach[g]) * qscale : -INFINITY;
         const float tmax = warp_max(sv);  // finite: every tile has >= 1 valid row
         const float m_new = fmaxf(m[g], tmax);
         const float corr = ex2_approx(m[g] - m_new);  // m = -inf -> 0
@@ -459,13 +585,13 @@ cudaError_t launch_decode_t(const DecodeArgs& a, int heads_per_cta, cudaStream_t
                                        C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int G = a.Hq / a.Hkv;
-  const int n_hg = (G + heads_per_cta - 1) / heads_per_cta;
-  if ((long long)a.B * n_hg > 65535) return cudaErrorInvalidValue;
-  dim3 grid(a.n_splits, a.Hkv, a.B * n_hg);
-  kern<<<grid, kDecodeThreads, C::kSmemBytes, stream>>>(a.tm_k, a.tm_v, a.q, a.kv_lens, a.part_o,
-                                                         a.part_lse, a.Hq, a.Hkv, a.max_kv,
-                                                         a.n_splits, a.min_rows, a.scale,
-                                                         heads_per_cta, a.err);
+  const int n_hg = SPLIT_HEADS ? (G + heads_per_cta - 1) / heads_per_cta : 1;
+  const long long ctas = (long long)a.B * a.n_splits * a.Hkv * n_hg;
+  if (ctas > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+  const int ordered = a.B <= kOrderMaxBatch ? 1 : 0;
+  kern<<<(unsigned)ctas, kDecodeThreads, C::kSmemBytes, stream>>>(
+      a.tm_k, a.tm_v, a.q, a.kv_lens, a.part_o, a.part_lse, a.Hq, a.Hkv, a.max_kv, a.n_splits,
+      a.min_rows, a.scale, heads_per_cta, ordered, a.B, a.err);
   return cudaGetLastError();
 }
 

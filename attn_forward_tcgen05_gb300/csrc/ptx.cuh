@@ -607,6 +607,16 @@ __device__ __forceinline__ void add_bf16x2_f32(uint32_t pk, float& acc_lo, float
       : "r"(pk));
 }
 
+// lo += a.lo * b.lo, hi += a.hi * b.hi for bf16 pairs a, b: mixed-precision fma
+// with bf16 multiplicands and an fp32 addend.  A product of two bf16 values is
+// exact in fp32, so this rounds once, like an fp32 fma of the widened values.
+__device__ __forceinline__ void fma_bf16x2_f32(uint32_t a, uint32_t b, float& lo, float& hi) {
+  asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %2;\n\tmov.b32 {bl, bh}, %3;\n\t"
+      "fma.rn.f32.bf16 %0, al, bl, %0;\n\tfma.rn.f32.bf16 %1, ah, bh, %1;\n\t}"
+      : "+f"(lo), "+f"(hi)
+      : "r"(a), "r"(b));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   // cvt packs its first source into the upper half.

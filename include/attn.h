@@ -245,6 +245,10 @@ int attn_prefill_varlen_window(const attn_bf16_t* q, const attn_bf16_t* kcache,
  * part_lse = -inf and part_o = 0.
  * Split rule: chunk_b = max(ceil(L_b / n_splits), min_rows_per_split); split s
  * covers [s*chunk_b, min(L_b, (s+1)*chunk_b)).
+ * Launch order (throughput only, results do not depend on it): the full splits
+ * of every sequence start first, then the partial last splits by size, then
+ * the empty ones.  Each CTA derives its split from kv_lens, so kv_lens must not
+ * change while the call runs.
  * Follows "66 . D2: explicit K+V register staging", section 3.2 (one split =
  * rows [lo, hi) of one sequence and KV head; score, running max, running sum
  * and running O) and section 2.2 (K and V loads issued ahead of the

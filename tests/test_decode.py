@@ -80,3 +80,31 @@ def test_merge_random_partials():
     ro, rl = oracle.merge(po, pl)
     check_o(o.cpu().numpy(), ro, False)
     check_lse(lse.cpu().numpy(), rl)
+
+
+def _order_lens(B, hi, seed, edges):
+    g = torch.Generator().manual_seed(seed)
+    lens = torch.randint(0, hi + 1, (B,), generator=g, dtype=torch.int32)
+    lens[: len(edges)] = torch.tensor(edges, dtype=torch.int32)
+    return lens
+
+
+@pytest.mark.parametrize("n_splits,min_rows", [(8, 64), (5, 1)])
+def test_unit_order_ragged_tails(n_splits, min_rows):
+    """The launch runs full splits first, then the partial last splits by size,
+    then the empty ones.  Lengths cover every size bucket of the partial splits,
+    ties inside a bucket, sequences with no partial split (multiples of the
+    chunk), empty sequences, and a batch that is not a multiple of 32."""
+    edges = [0, 64, 128, 512, 1, 3, 4, 63, 65, 100, 127, 129, 191, 255, 256, 257, 511, 513, 0, 4, 4, 1500]
+    lens = _order_lens(70, 1500, 77 + n_splits, edges)
+    q, kc, vc = W.decode_inputs(70, 8, 2, 128, lens, 78 + n_splits, Lmax=1500)
+    _compare(q, kc, vc, lens, n_splits, min_rows, 1.0 / math.sqrt(128))
+
+
+@pytest.mark.parametrize("B", [1024, 1030])
+def test_unit_order_large_batches(B):
+    """1024 sequences: the largest batch that takes the size order (32 passes of
+    the warp over the lengths); 1030 takes the batch-major order."""
+    lens = _order_lens(B, 40, B, [0, 1, 8, 16, 40])
+    q, kc, vc = W.decode_inputs(B, 4, 2, 64, lens, B + 1, Lmax=40)
+    _compare(q, kc, vc, lens, 4, 8, 0.125, torch.float32)
