@@ -501,6 +501,10 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<D, GMAX>::kMinBlocks
   }
 }
 
+// Non-empty splits whose partial rows a merge warp loads at once: eight covers
+// the common split counts in one round trip (four took two on eight splits).
+constexpr int kMergeBatch = 8;
+
 template <int D>
 __global__ void __launch_bounds__(128)
     merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse, void* o,
@@ -527,18 +531,18 @@ __global__ void __launch_bounds__(128)
       wsum += w;
       uint32_t live = __ballot_sync(0xFFFFFFFFu, w > 0.f);  // empty splits are never read
       while (live) {
-        // up to four non-empty splits per round: their loads are issued together
-        int idx[4];
-        float wk[4];
+        // up to kMergeBatch non-empty splits per round: their loads are issued together
+        int idx[kMergeBatch];
+        float wk[kMergeBatch];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < kMergeBatch; ++u) {
           idx[u] = live ? __ffs(live) - 1 : -1;
           if (live) live &= live - 1;
           wk[u] = __shfl_sync(0xFFFFFFFFu, w, idx[u] < 0 ? 0 : idx[u]);
         }
-        float x[4][DPL];
+        float x[kMergeBatch][DPL];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < kMergeBatch; ++u) {
           if (idx[u] >= 0) {
             const float* src = po + (size_t)(s0 + idx[u]) * D;
 #pragma unroll
@@ -550,7 +554,7 @@ __global__ void __launch_bounds__(128)
           }
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < kMergeBatch; ++u) {
           if (idx[u] >= 0) {
 #pragma unroll
             for (int e = 0; e < DPL; ++e) acc[e] = fmaf(wk[u], x[u][e], acc[e]);
