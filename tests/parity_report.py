@@ -89,16 +89,20 @@ def window_row(label, s, peak_tc):
     b = s.base
     q, k, v = W.prefill_inputs_for(b)
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
-    o, lse = prefill_window(qd, kd, vd, s.window, s.n_sink, scale=b.scale, out_dtype=torch.float32)
+    # timed with bf16 O (the bench line's output type); errors for both output types
+    o, lse = prefill_window(qd, kd, vd, s.window, s.n_sink, scale=b.scale, out_dtype=torch.bfloat16)
     ms = gpu_time_ms(lambda: prefill_window(qd, kd, vd, s.window, s.n_sink, scale=b.scale, out=(o, lse)))
+    o32, _ = prefill_window(qd, kd, vd, s.window, s.n_sink, scale=b.scale, out_dtype=torch.float32)
+    sync_check()
     t0 = time.perf_counter()
     ro, rl = oracle.sdpa_window(q, k, v, s.window, s.n_sink, b.scale)
     cpu_s = time.perf_counter() - t0
     tf = W.window_flops(s) / (ms * 1e-3) / 1e12
-    eo = max_err(o.cpu().numpy(), ro)
+    e16 = max_err(o.float().cpu().numpy(), ro)
+    eo = max_err(o32.cpu().numpy(), ro)
     el = max_err(lse.cpu().numpy(), rl)
     return (f"| {label} | {ms * 1e3:.1f} µs | {tf:.1f} TFLOP/s | {tf / peak_tc:.3f} of {peak_tc:.1f} TFLOP/s "
-            f"| {eo:.2e} (fp32 O) | {el:.2e} | {cpu_s:.2f} s ({oracle.num_cores()} cores) |")
+            f"| {eo:.2e} (fp32 O); {e16:.2e} (bf16 O) | {el:.2e} | {cpu_s:.2f} s ({oracle.num_cores()} cores) |")
 
 
 def decode_row(label, s, peak_hbm):
