@@ -108,3 +108,30 @@ def test_unit_order_large_batches(B):
     lens = _order_lens(B, 40, B, [0, 1, 8, 16, 40])
     q, kc, vc = W.decode_inputs(B, 4, 2, 64, lens, B + 1, Lmax=40)
     _compare(q, kc, vc, lens, 4, 8, 0.125, torch.float32)
+
+
+def test_unit_order_no_partial_splits():
+    """Every length a multiple of its chunk (8 splits, at least 64 rows each):
+    the launch has full and empty units only."""
+    lens = torch.tensor([64, 128, 512, 1024, 0, 192, 2048, 64, 448, 320], dtype=torch.int32)
+    q, kc, vc = W.decode_inputs(10, 8, 2, 128, lens, 91, Lmax=2048)
+    _compare(q, kc, vc, lens, 8, 64, 1.0 / math.sqrt(128))
+
+
+def test_unit_order_all_empty():
+    """No sequence has keys: every unit is empty, O = 0 and LSE = -inf."""
+    lens = torch.zeros(40, dtype=torch.int32)
+    q, kc, vc = W.decode_inputs(40, 8, 2, 64, lens, 92, Lmax=16)
+    po, pl = decode_split(q.cuda(), kc.cuda(), vc.cuda(), lens.cuda(), 8, 1, 0.125)
+    o, lse = merge(po, pl, torch.float32)
+    sync_check()
+    assert torch.all(pl.cpu() == -math.inf) and torch.all(po.cpu() == 0)
+    assert torch.all(o.cpu() == 0) and torch.all(lse.cpu() == -math.inf)
+
+
+def test_max_splits():
+    """The largest split count (1024) on short sequences: most units hold one or
+    two rows or none, and the merge walks 32 batches of split weights."""
+    lens = torch.tensor([1500, 1, 700], dtype=torch.int32)
+    q, kc, vc = W.decode_inputs(3, 8, 2, 128, lens, 93, Lmax=1500)
+    _compare(q, kc, vc, lens, 1024, 1, 1.0 / math.sqrt(128))
