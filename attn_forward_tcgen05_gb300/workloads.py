@@ -14,7 +14,7 @@ Workloads (names used throughout the tests and the benchmark):
                         8 splits (min 1 row per split), merged to O bf16 + LSE fp32
 * ``mha_noncausal_4096_d{64,128,256}``  B=2, Hq=Hkv=16, S=4096, non-causal, scale 1/sqrt(d)
 * ``ragged_gqa_decode_b64`` B=64, Hq=32, Hkv=8, d=128, KV lengths ~ U[512, 8192],
-                        at most 8 splits of at least 1024 rows each (1 to 8 per
+                        at most 4 splits of at least 1536 rows each (1 to 4 per
                         sequence, chosen by its length), O bf16 + LSE fp32
 * ``gqa_prefill_3314_window1024_sink4`` the GQA prefill inputs, causal over a
                         1024-position sliding window plus 4 sink positions
@@ -75,8 +75,10 @@ def mha_sweep(d: int) -> PrefillShape:
                         1.0 / math.sqrt(float(d)), "bf16", 1000 + 4 * 10 + d // 64)
 
 
-RAGGED_DECODE = DecodeShape("ragged_gqa_decode_b64", 64, 32, 8, 128, 1.0 / math.sqrt(128.0), 8,
-                            1024, 1005, len_range=(512, 8192))
+# split policy: 4 splits of at least 1536 rows (a sweep of 4/8/16 splits and
+# 512-2048 minimum rows on one GB300: 223.9 us split + merge, 8 of 1024: 231.0)
+RAGGED_DECODE = DecodeShape("ragged_gqa_decode_b64", 64, 32, 8, 128, 1.0 / math.sqrt(128.0), 4,
+                            1536, 1005, len_range=(512, 8192))
 
 # multi-query decode (one KV head for 128 query heads, the head count of the
 # FMHA page's D2 workload), head dimension 128, ragged lengths as the GQA batch

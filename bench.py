@@ -268,7 +268,9 @@ def run_ours(args, rank, world, local_rank):
     decode_roof = {"bound": "hbm", "kernel": "decode_split_kernel<128,4>", "workload": D5.name,
                    "achieved": round(split_gbs, 1), "peak": peak_hbm, "unit": "GB/s",
                    "frac": round(split_gbs / peak_hbm, 4),
-                   "traffic": traffic.get(f"decode_split_kernel<128,4> {D5.name}"),
+                   # keyed by split policy too: a capture holds for the grid it was taken on
+                   "traffic": traffic.get(f"decode_split_kernel<128,4> {D5.name} "
+                                          f"{D5.n_splits}x{D5.min_rows_per_split}"),
                    "step_share": round(t_split5 / ms_step, 4),
                    "peak_source": f"hbm_gbs of {peak_src}"}
     if not do_decode:

@@ -53,10 +53,13 @@ def test_large_scores():
     _compare(q, kc, vc, lens, 5, 1, 0.5)
 
 
-def test_ragged_b64_full():
+@pytest.mark.parametrize("policy", ["workload", "8x1024"])
+def test_ragged_b64_full(policy):
+    # the benchmark's split policy, and 8 splits of at least 1024 rows
     s = W.RAGGED_DECODE
     q, kc, vc, lens = W.decode_inputs_for(s)
-    _compare(q, kc, vc, lens, s.n_splits, s.min_rows_per_split, s.scale)
+    ns, mr = (s.n_splits, s.min_rows_per_split) if policy == "workload" else (8, 1024)
+    _compare(q, kc, vc, lens, ns, mr, s.scale)
 
 
 def test_ragged_b64_sixteen_splits():
