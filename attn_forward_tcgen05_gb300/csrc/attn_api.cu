@@ -313,7 +313,9 @@ int attn_decode_split(const attn_bf16_t* q, const attn_bf16_t* kcache, const att
     return ATTN_ERR_INVALID_ARG;
   if (n_splits < 1 || n_splits > 1024 || min_rows_per_split < 0 || !ok_scale(scale))
     return ATTN_ERR_INVALID_ARG;
-  if (B > 65535 || Hkv > 65535) return ATTN_ERR_INVALID_ARG;
+  // one CTA per (sequence, KV head, split) in a 1-D grid (launches of fewer than
+  // 128 such units also spread head groups, and stay far below the limit)
+  if ((long long)B * Hkv * n_splits > 0x7FFFFFFFLL) return ATTN_ERR_INVALID_ARG;
   if (!ok_dim(d)) return ATTN_ERR_UNSUPPORTED;
   if (B == 0) return ATTN_OK;
   if (!q || !kcache || !vcache || !kv_lens || !part_o || !part_lse) return ATTN_ERR_INVALID_ARG;

@@ -263,7 +263,7 @@ int attn_prefill_varlen_window(const attn_bf16_t* q, const attn_bf16_t* kcache,
  *   B, Hq, Hkv, d, max_kv                 B >= 0, Hq % Hkv == 0, Hq/Hkv <= 16, d in {64,128,256},
  *                                         max_kv >= 1
  *   scale                                 softmax scale (finite, > 0)
- *   n_splits                              >= 1 and <= 1024
+ *   n_splits                              >= 1 and <= 1024; B * Hkv * n_splits <= 2^31 - 1
  *   min_rows_per_split                    >= 0
  *   part_o    fp32 [B][Hq][n_splits][d]   output (scratch for attn_merge)
  *   part_lse  fp32 [B][Hq][n_splits]      output

@@ -138,6 +138,8 @@ def test_decode_and_merge_validation(lib):
     assert f(P, P, P, P, 1, 28, 4, 128, 10, 0.1, 0, 1, P, P, N) == attn.ATTN_ERR_INVALID_ARG  # n_splits
     assert f(P, P, P, P, 1, 28, 4, 128, 0, 0.1, 8, 1, P, P, N) == attn.ATTN_ERR_INVALID_ARG  # max_kv
     assert f(P, P, P, N, 1, 28, 4, 128, 10, 0.1, 8, 1, P, P, N) == attn.ATTN_ERR_INVALID_ARG  # lens
+    # one CTA per (sequence, KV head, split): more than 2^31 - 1 is refused up front
+    assert f(P, P, P, P, 1 << 20, 4, 4, 64, 1, 0.1, 1024, 1, P, P, N) == attn.ATTN_ERR_INVALID_ARG
     assert f(N, N, N, N, 0, 28, 4, 128, 10, 0.1, 8, 1, N, N, N) == attn.ATTN_OK
     g = attn.attn_merge
     assert g(P, P, P, P, 1, 4, 8, 100, 1, N) == attn.ATTN_ERR_UNSUPPORTED
