@@ -22,6 +22,7 @@ ATTN_ERR_UNSUPPORTED = -2
 ATTN_ERR_CUDA = -3
 ATTN_ERR_DEVICE_TIMEOUT = -4
 ATTN_ERR_SCRATCH_TOO_SMALL = -5
+ATTN_ERR_DEVICE_INPUT = -6
 ATTN_F32 = 0
 ATTN_BF16 = 1
 

@@ -93,11 +93,51 @@ int encode_bf16_q5d(CUtensorMap* map, const void* base, uint64_t d, uint64_t G, 
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool ok_dim(int d) { return d == 64 || d == 128 || d == 256; }
+// head dims of the fixed-length prefill (attn_prefill_fwd): also 512
+bool ok_dim_prefill(int d) { return ok_dim(d) || d == 512; }
 bool ok_scale(float s) { return std::isfinite(s) && s > 0.f; }
 
 int from_cuda(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
 
 }  // namespace
+
+namespace attn {
+
+int check_decode_split_args(const void* q, const void* kcache, const void* vcache, const int* kv_lens,
+                            int B, int Hq, int Hkv, int d, int max_kv, float scale, int n_splits,
+                            int min_rows, const void* part_o, const void* part_lse, bool check_parts) {
+  if (B < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Hq / Hkv > 16 || max_kv < 1)
+    return ATTN_ERR_INVALID_ARG;
+  if (n_splits < 1 || n_splits > 1024 || min_rows < 0 || !ok_scale(scale)) return ATTN_ERR_INVALID_ARG;
+  // one CTA per (sequence, KV head, split) in a 1-D grid (launches of fewer than
+  // 128 such units also spread head groups, and stay far below the limit)
+  if ((long long)B * Hkv * n_splits > 0x7FFFFFFFLL) return ATTN_ERR_INVALID_ARG;
+  if (!ok_dim(d)) return ATTN_ERR_UNSUPPORTED;
+  if (B == 0) return ATTN_OK;
+  if (!q || !kcache || !vcache || !kv_lens) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || (reinterpret_cast<uintptr_t>(kv_lens) & 3u))
+    return ATTN_ERR_INVALID_ARG;
+  if (check_parts && (!part_o || !part_lse || !aligned16(part_o) ||
+                      (reinterpret_cast<uintptr_t>(part_lse) & 3u)))
+    return ATTN_ERR_INVALID_ARG;
+  if ((long long)B * max_kv * Hkv >= (1LL << 31)) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+int check_merge_args(const void* part_o, const void* part_lse, const void* o, const void* lse, int B,
+                     int Hq, int n_splits, int d, int o_dtype, bool check_partials) {
+  if (B < 0 || Hq < 1 || n_splits < 1 || n_splits > 1024) return ATTN_ERR_INVALID_ARG;
+  if (!ok_dim(d) || (o_dtype != ATTN_F32 && o_dtype != ATTN_BF16)) return ATTN_ERR_UNSUPPORTED;
+  if (B == 0) return ATTN_OK;
+  if (!o || !lse || !aligned16(o) || (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_INVALID_ARG;
+  if (check_partials && (!part_o || !part_lse || !aligned16(part_o) ||
+                         (reinterpret_cast<uintptr_t>(part_lse) & 3u)))
+    return ATTN_ERR_INVALID_ARG;
+  if ((long long)B * Hq >= (1LL << 31)) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+}  // namespace attn
 
 // kv_lens (optional): keys per sequence, each sequence's Sq queries being its last
 // positions; pack: query heads folded into the tile rows (single-CTA kernel only).
@@ -108,7 +148,10 @@ static int prefill_impl(const attn_bf16_t* q, const attn_bf16_t* k, const attn_b
                         int split_min = 0, float* part_o = nullptr, float* part_lse = nullptr) {
   if (B < 0 || Sq < 0 || Skv < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (!ok_scale(scale)) return ATTN_ERR_INVALID_ARG;
-  if (!ok_dim(d) || (o_dtype != ATTN_F32 && o_dtype != ATTN_BF16)) return ATTN_ERR_UNSUPPORTED;
+  if (!ok_dim_prefill(d) || (o_dtype != ATTN_F32 && o_dtype != ATTN_BF16)) return ATTN_ERR_UNSUPPORTED;
+  // head dim 512: plain fixed-length prefill only (no window, packing, key splits or kv_lens)
+  const bool d512 = d == 512;
+  if (d512 && (window != 0 || pack != 1 || n_splits > 1 || kv_lens != nullptr)) return ATTN_ERR_UNSUPPORTED;
   if (B == 0 || Sq == 0) return ATTN_OK;
   if (!q || !o || !lse || !aligned16(q) || !aligned16(o) || !aligned16(lse))
     return ATTN_ERR_INVALID_ARG;
@@ -140,6 +183,13 @@ static int prefill_impl(const attn_bf16_t* q, const attn_bf16_t* k, const attn_b
   if (a.err == nullptr) return ATTN_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (Skv == 0) return from_cuda(attn::launch_prefill_empty_kv(a, s));
+  if (d512) {
+    int rc = encode_bf16_q5d(&a.tm_q, q, d, 1, Hq, Sq, B);
+    if (rc == ATTN_OK) rc = encode_bf16_4d(&a.tm_k, k, d, Hkv, Skv, B, attn::kPrefillKVStageRows);
+    if (rc == ATTN_OK) rc = encode_bf16_4d(&a.tm_v, v, d, Hkv, Skv, B, attn::kPrefillKVStageRows);
+    if (rc != ATTN_OK) return rc;
+    return from_cuda(attn::launch_prefill_d512(a, s));
+  }
   const bool pair = attn::prefill_uses_pair(d);
   if (pair && pack != 1) return ATTN_ERR_UNSUPPORTED;
   int rc = pair ? encode_bf16_4d(&a.tm_q, q, d, Hq, Sq, B, attn::kPrefillTileM)
@@ -214,6 +264,7 @@ const char* attn_strerror(int status) {
     case ATTN_ERR_CUDA: return "CUDA runtime or launch error";
     case ATTN_ERR_DEVICE_TIMEOUT: return "a kernel's bounded pipeline wait timed out";
     case ATTN_ERR_SCRATCH_TOO_SMALL: return "problem too large for the library's static decode scratch (24 MiB)";
+    case ATTN_ERR_DEVICE_INPUT: return "a kernel found a device-side input (kv_lens) changed while it ran";
     default: return "unknown status";
   }
 }
@@ -228,8 +279,6 @@ int attn_prefill_window(const attn_bf16_t* q, const attn_bf16_t* k, const attn_b
                         float* lse, int B, int Hq, int Hkv, int Sq, int Skv, int d, int window,
                         int n_sink, float scale, int o_dtype, attn_stream_t stream) {
   if (window < 1 || n_sink < 0) return ATTN_ERR_INVALID_ARG;
-  // the experimental d = 128 pair build has no window support
-  if (ATTN_PREFILL_PAIR_D128 && d == 128) return ATTN_ERR_UNSUPPORTED;
   return prefill_impl(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, d, 1, window, n_sink, scale, o_dtype, stream);
 }
 
@@ -299,8 +348,6 @@ int attn_prefill_varlen_window(const attn_bf16_t* q, const attn_bf16_t* kcache,
                                int total_q, int max_sq, int max_kv, int d, int window, int n_sink,
                                float scale, int o_dtype, attn_stream_t stream) {
   if (window < 1 || n_sink < 0) return ATTN_ERR_INVALID_ARG;
-  // the experimental d = 128 pair build has no window support
-  if (ATTN_PREFILL_PAIR_D128 && d == 128) return ATTN_ERR_UNSUPPORTED;
   return varlen_impl(q, kcache, vcache, o, lse, cu_seqlens_q, kv_lens, B, Hq, Hkv, total_q, max_sq,
                      max_kv, d, 1, window, n_sink, scale, o_dtype, stream);
 }
@@ -309,20 +356,9 @@ int attn_decode_split(const attn_bf16_t* q, const attn_bf16_t* kcache, const att
                       const int* kv_lens, int B, int Hq, int Hkv, int d, int max_kv, float scale,
                       int n_splits, int min_rows_per_split, float* part_o, float* part_lse,
                       attn_stream_t stream) {
-  if (B < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Hq / Hkv > 16 || max_kv < 1)
-    return ATTN_ERR_INVALID_ARG;
-  if (n_splits < 1 || n_splits > 1024 || min_rows_per_split < 0 || !ok_scale(scale))
-    return ATTN_ERR_INVALID_ARG;
-  // one CTA per (sequence, KV head, split) in a 1-D grid (launches of fewer than
-  // 128 such units also spread head groups, and stay far below the limit)
-  if ((long long)B * Hkv * n_splits > 0x7FFFFFFFLL) return ATTN_ERR_INVALID_ARG;
-  if (!ok_dim(d)) return ATTN_ERR_UNSUPPORTED;
-  if (B == 0) return ATTN_OK;
-  if (!q || !kcache || !vcache || !kv_lens || !part_o || !part_lse) return ATTN_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(part_o) ||
-      (reinterpret_cast<uintptr_t>(kv_lens) & 3u) || (reinterpret_cast<uintptr_t>(part_lse) & 3u))
-    return ATTN_ERR_INVALID_ARG;
-  if ((long long)B * max_kv * Hkv >= (1LL << 31)) return ATTN_ERR_INVALID_ARG;
+  const int rc0 = attn::check_decode_split_args(q, kcache, vcache, kv_lens, B, Hq, Hkv, d, max_kv, scale,
+                                                n_splits, min_rows_per_split, part_o, part_lse, true);
+  if (rc0 != ATTN_OK || B == 0) return rc0;
   attn::DecodeArgs a;
   std::memset(&a, 0, sizeof(a));
   a.q = q; a.kv_lens = kv_lens; a.part_o = part_o; a.part_lse = part_lse;
@@ -338,14 +374,8 @@ int attn_decode_split(const attn_bf16_t* q, const attn_bf16_t* kcache, const att
 
 int attn_merge(const float* part_o, const float* part_lse, void* o, float* lse, int B, int Hq,
                int n_splits, int d, int o_dtype, attn_stream_t stream) {
-  if (B < 0 || Hq < 1 || n_splits < 1 || n_splits > 1024) return ATTN_ERR_INVALID_ARG;
-  if (!ok_dim(d) || (o_dtype != ATTN_F32 && o_dtype != ATTN_BF16)) return ATTN_ERR_UNSUPPORTED;
-  if (B == 0) return ATTN_OK;
-  if (!part_o || !part_lse || !o || !lse) return ATTN_ERR_INVALID_ARG;
-  if (!aligned16(part_o) || !aligned16(o) || (reinterpret_cast<uintptr_t>(part_lse) & 3u) ||
-      (reinterpret_cast<uintptr_t>(lse) & 3u))
-    return ATTN_ERR_INVALID_ARG;
-  if ((long long)B * Hq >= (1LL << 31)) return ATTN_ERR_INVALID_ARG;
+  const int rc0 = attn::check_merge_args(part_o, part_lse, o, lse, B, Hq, n_splits, d, o_dtype, true);
+  if (rc0 != ATTN_OK || B == 0) return rc0;
   attn::MergeArgs a;
   a.part_o = part_o; a.part_lse = part_lse; a.o = o; a.lse = lse;
   a.B = B; a.Hq = Hq; a.n_splits = n_splits; a.d = d; a.o_bf16 = o_dtype == ATTN_BF16 ? 1 : 0;
@@ -362,7 +392,7 @@ int attn_sync_check(attn_stream_t stream) {
   if (h != 0) {
     const uint32_t zero = 0;
     if (cudaMemcpy(e, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return ATTN_ERR_CUDA;
-    return ATTN_ERR_DEVICE_TIMEOUT;
+    return h == attn::kErrBadShape ? ATTN_ERR_DEVICE_INPUT : ATTN_ERR_DEVICE_TIMEOUT;
   }
   return ATTN_OK;
 }

@@ -247,7 +247,14 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<D, GMAX>::kMinBlocks
     __syncthreads();
     b = unit_sh.x;
     s_idx = unit_sh.y;
-    if (b < 0) return;  // not reached while kv_lens is unchanged during the launch
+    if (b < 0) {
+      // Only reachable if kv_lens changed while the launch ran (the launch order is
+      // derived from it by every CTA): this unit's partials are not written, so the
+      // call is reported as failed through the error word rather than leaving stale
+      // partials for the merge to combine silently.
+      if (threadIdx.x == 0) atomicCAS(err, kErrNone, kErrBadShape);
+      return;
+    }
   } else {
     b = pos / n_splits;
     s_idx = pos % n_splits;

@@ -9,17 +9,20 @@
 // device allocator at all.  attn_decode_noalloc keeps those partials in a
 // fixed-size array of device memory that belongs to the library instead.
 //
-// The array below is reserved on every GPU that loads the library and stays
-// reserved until the process exits.  All calls on a device share it: a call
-// overwrites every entry it reads before reading it, so nothing has to start
-// at zero, but two calls whose work overlaps on the GPU (e.g. on two streams)
-// race on it.
+// The array below is part of this library's device code, so it is reserved on
+// a GPU when that code is loaded there -- with CUDA's default lazy loading, at
+// the library's first use on that device -- and stays reserved until the
+// process exits.  All calls on a device share it: a call overwrites every entry
+// it reads before reading it, so nothing has to start at zero, but two calls
+// whose work overlaps on the GPU (e.g. on two streams) race on it.  The cached
+// address below does not survive a cudaDeviceReset() of its device.
 #include <cuda_runtime.h>
 
 #include <cstdint>
 #include <mutex>
 
 #include "attn.h"
+#include "internal.h"
 
 namespace {
 
@@ -61,20 +64,21 @@ int attn_decode_noalloc(const attn_bf16_t* q, const attn_bf16_t* kcache, const a
                         const int* kv_lens, int B, int Hq, int Hkv, int d, int max_kv, float scale,
                         int n_splits, int min_rows_per_split, void* o, float* lse, int o_dtype,
                         attn_stream_t stream) {
-  // the same argument rules as attn_decode_split / attn_merge, checked before any CUDA call
-  if (B < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Hq / Hkv > 16 || max_kv < 1 ||
-      n_splits < 1 || n_splits > 1024 || min_rows_per_split < 0)
-    return ATTN_ERR_INVALID_ARG;
-  if ((d != 64 && d != 128 && d != 256) || (o_dtype != ATTN_F32 && o_dtype != ATTN_BF16))
-    return ATTN_ERR_UNSUPPORTED;
+  // the argument rules of attn_decode_split (its partial buffers aside: they are
+  // the scratch array) and of attn_merge, checked before the size and before any
+  // CUDA call, so a malformed call is reported as such whatever its size
+  int rc = attn::check_decode_split_args(q, kcache, vcache, kv_lens, B, Hq, Hkv, d, max_kv, scale,
+                                         n_splits, min_rows_per_split, nullptr, nullptr, false);
+  if (rc != ATTN_OK) return rc;
+  rc = attn::check_merge_args(nullptr, nullptr, o, lse, B, Hq, n_splits, d, o_dtype, false);
+  if (rc != ATTN_OK) return rc;
   if (B == 0) return ATTN_OK;
-  if (!q || !kcache || !vcache || !kv_lens || !o || !lse) return ATTN_ERR_INVALID_ARG;
   const size_t rows = (size_t)B * (size_t)Hq * (size_t)n_splits;
   const size_t o_bytes = round_up_256(rows * (size_t)d * sizeof(float));
   const size_t lse_bytes = round_up_256(rows * sizeof(float));
   if (o_bytes + lse_bytes > kScratchBytes) return ATTN_ERR_SCRATCH_TOO_SMALL;
   float* scratch = nullptr;
-  int rc = scratch_address(&scratch);
+  rc = scratch_address(&scratch);
   if (rc != ATTN_OK) return rc;
   float* part_o = scratch;
   float* part_lse = scratch + o_bytes / sizeof(float);

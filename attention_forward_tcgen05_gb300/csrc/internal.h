@@ -140,16 +140,24 @@ constexpr int kPrefillKVStageRows = 128;
 // Head dims served by the CTA-pair kernel (prefill_pair.cu); there each CTA
 // loads 64 of the 128 K rows of a tile, so the K map's box is 64 rows high.
 // d = 256 runs faster on pairs (1.6 PFLOP/s against 1.24 on the head-dim
-// sweep); d = 128 runs faster on single CTAs with two query tiles, so its pair
-// instantiation is built only when ATTN_PREFILL_PAIR_D128 is defined to 1.
-#ifndef ATTN_PREFILL_PAIR_D128
-#define ATTN_PREFILL_PAIR_D128 0
-#endif
-constexpr bool prefill_uses_pair(int d) { return d == 256 || (ATTN_PREFILL_PAIR_D128 && d == 128); }
+// sweep); d = 128 runs faster on single CTAs with two query tiles.
+constexpr bool prefill_uses_pair(int d) { return d == 256; }
 constexpr int prefill_k_box_rows(int d) { return prefill_uses_pair(d) ? kPrefillKVStageRows / 2 : kPrefillKVStageRows; }
+
+// Host-side argument rules of attn_decode_split and attn_merge (ATTN_OK, or the
+// status the entry point returns).  check_parts / check_partials = false skips the
+// partial buffers (part_o, part_lse), which attn_decode_noalloc supplies itself.
+int check_decode_split_args(const void* q, const void* kcache, const void* vcache, const int* kv_lens,
+                            int B, int Hq, int Hkv, int d, int max_kv, float scale, int n_splits,
+                            int min_rows, const void* part_o, const void* part_lse, bool check_parts);
+int check_merge_args(const void* part_o, const void* part_lse, const void* o, const void* lse, int B,
+                     int Hq, int n_splits, int d, int o_dtype, bool check_partials);
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill_pair(const PrefillArgs& a, cudaStream_t stream);
+// Head dimension 512 (prefill_d512.cu): fixed-length batches, causal or not; O in
+// two column halves (S recomputed for the second).
+cudaError_t launch_prefill_d512(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill_empty_kv(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_decode_split(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);

@@ -64,11 +64,7 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when m 
 template <int D, bool H = false>
 struct PrefillCfg {
   static constexpr int NQ = (D <= 128) ? 2 : 1;            // query tiles per CTA
-#ifndef ATTN_PREFILL_NS
   static constexpr int NS = (D == 256) ? 2 : 1;            // S buffers per query tile
-#else
-  static constexpr int NS = ATTN_PREFILL_NS;
-#endif
   // rows of a K / V tile (S has BN columns): TMEM holds NQ O tiles of d columns
   // and NQ*NS S buffers of BN columns
   static constexpr int BN = (NQ * D + NQ * NS * 128 <= 512) ? 128 : 64;
@@ -80,16 +76,8 @@ struct PrefillCfg {
   static constexpr int kSubBytes = BN * 128;               // offset of tile h of a stage in a panel
   static constexpr int kQTileBytes = kPanels * kQPanelBytes;
   static constexpr int kKVStageBytes = kPanels * kKVPanelBytes;
-#ifndef ATTN_PREFILL_KSTAGES
   static constexpr int kStagesK = (D == 64) ? (H ? 5 : 4) : (D == 128 ? (H ? 3 : 2) : 1);  // K ring depth
-#else
-  static constexpr int kStagesK = ATTN_PREFILL_KSTAGES;
-#endif
-#ifndef ATTN_PREFILL_VSTAGES
   static constexpr int kStagesV = (D == 64) ? 4 : (D == 128 ? 2 : 1);  // V ring depth
-#else
-  static constexpr int kStagesV = ATTN_PREFILL_VSTAGES;
-#endif
   static constexpr int kQTiles = H ? 1 : NQ;               // Q tiles in shared memory
   // K tiles the producer may issue ahead of V: the MMA warp needs K of the next
   // tile (item) before V of the current one; key halves stream from HBM and run further

@@ -1,7 +1,6 @@
 // prefill_pair.cu -- exact attention forward (FMHA) on CTA pairs: one tcgen05
-// MMA of M = 256 serves the query tiles of two CTAs.  Used for head dim 256;
-// the head-dim-128 instantiation is built for experiments only (see
-// prefill_uses_pair in internal.h).
+// MMA of M = 256 serves the query tiles of two CTAs.  Used for head dim 256
+// (head dim 128 runs faster on single CTAs with two query tiles, prefill.cu).
 //
 // A cluster of two CTAs takes 256 query rows of one (batch, query head); CTA r
 // holds rows [128r, 128r + 128) of them.  Rank 0's MMA warp issues every
@@ -75,14 +74,10 @@ struct PairCfg {
   static constexpr int kVPanels = D / 128;                 // V panels (64 columns) held by one CTA
   static constexpr int kVPanelBytes = BN * 128;
   static constexpr int kVStageBytes = kVPanels * kVPanelBytes;
-#ifndef ATTN_PAIR_SOFTMAX_WG
   // softmax warpgroups per CTA: two 64-column slices (four 32-column slices were
   // measured no faster at d = 128, and at d = 256 the larger O share of a
   // warpgroup does not fit the four-warpgroup register budget)
   static constexpr int NWG = 2;
-#else
-  static constexpr int NWG = ATTN_PAIR_SOFTMAX_WG;
-#endif
   static constexpr int kCols = BN / NWG;                   // S columns (keys) per warpgroup
   static_assert(kCols == 32 || kCols == 64, "one or two 32-column TMEM loads per tile");
   static constexpr int kStagesK = (D == 128) ? 3 : 2;
@@ -550,451 +545,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<D>::kThreads
   }
 }
 
-#if ATTN_PREFILL_PAIR_D128
-// ---------------------------------------------------------------------------
-// d = 128 on CTA pairs with independent key slices (built with
-// ATTN_PREFILL_PAIR_D128=1 only: 1,071 TFLOP/s on the head-dim-128 sweep against
-// the single-CTA kernel's 1,115; its MMA warp spends ~900 cycles per 128-key tile
-// on barrier waits and commits, against 1,024 cycles of MMA work).
-//
-// The two softmax warpgroups of a CTA own the key slices [0, 64) and [64, 128)
-// of every S tile, each with its own running max, row sums and O accumulator
-// (O_0 and O_1 in TMEM), so they never wait for each other inside the KV loop;
-// per KV tile the MMA warp issues S(j+1), then P_0(j).V_0(j) into O_0 and
-// P_1(j).V_1(j) into O_1 (each over its 64 keys).  At the end the two partial
-// results of every row are merged with their maxima and sums, as two splits of
-// the key range.  TMEM: O_0 [0, 128), O_1 [128, 256), S buffers at 256 and 384.
-struct SliceCfg {
-  static constexpr int D = 128;
-  static constexpr int BN = kPrefillKVStageRows;       // keys per KV tile
-  static constexpr int NS = 2;                         // S buffers
-  static constexpr int NSL = 2;                        // key slices = softmax warpgroups
-  static constexpr int KC = BN / NSL;                  // keys per slice
-  static constexpr int kPanels = D / 64;
-  static constexpr int kQPanelBytes = kPrefillTileM * 128;
-  static constexpr int kQBytes = kPanels * kQPanelBytes;
-  static constexpr int kKRows = BN / 2;
-  static constexpr int kKPanelBytes = kKRows * 128;
-  static constexpr int kKStageBytes = kPanels * kKPanelBytes;
-  static constexpr int kVPanels = D / 128;
-  static constexpr int kVPanelBytes = BN * 128;
-  static constexpr int kVStageBytes = kVPanels * kVPanelBytes;
-  static constexpr int kStagesK = 3, kStagesV = 3;  // 4 and 5 stages measured no faster
-  static constexpr int kQOff = 0;
-  static constexpr int kKOff = kQOff + kQBytes;
-  static constexpr int kVOff = kKOff + kStagesK * kKStageBytes;
-  static constexpr int kRedOff = kVOff + kStagesV * kVStageBytes;
-  static constexpr int kRedBytes = 3 * NSL * 128 * 4;   // final (m, l, l_rnd) per slice and row
-  static constexpr int kBarOff = kRedOff + kRedBytes;
-  // barriers: fullQ, fullK[SK], emptyK[SK], fullV[SV], emptyV[SV], S[NS], P[NS][NSL], O[NSL], Fin
-  static constexpr int kNumBars = 1 + 2 * kStagesK + 2 * kStagesV + NS + NS * NSL + NSL + 1;
-  static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;
-  static constexpr int kThreads = 12 * 32;
-  static constexpr int kMmaWarp = 8, kTmaWarp = 9;
-  static constexpr int kSoftmaxRegs = 208, kCtlRegs = 80;
-  static_assert((8 * kSoftmaxRegs + 4 * kCtlRegs) * 32 <= kThreads * 168, "register split");
-  static constexpr uint32_t kTmemCols = 512;
-  __host__ __device__ static constexpr uint32_t o_col(int h) { return (uint32_t)(h * D); }
-  __host__ __device__ static constexpr uint32_t s_col(int buf) { return (uint32_t)(NSL * D + buf * BN); }
-  static_assert(NSL * D + NS * BN <= 512, "TMEM budget");
-  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
-  static constexpr uint32_t kPArrivals = 8;  // the 4 warps of a slice in each CTA
-};
-
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(SliceCfg::kThreads, 1)
-    fmha_pair_slices_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                            const __grid_constant__ CUtensorMap tm_v, void* __restrict__ o_ptr,
-                            float* __restrict__ lse_ptr, int Hq, int Hkv, int Sq_max, int Skv_max, int causal,
-                            int o_bf16, float scale, int n_units_per_head_batch, uint32_t* err,
-                            const int* __restrict__ cu_q, const int* __restrict__ kv_lens, int total_q) {
-  using C = SliceCfg;
-  constexpr int D = C::D, BN = C::BN, NS = C::NS, NSL = C::NSL, KC = C::KC;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();
-
-  const int HB = n_units_per_head_batch;
-  const int n_blocks_q = (Sq_max + 2 * kPrefillTileM - 1) / (2 * kPrefillTileM);
-  const int pair = blockIdx.x >> 1;
-  // causal: heaviest query blocks first; non-causal: the query blocks of one head
-  // are neighbours, so that head's K/V stay in L2 while they run
-  const int qb = causal ? (n_blocks_q - 1 - pair / HB) : (pair % n_blocks_q);
-  const int hb = causal ? pair % HB : pair / n_blocks_q;
-  const int hq = hb % Hq, b = hb / Hq;
-  const int hk = hq / (Hq / Hkv);
-  // this sequence's query rows and keys (fixed-length or packed varlen batch)
-  const SeqExtent ext = seq_extent(b, Sq_max, Skv_max, cu_q, kv_lens, total_q);
-  const int Sq = ext.Sq, Skv = ext.Skv;
-  const int q0_pair = qb * 2 * kPrefillTileM;
-  const int q0 = q0_pair + (int)rank * kPrefillTileM;
-  const long long off = (long long)Skv - Sq;
-  int n_kv;
-  {
-    int kv_hi = Skv;
-    if (causal) {
-      const long long q_last = (long long)min(Sq, q0_pair + 2 * kPrefillTileM) - 1;
-      const long long hi = q_last + off + 1;
-      kv_hi = (int)(hi < 0 ? 0 : (hi > Skv ? Skv : hi));
-    }
-    n_kv = (kv_hi + BN - 1) / BN;
-    if (q0_pair >= Sq) n_kv = 0;  // a q-block past the end of this sequence (varlen)
-  }
-  int kv_lo = Skv;
-  if (causal) {
-    const long long lo = (long long)q0 + off + 1;
-    kv_lo = (int)(lo < 0 ? 0 : (lo > Skv ? Skv : lo));
-  }
-
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
-  uint8_t* sQ = smem + C::kQOff;
-  uint8_t* sK = smem + C::kKOff;
-  uint8_t* sV = smem + C::kVOff;
-  float* red = reinterpret_cast<float*>(smem + C::kRedOff);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
-  uint64_t* bar_q = bars;
-  uint64_t* bar_fullK = bars + 1;
-  uint64_t* bar_emptyK = bar_fullK + C::kStagesK;
-  uint64_t* bar_fullV = bar_emptyK + C::kStagesK;
-  uint64_t* bar_emptyV = bar_fullV + C::kStagesV;
-  uint64_t* bar_S = bar_emptyV + C::kStagesV;  // [NS] multicast
-  uint64_t* bar_P = bar_S + NS;                // [NS][NSL] rank 0
-  uint64_t* bar_O = bar_P + NS * NSL;          // [NSL] multicast: one phase per P_h.V_h group
-  uint64_t* bar_Fin = bar_O + NSL;             // multicast
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-
-  if (threadIdx.x == 0) {
-    mbar_init(bar_q, 1);
-    for (int s = 0; s < C::kStagesK; ++s) {
-      mbar_init(&bar_fullK[s], 1);
-      mbar_init(&bar_emptyK[s], 1);
-    }
-    for (int s = 0; s < C::kStagesV; ++s) {
-      mbar_init(&bar_fullV[s], 1);
-      mbar_init(&bar_emptyV[s], 1);
-    }
-    for (int i = 0; i < NS; ++i) mbar_init(&bar_S[i], 1);
-    for (int i = 0; i < NS * NSL; ++i) mbar_init(&bar_P[i], C::kPArrivals);
-    for (int h = 0; h < NSL; ++h) mbar_init(&bar_O[h], 1);
-    mbar_init(bar_Fin, 1);
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
-  if (warp == C::kMmaWarp) {
-    tmem_alloc_pair(tmem_slot, C::kTmemCols);
-    tmem_relinquish_pair();
-  }
-  tc_fence_before();
-  cluster_sync_all();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-
-  if (warp >= 8) {
-    setmaxnreg_dec<C::kCtlRegs>();
-    if (warp == C::kTmaWarp && n_kv > 0) {
-      // =========================== TMA producer ===========================
-      if (lane == 0) {
-        tma_prefetch_desc(&tm_q);
-        tma_prefetch_desc(&tm_k);
-        tma_prefetch_desc(&tm_v);
-      }
-      if (rank == 0) mbar_arrive_expect_tx_e(bar_q, 2 * C::kQBytes);
-      const uint32_t q_leader = mapa_shared(smem_u32(bar_q), 0);
-#pragma unroll
-      for (int p = 0; p < C::kPanels; ++p)
-        tma_load_4d_pair_e(sQ + p * C::kQPanelBytes, &tm_q, q_leader, p * 64, hq, ext.qbase + q0, ext.bq);
-      int jk = 0, jv = 0;
-      bool aborted = false;
-      while (jv < n_kv) {
-        if (jk < n_kv && jk <= jv + 1) {
-          const int s = jk % C::kStagesK;
-          const uint32_t ph = (uint32_t)(jk / C::kStagesK) & 1u;
-          if (!mbar_wait_cl_warp(&bar_emptyK[s], ph ^ 1u, err, abort_flag)) { aborted = true; break; }
-          if (rank == 0) mbar_arrive_expect_tx_e(&bar_fullK[s], 2 * C::kKStageBytes);
-          const uint32_t full_leader = mapa_shared(smem_u32(&bar_fullK[s]), 0);
-#pragma unroll
-          for (int p = 0; p < C::kPanels; ++p)
-            tma_load_4d_pair_e(sK + s * C::kKStageBytes + p * C::kKPanelBytes, &tm_k, full_leader, p * 64,
-                               hk, jk * BN + (int)rank * C::kKRows, b);
-          ++jk;
-          continue;
-        }
-        const int s = jv % C::kStagesV;
-        const uint32_t ph = (uint32_t)(jv / C::kStagesV) & 1u;
-        if (!mbar_wait_cl_warp(&bar_emptyV[s], ph ^ 1u, err, abort_flag)) { aborted = true; break; }
-        if (rank == 0) mbar_arrive_expect_tx_e(&bar_fullV[s], 2 * C::kVStageBytes);
-        const uint32_t full_leader = mapa_shared(smem_u32(&bar_fullV[s]), 0);
-#pragma unroll
-        for (int p = 0; p < C::kVPanels; ++p)
-          tma_load_4d_pair_e(sV + s * C::kVStageBytes + p * C::kVPanelBytes, &tm_v, full_leader,
-                             ((int)rank * C::kVPanels + p) * 64, hk, jv * BN, b);
-        ++jv;
-      }
-      if (aborted) {
-        const long long t0 = clock64();  // let issued copies land (their bytes go to rank 0's barriers)
-        while (clock64() - t0 < 2000000ll) {
-        }
-      }
-    } else if (warp == C::kMmaWarp && rank == 0 && n_kv > 0) {
-      // =========================== MMA issuer (rank 0) ===========================
-      constexpr uint32_t idesc_s = idesc_bf16_f32(256, BN, 0, 0);
-      constexpr uint32_t idesc_o = idesc_bf16_f32(256, D, 0, 1);
-      const uint64_t dq = smem_desc(smem_u32(sQ), 16, 1024, kSwizzle128B);
-      const uint64_t dk0 = smem_desc(smem_u32(sK), 16, 1024, kSwizzle128B);
-      const uint64_t dv0 = smem_desc(smem_u32(sV), C::kVPanelBytes, 1024, kSwizzle128B);
-      bool ok = mbar_wait_cl_warp(bar_q, 0, err, abort_flag);
-      tc_fence_after();
-      auto issue_s = [&](int j) {
-        const uint64_t dk = dk0 + (uint64_t)(((j % C::kStagesK) * C::kKStageBytes) >> 4);
-        const uint32_t d_tmem = tmem + C::s_col(j % NS);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t offq = (uint64_t)(((kk >> 2) * C::kQPanelBytes + (kk & 3) * 32) >> 4);
-          const uint64_t offk = (uint64_t)(((kk >> 2) * C::kKPanelBytes + (kk & 3) * 32) >> 4);
-          mma2_ss_e(d_tmem, dq + offq, dk + offk, idesc_s, kk > 0 ? 1u : 0u);
-        }
-        mma2_commit_both_e(&bar_S[j % NS]);
-      };
-      if (ok) {
-        ok = mbar_wait_cl_warp(&bar_fullK[0], 0, err, abort_flag);
-        tc_fence_after();
-        if (ok) {
-          issue_s(0);
-          mma2_commit_both_e(&bar_emptyK[0]);
-        }
-      }
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int jn = j + 1;
-        if (jn < n_kv) {
-          const int sn = jn % C::kStagesK;
-          if (!mbar_wait_cl_warp(&bar_fullK[sn], (uint32_t)(jn / C::kStagesK) & 1u, err, abort_flag)) break;
-          tc_fence_after();
-          issue_s(jn);
-          mma2_commit_both_e(&bar_emptyK[sn]);
-        }
-        const int s = j % C::kStagesV;
-        if (!mbar_wait_cl_warp(&bar_fullV[s], (uint32_t)(j / C::kStagesV) & 1u, err, abort_flag)) break;
-        tc_fence_after();
-        const int buf = j % NS;
-        const uint64_t dv = dv0 + (uint64_t)((s * C::kVStageBytes) >> 4);
-#pragma unroll
-        for (int h = 0; h < NSL; ++h) {
-          // P_h(j).V_h(j): the slice's 64 keys, A = its P columns, B = its 64 rows of V
-          if (!mbar_wait_cl_warp(&bar_P[buf * NSL + h], (uint32_t)(j / NS) & 1u, err, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t p_tmem = tmem + C::s_col(buf) + KC * h;
-#pragma unroll
-          for (int kk = 0; kk < KC / 16; ++kk)
-            mma2_ts_e(tmem + C::o_col(h), p_tmem + 8 * kk,
-                      dv + (uint64_t)(((h * (KC / 16) + kk) * 2048) >> 4), idesc_o,
-                      (j > 0 || kk > 0) ? 1u : 0u);
-          mma2_commit_both_e(&bar_O[h]);
-        }
-        if (!ok) break;
-        if (j == n_kv - 1) mma2_commit_both_e(bar_Fin);
-        mma2_commit_both_e(&bar_emptyV[s]);
-      }
-    }
-  } else {
-    // =========================== softmax: one warpgroup per key slice ===========================
-    setmaxnreg_inc<C::kSoftmaxRegs>();
-    const int h = warp >> 2;
-    const int wq = warp & 3;
-    const int r = wq * 32 + lane;
-    const int qrow = q0 + r;
-    const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
-    const float sl2 = scale * kLog2e;
-    int row_bound = Skv;
-    if (causal) {
-      const long long rb = (long long)qrow + off + 1;
-      row_bound = (int)(rb < 0 ? 0 : (rb > Skv ? Skv : rb));
-    }
-    float m_used = -INFINITY, l = 0.f, l_rnd = 0.f;
-    bool ok = true;
-    for (int j = 0; j < n_kv && ok; ++j) {
-      const int buf = j % NS;
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait_cl(&bar_S[buf], (uint32_t)(j / NS) & 1u, err, abort_flag))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t s_addr = lane_addr + C::s_col(buf) + KC * h;
-      uint32_t sr[KC];
-#pragma unroll
-      for (int c0 = 0; c0 < KC; c0 += 32) tmem_ld32(s_addr + c0, sr + c0);
-      tmem_wait_ld();
-      const int key0 = j * BN + KC * h;
-      if (key0 + KC > kv_lo) {
-        const int lim = row_bound - key0;
-#pragma unroll
-        for (int c = 0; c < KC; ++c)
-          if (c >= lim) sr[c] = __float_as_uint(-INFINITY);
-      }
-      float mx[4];
-#pragma unroll
-      for (int a = 0; a < 4; ++a)
-        mx[a] = max3f(__uint_as_float(sr[3 * a]), __uint_as_float(sr[3 * a + 1]), __uint_as_float(sr[3 * a + 2]));
-#pragma unroll
-      for (int c = 12; c < KC; c += 2)
-        mx[(c >> 1) & 3] = max3f(mx[(c >> 1) & 3], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
-      const float m_tile = fmaxf(max3f(mx[0], mx[1], mx[2]), mx[3]) * sl2;
-      const float m_new = fmaxf(m_used, m_tile);
-      const bool need = m_new > m_used + kRescaleThreshold;
-      if (__any_sync(0xFFFFFFFFu, need)) {
-        const float corr = need ? ex2_approx(m_used - m_new) : 1.f;
-        if (need) {
-          l *= corr;
-          l_rnd *= corr;
-          m_used = m_new;
-        }
-        if (j > 0) {
-          // O_h must hold P_h(j-1) V_h(j-1) before it is rescaled
-          if (!__all_sync(0xFFFFFFFFu, mbar_wait_cl(&bar_O[h], (uint32_t)(j - 1) & 1u, err, abort_flag))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t o_addr = lane_addr + C::o_col(h);
-#pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t ov[32];
-            tmem_ld32(o_addr + c0, ov);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * corr);
-            tmem_st32(o_addr + c0, ov);
-          }
-          tmem_wait_st();
-        }
-      }
-      const float msub = (m_used == -INFINITY) ? 0.f : m_used;
-      const uint64_t sl2x2 = f2pack(sl2, sl2), nmx2 = f2pack(-msub, -msub);
-      uint64_t lex2 = f2pack(0.f, 0.f);
-      float lrd0 = 0.f, lrd1 = 0.f;
-      uint32_t pk[KC / 2];
-#pragma unroll
-      for (int e = 0; e < KC / 2; ++e) {
-        const uint64_t x2 = fma2(f2pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), sl2x2, nmx2);
-        float x0, x1;
-        f2unpack(x2, x0, x1);
-        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-        pk[e] = pack_bf16x2(p0, p1);
-        lex2 = add2(lex2, f2pack(p0, p1));
-        add_bf16x2_f32(pk[e], lrd0, lrd1);
-      }
-      {
-        float a0, a1;
-        f2unpack(lex2, a0, a1);
-        l += a0 + a1;
-        l_rnd += lrd0 + lrd1;
-      }
-      tmem_st32(s_addr, pk);  // P_h: bf16 pairs over the first KC/2 columns of the slice
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if (rank == 0) mbar_arrive(&bar_P[buf * NSL + h]);
-        else mbar_arrive_cluster(mapa_shared(smem_u32(&bar_P[buf * NSL + h]), 0));
-      }
-    }
-
-    // ---- epilogue: merge the two slices' partial results of every row ----
-    if (ok && n_kv > 0) {
-      ok = __all_sync(0xFFFFFFFFu, mbar_wait_cl(bar_Fin, 0, err, abort_flag));
-      tc_fence_after();
-    }
-    ok = __all_sync(0xFFFFFFFFu, ok);
-    red[(0 * NSL + h) * 128 + r] = m_used;
-    red[(1 * NSL + h) * 128 + r] = l;
-    red[(2 * NSL + h) * 128 + r] = l_rnd;
-    asm volatile("bar.sync 1, 256;" ::: "memory");  // the 8 softmax warps
-    float M = -INFINITY;
-#pragma unroll
-    for (int g = 0; g < NSL; ++g) M = fmaxf(M, red[g * 128 + r]);
-    float f[NSL];
-    float L = 0.f, Lr = 0.f;
-#pragma unroll
-    for (int g = 0; g < NSL; ++g) {
-      const float mg = red[g * 128 + r];
-      f[g] = (mg == -INFINITY) ? 0.f : ex2_approx(mg - M);
-      L = fmaf(red[(NSL + g) * 128 + r], f[g], L);
-      Lr = fmaf(red[(2 * NSL + g) * 128 + r], f[g], Lr);
-    }
-    const bool load_o = ok && n_kv > 0;
-    const bool have = load_o && L > 0.f;
-    const float inv_l = have ? 1.f / Lr : 0.f;
-    const bool row_ok = qrow < Sq;
-    const size_t orow = ((size_t)ext.bq * ext.rows + ext.qbase + (size_t)(row_ok ? qrow : 0)) * Hq + hq;
-    // warpgroup h stores the output columns [64h, 64h + 64): f_0 O_0 + f_1 O_1, over Lr
-#pragma unroll
-    for (int c0 = 0; c0 < D / NSL; c0 += 32) {
-      const int col = h * (D / NSL) + c0;
-      float acc[32];
-#pragma unroll
-      for (int e = 0; e < 32; ++e) acc[e] = 0.f;
-      if (load_o) {
-#pragma unroll
-        for (int g = 0; g < NSL; ++g) {
-          uint32_t ov[32];
-          tmem_ld32(lane_addr + C::o_col(g) + col, ov);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) acc[e] = fmaf(__uint_as_float(ov[e]), f[g], acc[e]);
-        }
-      }
-      if (row_ok && ok) {
-        if (o_bf16) {
-          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(o_ptr) + orow * D + col);
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint4 w;
-            w.x = pack_bf16x2(acc[8 * q4 + 0] * inv_l, acc[8 * q4 + 1] * inv_l);
-            w.y = pack_bf16x2(acc[8 * q4 + 2] * inv_l, acc[8 * q4 + 3] * inv_l);
-            w.z = pack_bf16x2(acc[8 * q4 + 4] * inv_l, acc[8 * q4 + 5] * inv_l);
-            w.w = pack_bf16x2(acc[8 * q4 + 6] * inv_l, acc[8 * q4 + 7] * inv_l);
-            dst[q4] = w;
-          }
-        } else {
-          float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(o_ptr) + orow * D + col);
-#pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4)
-            dst[q4] = make_float4(acc[4 * q4 + 0] * inv_l, acc[4 * q4 + 1] * inv_l, acc[4 * q4 + 2] * inv_l,
-                                  acc[4 * q4 + 3] * inv_l);
-        }
-      }
-    }
-    if (h == 0 && row_ok && ok)
-      lse_ptr[((size_t)ext.bq * Hq + hq) * ext.rows + ext.qbase + qrow] = have ? (M + log2f(L)) * kLn2 : -INFINITY;
-  }
-
-  tc_fence_before();
-  cluster_sync_all();
-  if (warp == C::kMmaWarp) {
-    tc_fence_after();
-    tmem_dealloc_pair(tmem, C::kTmemCols);
-  }
-}
-
-cudaError_t launch_pair_slices(const PrefillArgs& a, cudaStream_t stream) {
-  using C = SliceCfg;
-  auto kern = fmha_pair_slices_kernel;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-  if (e != cudaSuccess) return e;
-  const int n_blocks_q = (a.Sq + 2 * kPrefillTileM - 1) / (2 * kPrefillTileM);
-  const long long units = (long long)n_blocks_q * a.Hq * a.B;
-  if (units <= 0) return cudaSuccess;
-  if (2 * units > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-  kern<<<(unsigned)(2 * units), C::kThreads, C::kSmemBytes, stream>>>(
-      a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, a.Hq, a.Hkv, a.Sq, a.Skv, a.causal, a.o_bf16, a.scale,
-      a.Hq * a.B, a.err, a.cu_q, a.kv_lens, a.total_q);
-  return cudaGetLastError();
-}
-#endif  // ATTN_PREFILL_PAIR_D128
-
 template <int D>
 cudaError_t launch_pair_t(const PrefillArgs& a, cudaStream_t stream) {
   using C = PairCfg<D>;
@@ -1015,9 +565,6 @@ cudaError_t launch_pair_t(const PrefillArgs& a, cudaStream_t stream) {
 
 cudaError_t launch_prefill_pair(const PrefillArgs& a, cudaStream_t stream) {
   switch (a.d) {
-#if ATTN_PREFILL_PAIR_D128
-    case 128: return launch_pair_slices(a, stream);
-#endif
     case 256: return launch_pair_t<256>(a, stream);
     default: return cudaErrorInvalidValue;
   }

@@ -28,7 +28,8 @@ constexpr double kMaxSmClockGHz = 2.07;
 enum : uint32_t {
   kErrNone = 0,
   kErrWaitTimeout = 1,  // an mbarrier wait ran out of time
-  kErrBadShape = 2,     // kernel-side shape check failed
+  kErrBadShape = 2,     // kernel-side shape check failed: a device-side input (kv_lens)
+                        // disagrees with what the launch was sized or ordered for
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

@@ -12,7 +12,7 @@ Workloads (names used throughout the tests and the benchmark):
 * ``gqa_prefill_3314``  B=1, Hq=28, Hkv=4, Sq=Skv=3314, d=128, causal, scale 1/sqrt(128), O bf16
 * ``gqa_decode_1641``   B=1, Hq=28, Hkv=4, one query token, KV length 1641, d=128,
                         8 splits (min 1 row per split), merged to O bf16 + LSE fp32
-* ``mha_noncausal_4096_d{64,128,256}``  B=2, Hq=Hkv=16, S=4096, non-causal, scale 1/sqrt(d)
+* ``mha_noncausal_4096_d{64,128,256,512}``  B=2, Hq=Hkv=16, S=4096, non-causal, scale 1/sqrt(d)
 * ``ragged_gqa_decode_b64`` B=64, Hq=32, Hkv=8, d=128, KV lengths ~ U[512, 8192],
                         at most 4 splits of at least 1536 rows each (1 to 4 per
                         sequence, chosen by its length), O bf16 + LSE fp32
@@ -71,6 +71,8 @@ GQA_DECODE = DecodeShape("gqa_decode_1641", 1, 28, 4, 128, 1.0 / math.sqrt(128.0
 
 
 def mha_sweep(d: int) -> PrefillShape:
+    """The non-causal head-dim sweep (B=2, H=16, S=4096) at head dim d: 64, 128 and
+    256 are the configured sweep, 512 extends it to the widest head the prefill takes."""
     return PrefillShape(f"mha_noncausal_4096_d{d}", 2, 16, 16, 4096, 4096, d, False,
                         1.0 / math.sqrt(float(d)), "bf16", 1000 + 4 * 10 + d // 64)
 

@@ -5,6 +5,10 @@ One step = one pass of the whole hot path over one batch of synthetic input:
   1. prefill FMHA on gqa_prefill_3314  (B=1, Hq=28, Hkv=4, S=3314, d=128, causal, O bf16)
   2. split-KV decode + merge on gqa_decode_1641 (B=1, Hq=28, Hkv=4, KV 1641, 8 splits)
   3. split-KV decode + merge on ragged_gqa_decode_b64 (B=64, Hq=32, Hkv=8, KV ~ U[512,8192])
+Beside the step, each further workload is timed alone and reported on its own
+line object: chunked (varlen) prefill, the sliding window with sinks, the
+128-head multi-query decode and the non-causal head-dim sweep (B=2, H=16,
+S=4096, d = 64, 128, 256, and 512).
 L2 is flushed (a 256 MiB device write) before every step, outside the kernel
 events.  `value` is the prefill throughput in TFLOP/s (algorithmic FLOPs:
 4*d per admissible (query, key) pair); the decode throughput (algorithmic K+V
@@ -123,8 +127,8 @@ def run_line(args):
     """One extra workload line alone (--line), for profiling its kernel."""
     import torch
 
-    import attn_forward_tcgen05_gb300 as attn
-    from attn_forward_tcgen05_gb300 import workloads as W
+    import attention_forward_tcgen05_gb300 as attn
+    from attention_forward_tcgen05_gb300 import workloads as W
 
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
@@ -132,6 +136,8 @@ def run_line(args):
     peaks, peak_src = load_peaks()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
+    if args.line.startswith("sweep"):
+        return time_sweep(args, attn, W, dev, stream, flush, peaks, peak_src, int(args.line[5:]))
     fn = {"varlen": time_varlen, "window": time_window, "mqa": time_mqa_decode}[args.line]
     return fn(args, attn, W, dev, stream, flush, peaks, peak_src)
 
@@ -139,8 +145,8 @@ def run_line(args):
 def run_ours(args, rank, world, local_rank):
     import torch
 
-    import attn_forward_tcgen05_gb300 as attn
-    from attn_forward_tcgen05_gb300 import workloads as W
+    import attention_forward_tcgen05_gb300 as attn
+    from attention_forward_tcgen05_gb300 import workloads as W
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
@@ -242,6 +248,9 @@ def run_ours(args, rank, world, local_rank):
     window = None if args.only else time_window(args, attn, W, dev, stream, flush, peaks, peak_src)
     # ---- multi-query decode on the tensor cores (heads packed into the tile rows) ----
     mqa = None if args.only else time_mqa_decode(args, attn, W, dev, stream, flush, peaks, peak_src)
+    # ---- non-causal head-dim sweep (B = 2, H = 16, S = 4096; d = 64, 128, 256) ----
+    sweep = None if args.only else [time_sweep(args, attn, W, dev, stream, flush, peaks, peak_src, d)
+                                    for d in (64, 128, 256, 512)]
 
     # ---- end to end through the public API with host buffers ----
     e2e = None if (args.no_e2e or args.only) else run_e2e(args, attn, W, dev, stream, P, dec, flops)
@@ -258,7 +267,7 @@ def run_ours(args, rank, world, local_rank):
     traffic = load_traffic()
     # one roofline per hot kernel; the top-level one is the kernel that takes the
     # largest share of the step's device time
-    pkern = f"fmha_pair_kernel<{P.d}>" if P.d == 256 else f"fmha_fwd_kernel<{P.d}>"
+    pkern = prefill_kernel_name(P.d)
     prefill_roof = {"bound": "tensor", "kernel": pkern, "workload": P.name,
                     "achieved": round(prefill_tflops / world, 2), "peak": peak_tc,
                     "unit": "TFLOP/s", "frac": round(prefill_tflops / world / peak_tc, 4),
@@ -319,6 +328,7 @@ def run_ours(args, rank, world, local_rank):
         "prefill_varlen": varlen,
         "prefill_window": window,
         "decode_packed": mqa,
+        "prefill_headdim_sweep": sweep,
         "clocks": clocks,
     }
     return line
@@ -393,7 +403,7 @@ def time_window(args, attn, W, dev, stream, flush, peaks, peak_src):
     ms = sum(a.elapsed_time(b) for a, b in evs) / n
     tf = flops / (ms * 1e-3) / 1e12
     peak_tc = float(peaks["bf16_tflops"])
-    kern = f"fmha_pair_kernel<{P.d}>" if P.d == 256 else f"fmha_fwd_kernel<{P.d}>"
+    kern = prefill_kernel_name(P.d)
     return {"workload": S.name, "B": P.B, "Hq": P.Hq, "Hkv": P.Hkv, "S": P.Sq, "d": P.d,
             "window": S.window, "n_sink": S.n_sink, "gflop": round(flops / 1e9, 3),
             "us": round(ms * 1e3, 2), "value": round(tf, 2), "unit": "TFLOP/s", "steps": n,
@@ -401,6 +411,58 @@ def time_window(args, attn, W, dev, stream, flush, peaks, peak_src):
                          "peak": peak_tc, "unit": "TFLOP/s", "frac": round(tf / peak_tc, 4),
                          "traffic": load_traffic().get(f"{kern} window {S.name}"),
                          "peak_source": f"bf16_tflops (burst) of {peak_src}"}}
+
+
+def time_sweep(args, attn, W, dev, stream, flush, peaks, peak_src, d):
+    """Non-causal MHA prefill of the head-dim sweep (B = 2, H = 16, S = 4096, bf16 O)
+    at head dim d: average launch time of attn_prefill_fwd over the timed
+    iterations, L2 flushed before each."""
+    import torch
+
+    P = W.mha_sweep(d)
+    q, k, v = (t.to(dev) for t in W.prefill_inputs_for(P))
+    flops = W.prefill_flops(P.B, P.Hq, P.Sq, P.Skv, P.d, P.causal)
+    o = torch.empty((P.B, P.Sq, P.Hq, P.d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((P.B, P.Hq, P.Sq), dtype=torch.float32, device=dev)
+
+    def call():
+        attn.prefill(q, k, v, causal=P.causal, scale=P.scale, out=(o, lse))
+
+    for _ in range(args.warmup):
+        call()
+    n = max(1, min(args.steps, 50))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for a, b in evs:
+        flush.zero_()
+        a.record(stream)
+        call()
+        b.record(stream)
+    torch.cuda.synchronize()
+    attn.sync_check()
+    ms = sum(a.elapsed_time(b) for a, b in evs) / n
+    tf = flops / (ms * 1e-3) / 1e12
+    peak_tc = float(peaks["bf16_tflops"])
+    kern = prefill_kernel_name(P.d)
+    line = {"workload": P.name, "B": P.B, "Hq": P.Hq, "Hkv": P.Hkv, "S": P.Sq, "d": P.d,
+            "causal": P.causal, "gflop": round(flops / 1e9, 3), "us": round(ms * 1e3, 2),
+            "value": round(tf, 2), "unit": "TFLOP/s", "steps": n,
+            "roofline": {"bound": "tensor", "kernel": kern, "achieved": round(tf, 2), "peak": peak_tc,
+                         "unit": "TFLOP/s", "frac": round(tf / peak_tc, 4),
+                         "traffic": load_traffic().get(f"{kern} {P.name}"),
+                         "peak_source": f"bf16_tflops (burst) of {peak_src}"}}
+    if P.d == 512:
+        # O is computed in two column halves and S = QK^T once per half: the tensor
+        # cores execute 6*d FLOPs per pair, 1.5x the algorithmic 4*d counted above
+        line["executed_gflop"] = round(1.5 * flops / 1e9, 3)
+        line["executed_tflops"] = round(1.5 * tf, 2)
+    return line
+
+
+def prefill_kernel_name(d: int) -> str:
+    """The kernel that runs a fixed-length prefill of head dim d."""
+    if d == 512:
+        return "fmha_d512_kernel"
+    return f"fmha_pair_kernel<{d}>" if d == 256 else f"fmha_fwd_kernel<{d}>"
 
 
 def time_mqa_decode(args, attn, W, dev, stream, flush, peaks, peak_src):
@@ -515,9 +577,9 @@ def run_e2e(args, attn, W, dev, stream, P, dec, flops):
 def prefill_workload(name: str):
     """The prefill workload of the step: gqa_prefill_3314 by default; the head-dim
     sweep shapes are selectable for profiling their kernels."""
-    from attn_forward_tcgen05_gb300 import workloads as W
+    from attention_forward_tcgen05_gb300 import workloads as W
     shapes = {W.GQA_PREFILL.name: W.GQA_PREFILL}
-    for d in (64, 128, 256):
+    for d in (64, 128, 256, 512):
         shapes[W.mha_sweep(d).name] = W.mha_sweep(d)
     if name not in shapes:
         raise SystemExit(f"unknown prefill workload {name!r}; one of {sorted(shapes)}")
@@ -544,7 +606,7 @@ def _oracle_sampler():
     import torch
 
     import oracle
-    from attn_forward_tcgen05_gb300 import workloads as W
+    from attention_forward_tcgen05_gb300 import workloads as W
 
     P = W.GQA_PREFILL
     q, k, v = W.prefill_inputs_for(P)
@@ -585,7 +647,7 @@ def run_reference(args, rank, world):
     few minutes whatever --steps and --warmup are."""
     if rank != 0:
         return None
-    from attn_forward_tcgen05_gb300 import workloads as W
+    from attention_forward_tcgen05_gb300 import workloads as W
     P = W.GQA_PREFILL
     sampler = _oracle_sampler()
     step_budget = max(0.05, REFERENCE_BUDGET_S / (args.steps + 0.25 * args.warmup))
@@ -623,7 +685,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--only", choices=("prefill", "decode"), default=None,
                     help="time only one part of the step (profiling runs)")
-    ap.add_argument("--line", choices=("varlen", "window", "mqa"), default=None,
+    ap.add_argument("--line", choices=("varlen", "window", "mqa", "sweep64", "sweep128", "sweep256", "sweep512"),
+                    default=None,
                     help="time only one of the extra workload lines and print it (profiling runs)")
     ap.add_argument("--prefill-workload", default="gqa_prefill_3314",
                     help="prefill workload of the step (the head-dim sweep shapes are for profiling)")
@@ -668,7 +731,7 @@ def main():
 
 
 def W_name():
-    from attn_forward_tcgen05_gb300 import workloads as W
+    from attention_forward_tcgen05_gb300 import workloads as W
     return W.GQA_PREFILL.name
 
 

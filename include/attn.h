@@ -45,10 +45,11 @@ typedef struct CUstream_st* attn_stream_t; /* == cudaStream_t */
 /* status codes */
 #define ATTN_OK 0
 #define ATTN_ERR_INVALID_ARG (-1)    /* null/misaligned pointer, bad size, Hq % Hkv != 0, ... */
-#define ATTN_ERR_UNSUPPORTED (-2)    /* head_dim not in {64, 128, 256}, unknown dtype code */
+#define ATTN_ERR_UNSUPPORTED (-2)    /* head_dim not served by the entry point, unknown dtype code */
 #define ATTN_ERR_CUDA (-3)           /* a CUDA runtime/driver call or a launch failed */
 #define ATTN_ERR_DEVICE_TIMEOUT (-4) /* a kernel's bounded wait ran out (attn_sync_check only) */
 #define ATTN_ERR_SCRATCH_TOO_SMALL (-5) /* attn_decode_noalloc: problem exceeds the static scratch */
+#define ATTN_ERR_DEVICE_INPUT (-6)   /* a kernel found device-side inputs changed under it (attn_sync_check only) */
 
 /* output dtype codes */
 #define ATTN_F32 0
@@ -78,7 +79,16 @@ typedef struct CUstream_st* attn_stream_t; /* == cudaStream_t */
  *   lse  fp32 [B][Hq][Sq]
  *   B, Hq, Hkv, Sq, Skv   sizes: B, Sq, Skv >= 0; Hq, Hkv >= 1; Hq % Hkv == 0;
  *                         Sq, Skv < 2^31; every tensor < 2^31 rows of d elements
- *   d                     head dim: 64, 128 or 256
+ *   d                     head dim: 64, 128, 256 or 512.  At 512 the fp32 O of a
+ *                         128-row tile fills all of tensor memory, so O is computed
+ *                         in two column halves by one CTA, S = Q K^T once per half
+ *                         (1.5x the tensor work of the other head dims); the pages'
+ *                         D1.4 of "STAGE_D.md -- FMHA Kernel Development" meets this
+ *                         head dim as a shared-memory limit and splits the head
+ *                         dimension, which the kernel does for Q, K, V and O.  Head
+ *                         dim 512 is served by attn_prefill_fwd only (the window,
+ *                         packed, variable-length and decode entry points return
+ *                         ATTN_ERR_UNSUPPORTED for it)
  *   causal                0 = full attention, else bottom-right causal mask
  *   scale                 softmax scale (finite, > 0), e.g. 1/sqrt(d)
  *   o_dtype               ATTN_F32 or ATTN_BF16
@@ -248,7 +258,8 @@ int attn_prefill_varlen_window(const attn_bf16_t* q, const attn_bf16_t* kcache,
  * Launch order (throughput only, results do not depend on it): the full splits
  * of every sequence start first, then the partial last splits by size, then
  * the empty ones.  Each CTA derives its split from kv_lens, so kv_lens must not
- * change while the call runs.
+ * change while the call runs; a CTA that finds no split at its position (only
+ * possible if it did) records ATTN_ERR_DEVICE_INPUT for attn_sync_check.
  * Follows "66 . D2: explicit K+V register staging", section 3.2 (one split =
  * rows [lo, hi) of one sequence and KV head; score, running max, running sum
  * and running O) and section 2.2 (K and V loads issued ahead of the
@@ -308,12 +319,19 @@ int attn_merge(const float* part_o, const float* part_lse, void* o, float* lse, 
  *
  *  - Limit: B * Hq * n_splits * (d + 1) * 4 bytes (each part rounded up to 256
  *    bytes) must fit in attn_decode_noalloc_scratch_bytes() = 24 MiB; larger
- *    problems return ATTN_ERR_SCRATCH_TOO_SMALL before any launch.
- *  - The array is reserved on every GPU that loads the library and stays
- *    reserved until the process exits.
+ *    problems return ATTN_ERR_SCRATCH_TOO_SMALL before any launch.  The other
+ *    arguments are checked first, by the rules of attn_decode_split and
+ *    attn_merge (a malformed call returns ATTN_ERR_INVALID_ARG or
+ *    ATTN_ERR_UNSUPPORTED whatever its size).
+ *  - The array is part of the library's device code: it is reserved on a GPU
+ *    when that code is first loaded there (with CUDA's default lazy loading,
+ *    at the library's first use on that device, not when the process loads
+ *    the library) and stays reserved until the process exits.
  *  - The first call on a device looks up the array's device address (with that
  *    device current) and caches it; make that first call before any stream
- *    capture.
+ *    capture.  A cudaDeviceReset() invalidates that address and the library's
+ *    other per-device state: do not call the library on a device again in the
+ *    same process after resetting it.
  *  - All calls on a device share the array; each call writes every entry it
  *    later reads, so nothing needs to start at zero, but calls whose work
  *    overlaps on the GPU (e.g. on two streams) race on it.
@@ -332,7 +350,10 @@ unsigned long long attn_decode_noalloc_scratch_bytes(void);
 /*
  * attn_sync_check -- synchronise `stream`, then read and clear this device's
  * error word.  Returns ATTN_OK, ATTN_ERR_DEVICE_TIMEOUT (a kernel's bounded
- * wait gave up; that kernel's outputs are invalid) or ATTN_ERR_CUDA.
+ * wait gave up; that kernel's outputs are invalid), ATTN_ERR_DEVICE_INPUT (a
+ * kernel found a device-side input inconsistent with its launch, e.g. kv_lens
+ * changed while attn_decode_split ran; that call's outputs are invalid) or
+ * ATTN_ERR_CUDA.  The first error recorded since the last check is reported.
  */
 int attn_sync_check(attn_stream_t stream);
 

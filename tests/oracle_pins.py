@@ -339,6 +339,38 @@ def pin_torch_sdpa(lib=None):
         _close(lse, torch.logsumexp(s, dim=-1).numpy(), 1e-12, "torch logsumexp LSE")
 
 
+def pin_head_dim_512(lib=None):
+    """Head dimension 512 (the prefill's widest head): exact brute force on a tiny
+    causal GQA case with Sq < Skv, and torch's float64 SDPA on a larger one with
+    Sq > Skv (fully masked leading rows)."""
+    from torch.nn.attention.bias import causal_lower_right
+    rng = np.random.default_rng(512)
+    B, Hq, Hkv, Sq, Skv, d = 1, 2, 1, 3, 5, 512
+    scale = 1.0 / math.sqrt(d)
+    q, k, v = _bf16((B, Sq, Hq, d), rng), _bf16((B, Skv, Hkv, d), rng), _bf16((B, Skv, Hkv, d), rng)
+    o, lse = oracle.sdpa(q, k, v, True, scale, lib=lib)
+    eo, el = _exact_attention(q, k, v, True, scale)
+    _close(o, eo, 1e-12, "d512 brute O")
+    _close(lse, el, 1e-12, "d512 brute LSE")
+    B, Hq, Hkv, Sq, Skv = 2, 4, 2, 37, 29
+    q, k, v = _bf16((B, Sq, Hq, d), rng), _bf16((B, Skv, Hkv, d), rng), _bf16((B, Skv, Hkv, d), rng)
+    o, lse = oracle.sdpa(q, k, v, True, scale, lib=lib)
+    G = Hq // Hkv
+    tq = torch.from_numpy(q).permute(0, 2, 1, 3)
+    tk = torch.from_numpy(k).permute(0, 2, 1, 3).repeat_interleave(G, dim=1)
+    tv = torch.from_numpy(v).permute(0, 2, 1, 3).repeat_interleave(G, dim=1)
+    live = Sq - Skv  # rows before this one admit no key (bottom-right alignment)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        tq[:, :, live:], tk, tv, attn_mask=causal_lower_right(Sq - live, Skv), scale=scale)
+    _close(o[:, live:], ref.permute(0, 2, 1, 3).numpy(), 1e-12, "d512 torch sdpa O")
+    assert np.all(o[:, :live] == 0) and np.all(np.isneginf(lse[:, :, :live])), "d512 masked rows"
+    s_ = torch.matmul(tq, tk.transpose(-1, -2)) * scale
+    i = torch.arange(Sq).view(-1, 1)
+    j = torch.arange(Skv).view(1, -1)
+    s_ = s_.masked_fill(j > i + (Skv - Sq), float("-inf"))
+    _close(lse[:, :, live:], torch.logsumexp(s_, dim=-1)[:, :, live:].numpy(), 1e-12, "d512 LSE")
+
+
 # ---------------------------------------------------------------- invariants
 def pin_rows_sum_to_one(lib=None):
     """V = a constant per KV head -> O = that constant iff every row of P sums to 1."""
@@ -477,5 +509,5 @@ ALL_PINS = [
     pin_rows_sum_to_one, pin_permutation_invariance, pin_linearity_in_v,
     pin_split_merge_equals_unsplit, pin_merge_identity, pin_decode_equals_prefill, pin_closed_forms,
     pin_varlen_brute_force, pin_window_brute_force, pin_window_closed_forms,
-    pin_varlen_window_brute_force,
+    pin_varlen_window_brute_force, pin_head_dim_512,
 ]

@@ -6,8 +6,8 @@ import re
 
 import pytest
 
-import attn_forward_tcgen05_gb300 as attn
-from attn_forward_tcgen05_gb300 import build as attn_build
+import attention_forward_tcgen05_gb300 as attn
+from attention_forward_tcgen05_gb300 import build as attn_build
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "attn.h")
@@ -33,7 +33,7 @@ def test_exports_every_declared_symbol(lib):
 
 def test_version_and_strerror(lib):
     assert attn.attn_version() >= 10000
-    for code in (0, -1, -2, -3, -4):
+    for code in (0, -1, -2, -3, -4, -5, -6):
         assert attn.attn_strerror(code)
     assert attn.attn_strerror(12345) == "unknown status"
 
@@ -55,6 +55,19 @@ def test_prefill_validation(lib):
     assert f(P, P, M, P, P, 1, 2, 2, 4, 4, 64, 1, 0.5, 0, N) == attn.ATTN_ERR_INVALID_ARG  # misaligned v
     assert f(N, N, N, N, N, 0, 2, 2, 4, 4, 64, 1, 0.5, 0, N) == attn.ATTN_OK  # empty batch: no-op
     assert f(N, N, N, N, N, 2, 2, 2, 0, 4, 64, 1, 0.5, 0, N) == attn.ATTN_OK  # no queries: no-op
+    assert f(N, N, N, N, N, 0, 2, 2, 4, 4, 512, 1, 0.5, 0, N) == attn.ATTN_OK  # d = 512 accepted
+    assert f(P, P, P, P, P, 1, 2, 2, 4, 4, 1024, 1, 0.5, 0, N) == attn.ATTN_ERR_UNSUPPORTED
+
+
+def test_head_dim_512_only_on_the_plain_prefill(lib):
+    """d = 512 runs through attn_prefill_fwd; the other entry points refuse it."""
+    assert attn.attn_prefill_window(P, P, P, P, P, 1, 2, 2, 4, 4, 512, 8, 0, 0.5, 0, N) == attn.ATTN_ERR_UNSUPPORTED
+    assert attn.attn_prefill_packed(P, P, P, P, P, 1, 8, 1, 4, 4, 512, 1, 0.5, 0, N) == attn.ATTN_ERR_UNSUPPORTED
+    assert attn.attn_prefill_varlen(P, P, P, P, P, P, P, 2, 2, 2, 10, 8, 16, 512, 1, 0.5, 0, N) == \
+        attn.ATTN_ERR_UNSUPPORTED
+    assert attn.attn_decode_split(P, P, P, P, 1, 8, 2, 512, 10, 0.1, 4, 1, P, P, N) == attn.ATTN_ERR_UNSUPPORTED
+    assert attn.attn_decode_packed(P, P, P, P, 2, 8, 1, 512, 16, 0.5, P, P, 0, N) == attn.ATTN_ERR_UNSUPPORTED
+    assert attn.attn_merge(P, P, P, P, 1, 4, 8, 512, 1, N) == attn.ATTN_ERR_UNSUPPORTED
 
 
 def test_prefill_window_validation(lib):
@@ -151,3 +164,29 @@ def test_decode_and_merge_validation(lib):
 def test_debug_wait_limits(lib):
     assert attn.attn_debug_wait_timeout(10, N) == attn.ATTN_ERR_INVALID_ARG
     assert attn.attn_debug_wait_timeout(10**11, N) == attn.ATTN_ERR_INVALID_ARG
+
+
+def test_noalloc_validation(lib):
+    """attn_decode_noalloc checks its arguments by the rules of attn_decode_split and
+    attn_merge first, and the size of its problem against the static scratch after
+    them: a malformed call is reported as malformed whatever its size."""
+    f = attn.attn_decode_noalloc
+    limit = attn.attn_decode_noalloc_scratch_bytes()
+    assert limit == 24 << 20
+    B, Hq, Hkv, d, n_splits = 64, 32, 8, 128, 32  # partials of 33.8 MB: beyond the scratch
+    assert B * Hq * n_splits * (d + 1) * 4 > limit
+    #      q  kc vc kv  B  Hq  Hkv  d  mkv scale  ns  mr o  lse dtype stream
+    assert f(P, P, P, P, B, Hq, Hkv, d, 16, 0.1, n_splits, 1, P, P, attn.ATTN_BF16, N) == \
+        attn.ATTN_ERR_SCRATCH_TOO_SMALL
+    # oversized and malformed: the malformation is what is reported
+    assert f(P, P, P, P, B, Hq, Hkv, d, 16, float("nan"), n_splits, 1, P, P, 1, N) == attn.ATTN_ERR_INVALID_ARG
+    assert f(P, M, P, P, B, Hq, Hkv, d, 16, 0.1, n_splits, 1, P, P, 1, N) == attn.ATTN_ERR_INVALID_ARG
+    assert f(P, P, P, P, B, Hq, Hkv, d, 16, 0.1, n_splits, 1, M, P, 1, N) == attn.ATTN_ERR_INVALID_ARG
+    assert f(P, P, P, P, B, Hq, Hkv, d, 16, 0.1, n_splits, 1, P, N, 1, N) == attn.ATTN_ERR_INVALID_ARG
+    assert f(P, P, P, P, B, Hq, Hkv, 96, 16, 0.1, n_splits, 1, P, P, 1, N) == attn.ATTN_ERR_UNSUPPORTED
+    assert f(P, P, P, P, B, Hq, Hkv, d, 16, 0.1, n_splits, 1, P, P, 5, N) == attn.ATTN_ERR_UNSUPPORTED
+    assert f(P, P, P, P, B, 34, 2, d, 16, 0.1, n_splits, 1, P, P, 1, N) == attn.ATTN_ERR_INVALID_ARG  # G > 16
+    assert f(P, P, P, P, B, Hq, Hkv, d, 16, 0.1, 2000, 1, P, P, 1, N) == attn.ATTN_ERR_INVALID_ARG  # n_splits
+    # the rules shared with attn_decode_split on a problem that fits
+    assert f(P, P, P, N, 2, 8, 2, 64, 16, 0.1, 4, 1, P, P, 1, N) == attn.ATTN_ERR_INVALID_ARG  # null kv_lens
+    assert f(N, N, N, N, 0, 8, 2, 64, 16, 0.1, 4, 1, N, N, 1, N) == attn.ATTN_OK  # empty batch

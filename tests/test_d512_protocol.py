@@ -1,0 +1,210 @@
+"""The head-dimension-512 prefill kernel's mbarrier protocol, modelled on the CPU.
+
+The d = 512 kernel computes O in two column halves one after the other (S is
+recomputed for the second), so its T = 2 n_kv tiles form one sequence: tile jj
+belongs to phase jj // n_kv and key tile jj % n_kv.  A TMA producer warp fills
+a ring of single-panel slots in the order K(0) K(1) { V(jj) K(jj + 2) } (8 K
+panels, 4 V panels per tile), the MMA warp consumes them in that order issuing
+S(0) S(1) { P(jj).V(jj) S(jj + 2) } (two S buffers, S(jj) in buffer jj % 2,
+each with its own S and P barrier), and one softmax warpgroup waits for S(jj),
+optionally rescales O in phase 0 (waiting for P(jj-1).V(jj-1) on the O
+barrier), publishes P(jj), and at the end of each phase waits for that phase's
+last P.V on the final barrier (its phase-th phase) before reading the O half.
+
+A wait tests a phase parity, so it is sound only if its barrier has completed
+exactly the phases before the awaited one or that phase too.  The model runs
+the schedule against exact mbarrier semantics with random TMA, MMA and softmax
+latencies, checks every wait for soundness and that the pipeline drains, and
+must catch the unsound variants kept as negative cases.
+"""
+import heapq
+import itertools
+import random
+
+import pytest
+
+from tests.test_prefill_protocol import Bar
+
+K_PANELS, V_PANELS = 8, 4
+
+
+def simulate(n_kv, slots, seed, s_per_buffer=True, fin_parity_by_phase=True):
+    """Run one randomised schedule; raises AssertionError on an unsound wait or a
+    deadlock.  s_per_buffer=False keys the S and P barriers by nothing (one of each
+    for both buffers); fin_parity_by_phase=False waits for the final barrier's
+    phase 0 at the end of both phases."""
+    rng = random.Random(seed)
+    bars = {}
+
+    def bar(name, count=1):
+        if name not in bars:
+            bars[name] = Bar(name, count)
+        return bars[name]
+
+    def s_bar(buf):
+        return bar(("S", buf if s_per_buffer else 0))
+
+    def p_bar(buf):
+        return bar(("P", buf if s_per_buffer else 0), 4)
+
+    def buf_use(jj):  # index of the awaited phase of tile jj's S / P barrier
+        return jj >> 1 if s_per_buffer else jj
+
+    T = 2 * n_kv
+    now = [0]
+    events = []
+    seq = itertools.count()
+    mma_free = [0]
+
+    def at(time, fn):
+        heapq.heappush(events, (time, next(seq), fn))
+
+    def mma(dur):
+        mma_free[0] = max(now[0], mma_free[0]) + dur
+
+    def commit(b):
+        at(mma_free[0], b.arrive)
+
+    def wait(b, parity, use):
+        assert b.done in (use, use + 1), f"{b.name}: waiting for phase {use} with {b.done} done"
+        return ("wait", b, parity)
+
+    def items():  # the ring's item order, shared by producer and MMA warp
+        seq_ = [("K", 0)] * K_PANELS + [("K", 1)] * K_PANELS
+        for jj in range(T):
+            seq_ += [("V", jj)] * V_PANELS
+            if jj + 2 < T:
+                seq_ += [("K", jj + 2)] * K_PANELS
+        return seq_
+
+    def producer():
+        bar("q").expect_tx(1)
+        at(now[0] + rng.randint(50, 3000), lambda: bar("q").complete_tx(1))
+        for g, _ in enumerate(items()):
+            s, u = g % slots, g // slots
+            if u > 0:
+                yield wait(bar(("empty", s)), (u & 1) ^ 1, u - 1)
+            b = bar(("full", s))
+            b.expect_tx(1)
+            at(now[0] + rng.randint(50, 3000), lambda b=b: b.complete_tx(1))
+
+    def mma_warp():
+        yield wait(bar("q"), 0, 0)
+        g = [0]
+
+        def take():
+            s, u = g[0] % slots, g[0] // slots
+            yield wait(bar(("full", s)), u & 1, u)
+            return s
+
+        def issue_s(jj):
+            for _ in range(K_PANELS):
+                s = yield from take()
+                for _ in range(4):
+                    mma(rng.randint(20, 80))
+                commit(bar(("empty", s)))
+                g[0] += 1
+            commit(s_bar(jj & 1))
+
+        def issue_pv(jj):
+            u = buf_use(jj)
+            yield wait(p_bar(jj & 1), u & 1, u)
+            for _ in range(V_PANELS):
+                s = yield from take()
+                for _ in range(8):
+                    mma(rng.randint(10, 40))
+                commit(bar(("empty", s)))
+                g[0] += 1
+            commit(bar("O"))
+            if jj % n_kv == n_kv - 1:
+                commit(bar("Fin"))
+
+        yield from issue_s(0)
+        yield from issue_s(1)
+        for jj in range(T):
+            yield from issue_pv(jj)
+            if jj + 2 < T:
+                yield from issue_s(jj + 2)
+
+    def softmax():
+        for jj in range(T):
+            ph, j = divmod(jj, n_kv)
+            u = buf_use(jj)
+            yield wait(s_bar(jj & 1), u & 1, u)
+            yield ("sleep", rng.randint(20, 400))
+            if ph == 0 and j > 0 and rng.random() < 0.3:  # O rescale needs P(jj-1).V(jj-1) done
+                yield wait(bar("O"), (jj - 1) & 1, jj - 1)
+                yield ("sleep", rng.randint(20, 200))
+            for _ in range(4):  # one arrival per softmax warp
+                p_bar(jj & 1).arrive()
+            if j == n_kv - 1:  # end of the phase: its O half is complete
+                fu = ph if fin_parity_by_phase else 0
+                yield wait(bar("Fin"), fu & 1, fu)
+                # the O half is read now: every P.V of the phase must have completed
+                assert bar("O").done >= (ph + 1) * n_kv, "O half read before its last P.V completed"
+                yield ("sleep", rng.randint(1000, 8000))  # the O half's epilogue
+            elif rng.random() < 0.2:
+                yield ("sleep", rng.randint(100, 4000))  # the warps fall behind the MMAs
+
+    procs = [producer(), softmax(), mma_warp()]
+    blocked = {}
+    finished = set()
+
+    def step(i):
+        while True:
+            if i in blocked:
+                _, b, parity = blocked[i]
+                if not b.ready(parity):
+                    return
+                del blocked[i]
+            try:
+                req = next(procs[i])
+            except StopIteration:
+                finished.add(i)
+                return
+            if req[0] == "wait":
+                blocked[i] = req
+            elif req[0] == "sleep":
+                at(now[0] + req[1], lambda i=i: step(i))
+                return
+
+    for i in range(len(procs)):
+        step(i)
+    for _ in range(400000):
+        for i in list(blocked):
+            step(i)
+        if len(finished) == len(procs):
+            break
+        if not events:
+            raise AssertionError(f"deadlock: blocked on {[blocked[i][1].name for i in blocked]}")
+        now[0], _, fn = heapq.heappop(events)
+        fn()
+    assert len(finished) == len(procs), "pipeline did not drain"
+
+
+@pytest.mark.parametrize("n_kv", [1, 2, 3, 8, 17])
+@pytest.mark.parametrize("slots", [6, 1, 4])
+def test_d512_protocol_is_sound(n_kv, slots):
+    for seed in range(60):
+        simulate(n_kv, slots, seed)
+
+
+def test_d512_one_s_barrier_for_both_buffers_is_unsound():
+    """One S barrier and one P barrier for both S buffers: S(jj+1) can complete
+    before the softmax waits for S(jj), two phases ahead.  The model must catch it."""
+    failures = 0
+    for seed in range(100):
+        try:
+            simulate(5, 6, seed, s_per_buffer=False)
+        except AssertionError:
+            failures += 1
+    assert failures > 0
+
+
+def test_d512_final_barrier_waited_with_phase_zero_twice_is_unsound():
+    """Waiting for the final barrier's phase 0 at the end of phase 1 too: the wait
+    passes at once and the second O half would be read before its last P.V
+    completed.  The model must catch it."""
+    with pytest.raises(AssertionError):
+        for seed in range(50):
+            simulate(3, 6, seed, fin_parity_by_phase=False)

@@ -6,8 +6,8 @@ import pytest
 import torch
 
 import oracle
-from attn_forward_tcgen05_gb300 import decode_split, merge, sync_check
-from attn_forward_tcgen05_gb300 import workloads as W
+from attention_forward_tcgen05_gb300 import decode_split, merge, sync_check
+from attention_forward_tcgen05_gb300 import workloads as W
 from tests.tolerances import check_lse, check_o
 
 pytestmark = pytest.mark.gpu

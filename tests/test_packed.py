@@ -7,8 +7,8 @@ import pytest
 import torch
 
 import oracle
-from attn_forward_tcgen05_gb300 import decode_packed, prefill, sync_check
-from attn_forward_tcgen05_gb300 import workloads as W
+from attention_forward_tcgen05_gb300 import decode_packed, prefill, sync_check
+from attention_forward_tcgen05_gb300 import workloads as W
 from tests.tolerances import check_lse, check_o
 
 pytestmark = pytest.mark.gpu
@@ -89,26 +89,13 @@ def test_packed_decode_cache_rows_past_length_ignored():
     check_lse(lse.cpu().numpy(), rl)
 
 
-def test_mqa_decode_workload_sampled():
-    """The full multi-query decode workload in the benchmark's configuration
-    (bf16 output), checked on sampled sequences against the oracle."""
-    s = W.MQA_DECODE
-    q, kc, vc, lens = W.decode_inputs_for(s)
-    o, lse = decode_packed(q.cuda(), kc.cuda(), vc.cuda(), lens.cuda(), s.scale)
-    sync_check()
-    pick = [0, 1, 17, 63, 64, 100, s.B - 1]
-    ro, rl = oracle.decode(q[pick], kc[pick], vc[pick], lens[pick], s.scale)
-    check_o(o[pick].float().cpu().numpy(), ro, True)
-    check_lse(lse[pick].cpu().numpy(), rl)
-
-
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("Hq,Hkv", [(128, 1), (16, 2)])
 @pytest.mark.parametrize("n_splits,min_rows", [(1, 1), (3, 1), (8, 256), (16, 64)])
 def test_packed_decode_split_partials(d, Hq, Hkv, n_splits, min_rows):
     """Partials with the decode split rule (empty splits included) against the
     oracle's split partials, then merged against the oracle's decode."""
-    from attn_forward_tcgen05_gb300 import decode_split_packed, merge
+    from attention_forward_tcgen05_gb300 import decode_split_packed, merge
     lens = torch.tensor([0, 1, 29, 300, 1000, 2049, 5], dtype=torch.int32)
     q, kc, vc = W.decode_inputs(len(lens), Hq, Hkv, d, lens, 700 + d + n_splits)
     scale = 1.0 / np.sqrt(d)
@@ -127,26 +114,9 @@ def test_packed_decode_split_partials(d, Hq, Hkv, n_splits, min_rows):
 
 
 def test_packed_decode_no_keys_with_splits():
-    from attn_forward_tcgen05_gb300 import decode_split_packed
+    from attention_forward_tcgen05_gb300 import decode_split_packed
     lens = torch.zeros(3, dtype=torch.int32)
     q, kc, vc = W.decode_inputs(3, 8, 1, 64, lens, 721, Lmax=0)
     po, pl = decode_split_packed(q.cuda(), kc.cuda(), vc.cuda(), lens.cuda(), 4, 1, 0.125)
     sync_check()
     assert np.all(po.cpu().numpy() == 0) and np.all(np.isneginf(pl.cpu().numpy()))
-
-
-def test_mqa_decode_workload_split_sampled():
-    """The multi-query decode workload as the benchmark runs it (split partials +
-    merge), sampled sequences against the oracle."""
-    s = W.MQA_DECODE
-    q, kc, vc, lens = W.decode_inputs_for(s)
-    o, lse = decode_packed(q.cuda(), kc.cuda(), vc.cuda(), lens.cuda(), s.scale,
-                           n_splits=MQA_SPLITS, min_rows_per_split=MQA_MIN_ROWS)
-    sync_check()
-    pick = [0, 5, 31, 64, 127]
-    ro, rl = oracle.decode(q[pick], kc[pick], vc[pick], lens[pick], s.scale)
-    check_o(o[pick].float().cpu().numpy(), ro, True)
-    check_lse(lse[pick].cpu().numpy(), rl)
-
-
-MQA_SPLITS, MQA_MIN_ROWS = W.MQA_DECODE_SPLITS

@@ -4,7 +4,7 @@ import ctypes
 import pytest
 import torch
 
-import attn_forward_tcgen05_gb300 as attn
+import attention_forward_tcgen05_gb300 as attn
 
 pytestmark = pytest.mark.gpu
 

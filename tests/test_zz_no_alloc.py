@@ -4,9 +4,10 @@ Callers that cannot call cudaMalloc (a memory pool that already reserved the
 device, code that must not synchronise the device, C callers without a device
 allocator) use this entry point; its split partials live in the library's
 static device array.  The test calls it through the C ABI and compares with
-attn_decode_split + attn_merge on caller-allocated partials, within the
-parity tolerances, on two calls in a row -- the second one smaller, so stale
-contents of the shared array from the first call must not leak into it.
+attn_decode_split + attn_merge on caller-allocated partials, and with the
+fp64 oracle's decode, within the parity tolerances, on two calls in a row --
+the second one smaller, so stale contents of the shared array from the first
+call must not leak into it.
 
 This file is collected last so that a run stopping at the first failure has
 already run every other test.
@@ -18,8 +19,9 @@ import numpy as np
 import pytest
 import torch
 
-import attn_forward_tcgen05_gb300 as attn
-from attn_forward_tcgen05_gb300 import workloads as W
+import attention_forward_tcgen05_gb300 as attn
+import oracle
+from attention_forward_tcgen05_gb300 import workloads as W
 from tests.tolerances import check_lse, check_o
 
 pytestmark = pytest.mark.gpu
@@ -45,7 +47,7 @@ def _noalloc(q, kc, vc, lens, n_splits, min_rows, scale, out_dtype):
 def _case(lens, Hq, Hkv, d, seed):
     lens = torch.tensor(lens, dtype=torch.int32)
     q, kc, vc = W.decode_inputs(len(lens), Hq, Hkv, d, lens, seed)
-    return q.cuda(), kc.cuda(), vc.cuda(), lens.cuda()
+    return (q, kc, vc, lens), (q.cuda(), kc.cuda(), vc.cuda(), lens.cuda())
 
 
 def test_noalloc_matches_decode_split_and_merge_twice():
@@ -56,23 +58,16 @@ def test_noalloc_matches_decode_split_and_merge_twice():
         ([300, 5], 8, 2, 64, 4, 0, torch.float32),
     ]
     for i, (lens, Hq, Hkv, d, n_splits, min_rows, odt) in enumerate(calls):
-        q, kc, vc, lg = _case(lens, Hq, Hkv, d, 100 + i)
+        host, (q, kc, vc, lg) = _case(lens, Hq, Hkv, d, 100 + i)
         scale = 1.0 / math.sqrt(d)
         o_ref, l_ref = attn.decode(q, kc, vc, lg, n_splits, min_rows, scale, odt)
         o, l = _noalloc(q, kc, vc, lg, n_splits, min_rows, scale, odt)
         assert attn.attn_sync_check(ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)) == 0
-        check_o(o.float().cpu().numpy(), o_ref.float().cpu().numpy(), odt == torch.bfloat16,
-                f"call {i} O")
-        check_lse(l.cpu().numpy(), l_ref.cpu().numpy(), f"call {i} LSE")
-
-
-def test_noalloc_rejects_problems_beyond_the_scratch():
-    limit = attn.attn_decode_noalloc_scratch_bytes()
-    assert limit == 24 << 20
-    # B * Hq * n_splits * (d + 1) * 4 bytes > 24 MiB: rejected before any launch
-    B, Hq, Hkv, d, n_splits = 64, 32, 8, 128, 32
-    assert B * Hq * n_splits * (d + 1) * 4 > limit
-    dummy = ctypes.c_void_p(256)
-    rc = attn.attn_decode_noalloc(dummy, dummy, dummy, dummy, B, Hq, Hkv, d, 16, 0.1, n_splits, 1,
-                                  dummy, dummy, attn.ATTN_BF16, None)
-    assert rc == attn.ATTN_ERR_SCRATCH_TOO_SMALL
+        got_o, got_l = o.float().cpu().numpy(), l.cpu().numpy()
+        # against the entry point that takes caller-allocated partials ...
+        check_o(got_o, o_ref.float().cpu().numpy(), odt == torch.bfloat16, f"call {i} O vs decode")
+        check_lse(got_l, l_ref.cpu().numpy(), f"call {i} LSE vs decode")
+        # ... and against the fp64 oracle's unsplit decode
+        ro, rl = oracle.decode(*host, scale)
+        check_o(got_o, ro, odt == torch.bfloat16, f"call {i} O vs oracle")
+        check_lse(got_l, rl, f"call {i} LSE vs oracle")

@@ -10,6 +10,14 @@ import numpy as np
 O_TOL = 5e-3
 LSE_TOL = 1e-3
 
+# (workload, output, max|dO|, max|dLSE|) of every whole-output comparison at full
+# size, printed at the end of the test session (tests/conftest.py)
+PARITY_LOG = []
+
+
+def log_parity(what: str, o_err: float, lse_err: float):
+    PARITY_LOG.append((what, float(o_err), float(lse_err)))
+
 
 def half_ulp_bf16(x):
     """Half of the bf16 spacing at |x| (bf16 keeps 8 significant bits)."""
