@@ -16,8 +16,9 @@
 //   * warp 4*NQ       MMA issuer: S = Q K^T and O += P V with tcgen05.mma
 //       (kind::f16, bf16 in, fp32 accumulate in TMEM; P is the A operand
 //       straight from TMEM);
-//   * warp 4*NQ+1     TMA producer: Q once, then a ring of K and a ring of V
-//       stages, each 128 rows x d, 128-byte swizzled.
+//   * warps 4*NQ+1, 4*NQ+2  TMA producers: Q once and then a ring of K stages,
+//       and a ring of V stages, each 128 rows x d, 128-byte swizzled; the two
+//       rings fill independently.
 // The MMA and TMA warps run their loops as whole warps (warp-uniform
 // descriptors); one elected lane issues each instruction.
 //
@@ -77,11 +78,8 @@ struct PrefillCfg {
   static constexpr int kQTileBytes = kPanels * kQPanelBytes;
   static constexpr int kKVStageBytes = kPanels * kKVPanelBytes;
   static constexpr int kStagesK = (D == 64) ? (H ? 5 : 4) : (D == 128 ? (H ? 3 : 2) : 1);  // K ring depth
-  static constexpr int kStagesV = (D == 64) ? 4 : (D == 128 ? 2 : 1);  // V ring depth
+  static constexpr int kStagesV = (D == 64) ? 4 : (D == 128 ? (H ? 2 : 3) : 1);  // V ring depth
   static constexpr int kQTiles = H ? 1 : NQ;               // Q tiles in shared memory
-  // K tiles the producer may issue ahead of V: the MMA warp needs K of the next
-  // tile (item) before V of the current one; key halves stream from HBM and run further
-  static constexpr int kLookK = H ? 2 : 1;
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQTiles * kQTileBytes;
   static constexpr int kVOff = kKOff + kStagesK * kKVStageBytes;
@@ -91,13 +89,15 @@ struct PrefillCfg {
   // is at most one phase ahead of the warp that waits on it.
   static constexpr int kNumBars = 1 + 2 * kStagesK + 2 * kStagesV + 2 * NQ * NS + 2 * NQ;
   // merge of the two key halves of a decode unit: per row (m, l, l_rnd, ok), fp32
+  // (key-halves layout only)
   static constexpr int kMergeOff = kBarOff + kNumBars * 8 + 16;
-  static constexpr int kMergeBytes = 128 * 4 * 4;
+  static constexpr int kMergeBytes = H ? 128 * 4 * 4 : 0;
   static constexpr int kSmemBytes = kMergeOff + kMergeBytes + 1024;
-  // NQ softmax warpgroups + one control warpgroup (MMA warp, TMA warp, two spare warps).
+  // NQ softmax warpgroups + one control warpgroup (MMA warp, K and V TMA warps, one
+  // spare warp).
   static constexpr int kThreads = (4 * NQ + 4) * 32;
   static constexpr int kMmaWarp = 4 * NQ;
-  static constexpr int kTmaWarp = 4 * NQ + 1;
+  static constexpr int kTmaWarp = 4 * NQ + 1;  // K producer; kTmaWarp + 1: V producer
   // Register split (NQ == 2 only; 12 warps launch with 168 registers each):
   // the control warpgroup drops to kCtlRegs, the softmax warpgroups grow to
   // kSoftmaxRegs: 8*32*208 + 4*32*80 = 63488 <= 384*168 = 64512 (the launch
@@ -296,66 +296,62 @@ __global__ void __launch_bounds__(PrefillCfg<D, HALVES>::kThreads, 1)
   if (warp >= 4 * NQ) {
     // ======================= control warpgroup =======================
     if constexpr (NQ == 2) setmaxnreg_dec<C::kCtlRegs>();  // whole warpgroup, same instruction
-  if (warp == C::kTmaWarp) {
-    // =========================== TMA producer ===========================
+  if (warp == C::kTmaWarp || warp == C::kTmaWarp + 1) {
+    // =========================== TMA producers ===========================
+    // Warp kTmaWarp loads Q once and then the K ring, warp kTmaWarp + 1 the V ring.
+    // The rings fill independently: a stage is requested as soon as it is free,
+    // so a V stage never waits behind a K stage that is still in use (with one
+    // producer issuing K(j+1) before V(j), a wait for a K slot held up the V load
+    // the MMA warp needed next).
     if (n_kv > 0) {
+      const bool is_k = warp == C::kTmaWarp;
       if (lane == 0) {
-        tma_prefetch_desc(&tm_q);
-        tma_prefetch_desc(&tm_k);
-        tma_prefetch_desc(&tm_v);
-      }
-      uint32_t qbytes = 0;
-#pragma unroll
-      for (int t = 0; t < C::kQTiles; ++t)
-        if (ti[t].n_kv > 0) qbytes += C::kQTileBytes;
-      mbar_arrive_expect_tx_e(bar_q, qbytes);
-#pragma unroll
-      for (int t = 0; t < C::kQTiles; ++t) {
-        if (ti[t].n_kv > 0) {
-#pragma unroll
-          for (int p = 0; p < C::kPanels; ++p)
-            tma_load_5d_e(sQ + t * C::kQTileBytes + p * C::kQPanelBytes, &tm_q, bar_q, p * 64, 0, hu,
-                          ext.qbase + ti[t].q0 / G, ext.bq);
+        if (is_k) {
+          tma_prefetch_desc(&tm_q);
+          tma_prefetch_desc(&tm_k);
+        } else {
+          tma_prefetch_desc(&tm_v);
         }
       }
-      // Stages of kSub KV tiles (ring items with key halves).  The MMA warp takes
-      // K of tile (item) j+1 before V of tile j, so K stage uk goes out before V
-      // stage uv while uk*kSub <= uv*kSub + kLookK (kLookK = 1; 2 with key halves,
-      // whose deeper K ring streams from HBM).
+      if (is_k) {
+        uint32_t qbytes = 0;
+#pragma unroll
+        for (int t = 0; t < C::kQTiles; ++t)
+          if (ti[t].n_kv > 0) qbytes += C::kQTileBytes;
+        mbar_arrive_expect_tx_e(bar_q, qbytes);
+#pragma unroll
+        for (int t = 0; t < C::kQTiles; ++t) {
+          if (ti[t].n_kv > 0) {
+#pragma unroll
+            for (int p = 0; p < C::kPanels; ++p)
+              tma_load_5d_e(sQ + t * C::kQTileBytes + p * C::kQPanelBytes, &tm_q, bar_q, p * 64, 0, hu,
+                            ext.qbase + ti[t].q0 / G, ext.bq);
+          }
+        }
+      }
+      // stages of kSub KV tiles (ring items with key halves), in the order the MMA
+      // warp consumes them
       const int n_st = (n_items + C::kSub - 1) / C::kSub;
-      int jk = 0, jv = 0;  // next K / V stage
-      bool aborted = false;
-      while (jv < n_st) {
-        if (jk < n_st && jk * C::kSub <= jv * C::kSub + C::kLookK) {
-          const int s = jk % C::kStagesK;
-          const uint32_t ph = (uint32_t)(jk / C::kStagesK) & 1u;
-          if (!mbar_wait_warp(&bar_emptyK[s], ph ^ 1u, err, abort_flag)) { aborted = true; break; }
-          mbar_arrive_expect_tx_e(&bar_fullK[s], C::kKVStageBytes);
-#pragma unroll
-          for (int p = 0; p < C::kPanels; ++p)
-            tma_load_4d_e(sK + s * C::kKVStageBytes + p * C::kKVPanelBytes, &tm_k, &bar_fullK[s], p * 64,
-                          hk, item_key(jk) * C::kStageRows, b);
-          ++jk;
-          continue;
-        }
-        const int s = jv % C::kStagesV;
-        const uint32_t ph = (uint32_t)(jv / C::kStagesV) & 1u;
-        if (!mbar_wait_warp(&bar_emptyV[s], ph ^ 1u, err, abort_flag)) { aborted = true; break; }
-        mbar_arrive_expect_tx_e(&bar_fullV[s], C::kKVStageBytes);
+      const int stages = is_k ? C::kStagesK : C::kStagesV;
+      uint64_t* const full = is_k ? bar_fullK : bar_fullV;
+      uint64_t* const empty = is_k ? bar_emptyK : bar_emptyV;
+      uint8_t* const ring = is_k ? sK : sV;
+      const CUtensorMap* const map = is_k ? &tm_k : &tm_v;
+      int u = 0;
+      for (; u < n_st; ++u) {
+        const int s = u % stages;
+        const uint32_t ph = (uint32_t)(u / stages) & 1u;
+        if (!mbar_wait_warp(&empty[s], ph ^ 1u, err, abort_flag)) break;
+        mbar_arrive_expect_tx_e(&full[s], C::kKVStageBytes);
 #pragma unroll
         for (int p = 0; p < C::kPanels; ++p)
-          tma_load_4d_e(sV + s * C::kKVStageBytes + p * C::kKVPanelBytes, &tm_v, &bar_fullV[s], p * 64,
-                        hk, item_key(jv) * C::kStageRows, b);
-        ++jv;
+          tma_load_4d_e(ring + s * C::kKVStageBytes + p * C::kKVPanelBytes, map, &full[s], p * 64, hk,
+                        item_key(u) * C::kStageRows, b);
       }
-      if (aborted) {
-        // let the copies already issued land before shared memory is released
-        for (int u2 = max(0, jk - C::kStagesK); u2 < jk; ++u2)
-          mbar_wait(&bar_fullK[u2 % C::kStagesK], (uint32_t)(u2 / C::kStagesK) & 1u, nullptr, nullptr,
-                    100000000ull);
-        for (int u2 = max(0, jv - C::kStagesV); u2 < jv; ++u2)
-          mbar_wait(&bar_fullV[u2 % C::kStagesV], (uint32_t)(u2 / C::kStagesV) & 1u, nullptr, nullptr,
-                    100000000ull);
+      if (u < n_st) {
+        // aborted: let the copies already issued land before shared memory is released
+        for (int u2 = max(0, u - stages); u2 < u; ++u2)
+          mbar_wait(&full[u2 % stages], (uint32_t)(u2 / stages) & 1u, nullptr, nullptr, 100000000ull);
       }
     }
   } else if (warp == C::kMmaWarp) {

@@ -149,6 +149,7 @@ def simulate(n_kv, slots, seed, s_per_buffer=True, fin_parity_by_phase=True):
     procs = [producer(), softmax(), mma_warp()]
     blocked = {}
     finished = set()
+    advanced = [0]  # process steps taken
 
     def step(i):
         while True:
@@ -157,6 +158,7 @@ def simulate(n_kv, slots, seed, s_per_buffer=True, fin_parity_by_phase=True):
                 if not b.ready(parity):
                     return
                 del blocked[i]
+            advanced[0] += 1
             try:
                 req = next(procs[i])
             except StopIteration:
@@ -171,8 +173,14 @@ def simulate(n_kv, slots, seed, s_per_buffer=True, fin_parity_by_phase=True):
     for i in range(len(procs)):
         step(i)
     for _ in range(400000):
-        for i in list(blocked):
-            step(i)
+        # step the blocked processes until none makes progress (an arrival made by
+        # one of them can release another that was stepped before it)
+        while True:
+            before = advanced[0]
+            for i in list(blocked):
+                step(i)
+            if advanced[0] == before:
+                break
         if len(finished) == len(procs):
             break
         if not events:

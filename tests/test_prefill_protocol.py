@@ -52,11 +52,14 @@ class Bar:
         return (self.done & 1) != parity
 
 
-def simulate(NQ, SK, SV, n_t, seed, p_per_buffer=True, NS=2, SUB=1, LOOK=1, NO=1):
+def simulate(NQ, SK, SV, n_t, seed, p_per_buffer=True, NS=2, SUB=1, LOOK=1, NO=1, split=False):
     """Run one randomised schedule; raises AssertionError on an unsound wait or a deadlock.
 
     p_per_buffer=False keys the P barriers by query tile only (one barrier shared
-    by both S buffers), the form whose parity can alias.
+    by both S buffers), the form whose parity can alias.  split=True gives the K
+    ring and the V ring producers of their own, which fill their rings
+    independently (the single-CTA kernel); otherwise one producer issues K stage
+    jk before V stage jv while jk <= jv + LOOK (the CTA-pair kernel).
     """
     rng = random.Random(seed)
     bars = {}
@@ -99,6 +102,19 @@ def simulate(NQ, SK, SV, n_t, seed, p_per_buffer=True, NS=2, SUB=1, LOOK=1, NO=1
         # use = index of the awaited phase; sound iff done in {use, use + 1}
         assert b.done in (use, use + 1), f"{b.name}: waiting for phase {use} with {b.done} done"
         return ("wait", b, parity)
+
+    def producer_ring(kind, stages):
+        for u in range(n_st):
+            s, k = u % stages, u // stages
+            if k > 0:
+                yield wait(bar(("e" + kind, s)), (k & 1) ^ 1, k - 1)
+            bar(("f" + kind, s)).expect_tx(1)
+            tma(bar(("f" + kind, s)), 1)
+
+    def producer_k():
+        bar("q").expect_tx(1)
+        tma(bar("q"), 1)
+        yield from producer_ring("K", SK)
 
     def producer():
         bar("q").expect_tx(1)
@@ -219,9 +235,11 @@ def simulate(NQ, SK, SV, n_t, seed, p_per_buffer=True, NS=2, SUB=1, LOOK=1, NO=1
         if n_t[t] > 0:
             yield wait(bar(("Fin", t)), 0, 0)
 
-    procs = [producer()] + [softmax(t) for t in range(NQ)] + [mma_warp()]
+    prods = [producer_k(), producer_ring("V", SV)] if split else [producer()]
+    procs = prods + [softmax(t) for t in range(NQ)] + [mma_warp()]
     blocked = {}
     finished = set()
+    advanced = [0]  # process steps taken
 
     def step(i):
         # advance process i until it blocks on a wait or sleeps
@@ -231,6 +249,7 @@ def simulate(NQ, SK, SV, n_t, seed, p_per_buffer=True, NS=2, SUB=1, LOOK=1, NO=1
                 if not b.ready(parity):
                     return
                 del blocked[i]
+            advanced[0] += 1
             try:
                 req = next(procs[i])
             except StopIteration:
@@ -245,8 +264,14 @@ def simulate(NQ, SK, SV, n_t, seed, p_per_buffer=True, NS=2, SUB=1, LOOK=1, NO=1
     for i in range(len(procs)):
         step(i)
     for _ in range(200000):
-        for i in list(blocked):
-            step(i)
+        # step the blocked processes until none makes progress (an arrival made by
+        # one of them can release another that was stepped before it)
+        while True:
+            before = advanced[0]
+            for i in list(blocked):
+                step(i)
+            if advanced[0] == before:
+                break
         if len(finished) == len(procs):
             break
         if not events:
@@ -323,6 +348,25 @@ def test_three_s_buffers_with_one_o_barrier_is_unsound():
 def test_prefill_protocol_one_s_buffer_is_sound(NQ, SUB, SK, SV, n_t):
     for seed in range(120):
         simulate(NQ, SK, SV, list(n_t), seed, SUB=SUB, NS=1)
+
+
+CASES_SPLIT = [
+    # the single-CTA kernel: one S buffer per tile, K and V producers of their own
+    # query tiles, K stages, V stages, KV tiles per query tile
+    (2, 2, 3, (5, 6)),    # d = 128, causal
+    (2, 2, 3, (13, 13)),  # d = 128, non-causal
+    (2, 4, 4, (9, 10)),   # d = 64
+    (2, 2, 3, (0, 1)),
+    (2, 2, 3, (1, 1)),
+    (2, 1, 1, (4, 5)),
+    (2, 3, 1, (6, 6)),
+]
+
+
+@pytest.mark.parametrize("NQ,SK,SV,n_t", CASES_SPLIT, ids=[str(c) for c in CASES_SPLIT])
+def test_prefill_protocol_split_producers_is_sound(NQ, SK, SV, n_t):
+    for seed in range(120):
+        simulate(NQ, SK, SV, list(n_t), seed, SUB=1, NS=1, split=True)
 
 
 def simulate_slices(SK, SV, n, seed, NSL=2, NS=2):
@@ -424,6 +468,7 @@ def simulate_slices(SK, SV, n, seed, NSL=2, NS=2):
     procs = [producer()] + [softmax(h) for h in range(NSL)] + [mma_warp()]
     blocked = {}
     finished = set()
+    advanced = [0]  # process steps taken
 
     def step(i):
         while True:
@@ -432,6 +477,7 @@ def simulate_slices(SK, SV, n, seed, NSL=2, NS=2):
                 if not b.ready(parity):
                     return
                 del blocked[i]
+            advanced[0] += 1
             try:
                 req = next(procs[i])
             except StopIteration:
@@ -446,8 +492,14 @@ def simulate_slices(SK, SV, n, seed, NSL=2, NS=2):
     for i in range(len(procs)):
         step(i)
     for _ in range(200000):
-        for i in list(blocked):
-            step(i)
+        # step the blocked processes until none makes progress (an arrival made by
+        # one of them can release another that was stepped before it)
+        while True:
+            before = advanced[0]
+            for i in list(blocked):
+                step(i)
+            if advanced[0] == before:
+                break
         if len(finished) == len(procs):
             break
         if not events:
