@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libattn.so")
 BUILD_DIR = os.path.join(HERE, "_build")
-SOURCES = ["attn_api.cu", "prefill.cu", "prefill_pair.cu", "prefill_d512.cu", "decode.cu", "decode_noalloc.cu"]
+SOURCES = ["attn_api.cu", "prefill.cu", "prefill_pair.cu", "prefill_d512.cu", "prefill_persist.cu", "decode.cu", "decode_noalloc.cu"]
 HEADERS = ["ptx.cuh", "internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

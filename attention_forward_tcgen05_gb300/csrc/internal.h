@@ -155,6 +155,9 @@ int check_merge_args(const void* part_o, const void* part_lse, const void* o, co
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill_pair(const PrefillArgs& a, cudaStream_t stream);
+// Persistent single-CTA kernel (prefill_persist.cu): fixed-length batches, one head
+// per tile (pack = 1), no window, key splits or kv_lens; d in {64, 128}.
+cudaError_t launch_prefill_persistent(const PrefillArgs& a, cudaStream_t stream);
 // Head dimension 512 (prefill_d512.cu): fixed-length batches, causal or not; O in
 // two column halves (S recomputed for the second).
 cudaError_t launch_prefill_d512(const PrefillArgs& a, cudaStream_t stream);

@@ -845,6 +845,11 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, cudaStream_t stream) {
   if (units <= 0) return cudaSuccess;
   if (2 * units > 0x7FFFFFFFLL || rows > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
   if (a.halves) return launch_prefill_grid<D, true>(a, stream, 0, units, 0);
+  // a causal fixed-length launch (one head per tile, no window or key splits) runs
+  // on the persistent kernel, which overlaps each unit's Q load, first MMAs and O
+  // epilogue with its neighbours (prefill_persist.cu)
+  if (a.causal && a.window == 0 && n_splits == 1 && a.cu_q == nullptr && a.kv_lens == nullptr && G == 1)
+    return launch_prefill_persistent(a, stream);
   // A non-causal fixed-length launch whose last wave is at most half full: that
   // wave's units run as two 128-row halves each, whose two query tiles take the
   // two halves of the keys (the key-halves kernel), in about half a unit's time.

@@ -177,3 +177,26 @@ def test_d512_deterministic_and_halves_consistent():
     check_o(got[..., :256], ro[..., :256], False, "O columns [0, 256)")
     check_o(got[..., 256:], ro[..., 256:], False, "O columns [256, 512)")
     check_lse(a[1].cpu().numpy(), rl)
+
+
+PERSIST_SHAPES = [
+    # B, Hq, Hkv, Sq, Skv: causal launches with more units (256-row query blocks x
+    # heads x batch) than SMs, so each CTA of the persistent kernel walks several
+    (2, 8, 2, 2900, 2900),    # ragged last block: its second tile partly past the end
+    (3, 20, 4, 1000, 1300),   # Sq < Skv (bottom-right), a last block with one tile
+    (1, 64, 8, 1100, 700),    # Sq > Skv: rows and whole tiles without any key
+    (1, 40, 40, 2048, 2048),  # MHA, whole blocks
+]
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("shape", PERSIST_SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16], ids=["o_f32", "o_bf16"])
+def test_causal_many_units_per_cta(shape, d, out_dtype):
+    """Causal prefill whose units outnumber the SMs: every output element against
+    the oracle, for both output types (bf16 O leaves through the staging tile the
+    two query tiles take in turn, fp32 O through direct stores)."""
+    B, Hq, Hkv, Sq, Skv = shape
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    assert -(-Sq // 256) * Hq * B > n_sm
+    _full_compare(B, Hq, Hkv, Sq, Skv, d, True, 1.0 / math.sqrt(d), 400 + d + Sq, out_dtype)
