@@ -58,20 +58,23 @@ def load(path: str | None = None):
         lib.attn_decode_split_packed.argtypes = [vp] * 4 + [i] * 5 + [f, i, i, vp, vp, vp]
         lib.attn_decode_split.argtypes = [vp, vp, vp, vp] + [i] * 5 + [f, i, i, vp, vp, vp]
         lib.attn_merge.argtypes = [vp, vp, vp, vp] + [i] * 5 + [vp]
+        lib.attn_decode.argtypes = [vp] * 4 + [i] * 5 + [f, i, i, vp, vp, vp, vp, i, vp, vp]
         lib.attn_sync_check.argtypes = [vp]
         lib.attn_strerror.argtypes = [i]
         lib.attn_strerror.restype = ctypes.c_char_p
         lib.attn_version.argtypes = []
         lib.attn_debug_wait_timeout.argtypes = [ull, vp]
+        lib.attn_prefill_schedule.argtypes = [i] * 5 + [vp, vp, i]
         lib.attn_decode_noalloc.argtypes = [vp, vp, vp, vp] + [i] * 5 + [f, i, i, vp, vp, i, vp]
         lib.attn_decode_noalloc_scratch_bytes.argtypes = []
         lib.attn_decode_noalloc_scratch_bytes.restype = ull
         for name in ("attn_prefill_fwd", "attn_prefill_varlen", "attn_prefill_window",
                      "attn_prefill_varlen_window", "attn_prefill_packed", "attn_decode_packed",
                      "attn_decode_split_packed",
-                     "attn_decode_split", "attn_merge",
+                     "attn_decode_split", "attn_merge", "attn_decode",
                      "attn_sync_check",
-                     "attn_version", "attn_debug_wait_timeout", "attn_decode_noalloc"):
+                     "attn_version", "attn_debug_wait_timeout", "attn_decode_noalloc",
+                     "attn_prefill_schedule"):
             getattr(lib, name).restype = i
         _lib = lib
         return lib
@@ -130,6 +133,31 @@ def attn_decode_split(q, kcache, vcache, kv_lens, B, Hq, Hkv, d, max_kv, scale, 
 
 def attn_merge(part_o, part_lse, o, lse, B, Hq, n_splits, d, o_dtype, stream) -> int:
     return load().attn_merge(part_o, part_lse, o, lse, B, Hq, n_splits, d, o_dtype, stream)
+
+
+def attn_decode(q, kcache, vcache, kv_lens, B, Hq, Hkv, d, max_kv, scale, n_splits,
+                min_rows_per_split, part_o, part_lse, o, lse, o_dtype, counters, stream) -> int:
+    return load().attn_decode(q, kcache, vcache, kv_lens, B, Hq, Hkv, d, max_kv, float(scale),
+                              n_splits, min_rows_per_split, part_o, part_lse, o, lse, o_dtype,
+                              counters, stream)
+
+
+def attn_prefill_schedule(BH, Sq, Skv, causal, grid, offsets, units, max_units) -> int:
+    return load().attn_prefill_schedule(BH, Sq, Skv, int(causal), grid, offsets, units, max_units)
+
+
+def prefill_schedule(BH: int, Sq: int, Skv: int, causal: bool, grid: int):
+    """The causal prefill's unit lists, one per CTA (host only), or None when the
+    launch deals its units in waves."""
+    n_units = -(-Sq // 256) * BH
+    offs = (ctypes.c_int * (grid + 1))()
+    units = (ctypes.c_int * max(n_units, 1))()
+    n = attn_prefill_schedule(BH, Sq, Skv, causal, grid, offs, units, n_units)
+    if n < 0:
+        raise AttnError(n, "attn_prefill_schedule")
+    if n == 0:
+        return None
+    return [list(units[offs[c]:offs[c + 1]]) for c in range(grid)]
 
 
 def attn_decode_noalloc(q, kcache, vcache, kv_lens, B, Hq, Hkv, d, max_kv, scale, n_splits,
@@ -340,11 +368,60 @@ def merge(part_o, part_lse, out_dtype=None, stream=None, out=None):
     return o, lse
 
 
+_counters = {}  # (device type, index) -> the shared zeroed completion counters of decode()
+
+
+def decode_counters(n: int, device):
+    """The shared completion-counter buffer of decode() on `device`: int32, at least n
+    entries, zero between calls.  Calls that use it must be ordered on one stream."""
+    torch = _torch()
+    key = (device.type, device.index)
+    with _lock:
+        buf = _counters.get(key)
+        if buf is None or buf.numel() < n:
+            buf = torch.zeros(max(n, 4096), dtype=torch.int32, device=device)
+            torch.cuda.synchronize(device)  # zeroed before any stream uses it
+            _counters[key] = buf
+    return buf
+
+
 def decode(q, kcache, vcache, kv_lens, n_splits: int, min_rows_per_split: int = 1,
-           scale: float | None = None, out_dtype=None, stream=None):
-    """Split-KV decode followed by the merge: (o [B,Hq,d], lse [B,Hq])."""
-    po, pl = decode_split(q, kcache, vcache, kv_lens, n_splits, min_rows_per_split, scale, stream)
-    return merge(po, pl, out_dtype, stream)
+           scale: float | None = None, out_dtype=None, stream=None, out=None, parts=None,
+           counters=None):
+    """Split-KV decode and its merge in one launch (attn_decode): (o [B,Hq,d], lse [B,Hq]).
+
+    parts: optional (part_o [B,Hq,n_splits,d], part_lse [B,Hq,n_splits]) fp32 buffers for
+    the split partials; counters: optional int32 [>= B*Hq] completion counters, zeroed by
+    the caller (default: a buffer shared by the calls without their own)."""
+    torch = _torch()
+    _check_tensor(q, "q", torch.bfloat16, 3)
+    _check_tensor(kcache, "kcache", torch.bfloat16, 4)
+    _check_tensor(vcache, "vcache", torch.bfloat16, 4)
+    _check_tensor(kv_lens, "kv_lens", torch.int32, 1)
+    B, Hq, d = q.shape
+    _, max_kv, Hkv, _ = kcache.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if parts is None:
+        part_o = torch.empty((B, Hq, n_splits, d), dtype=torch.float32, device=q.device)
+        part_lse = torch.empty((B, Hq, n_splits), dtype=torch.float32, device=q.device)
+    else:
+        part_o, part_lse = parts
+    if out is None:
+        o = torch.empty((B, Hq, d), dtype=out_dtype or torch.bfloat16, device=q.device)
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    else:
+        o, lse = out
+    if counters is None:
+        counters = decode_counters(B * Hq, q.device)
+    elif counters.dtype != torch.int32 or not counters.is_cuda or counters.numel() < B * Hq:
+        raise TypeError("counters must be a CUDA int32 tensor of at least B*Hq entries")
+    rc = attn_decode(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(kv_lens), B, Hq, Hkv, d, max_kv,
+                     scale, n_splits, min_rows_per_split, _ptr(part_o), _ptr(part_lse), _ptr(o),
+                     _ptr(lse), _out_code(o.dtype), _ptr(counters), _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_decode")
+    return o, lse
 
 
 def decode_split_packed(q, kcache, vcache, kv_lens, n_splits: int, min_rows_per_split: int = 1,
@@ -408,6 +485,13 @@ def decode_packed(q, kcache, vcache, kv_lens, scale: float | None = None, out_dt
 
 
 def sync_check(stream=None) -> None:
+    """Synchronise `stream` and raise if a kernel recorded a device-side error.  After
+    such an error the shared decode counters are zeroed again (their count is void)."""
     rc = attn_sync_check(_stream_handle(stream))
     if rc != ATTN_OK:
+        with _lock:
+            bufs = list(_counters.values())
+        for buf in bufs:
+            buf.zero_()
+            _torch().cuda.synchronize(buf.device)
         raise AttnError(rc, "attn_sync_check")

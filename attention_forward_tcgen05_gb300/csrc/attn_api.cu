@@ -9,6 +9,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "attn.h"
 #include "internal.h"
@@ -106,12 +107,14 @@ namespace attn {
 int check_decode_split_args(const void* q, const void* kcache, const void* vcache, const int* kv_lens,
                             int B, int Hq, int Hkv, int d, int max_kv, float scale, int n_splits,
                             int min_rows, const void* part_o, const void* part_lse, bool check_parts) {
-  if (B < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Hq / Hkv > 16 || max_kv < 1)
+  if (B < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Hq / Hkv > kMaxDecodeGroup || max_kv < 1)
     return ATTN_ERR_INVALID_ARG;
   if (n_splits < 1 || n_splits > 1024 || min_rows < 0 || !ok_scale(scale)) return ATTN_ERR_INVALID_ARG;
-  // one CTA per (sequence, KV head, split) in a 1-D grid (launches of fewer than
-  // 128 such units also spread head groups, and stay far below the limit)
-  if ((long long)B * Hkv * n_splits > 0x7FFFFFFFLL) return ATTN_ERR_INVALID_ARG;
+  // one CTA per (sequence, KV head, split, head group) in a 1-D grid: groups above
+  // kMaxHeadsPerCta heads take several CTAs (launches of fewer than 128 units
+  // also spread head groups, and stay far below the limit)
+  const long long n_hg = (Hq / Hkv + kMaxHeadsPerCta - 1) / kMaxHeadsPerCta;
+  if ((long long)B * Hkv * n_splits * n_hg > 0x7FFFFFFFLL) return ATTN_ERR_INVALID_ARG;
   if (!ok_dim(d)) return ATTN_ERR_UNSUPPORTED;
   if (B == 0) return ATTN_OK;
   if (!q || !kcache || !vcache || !kv_lens) return ATTN_ERR_INVALID_ARG;
@@ -352,6 +355,25 @@ int attn_prefill_varlen_window(const attn_bf16_t* q, const attn_bf16_t* kcache,
                      max_kv, d, 1, window, n_sink, scale, o_dtype, stream);
 }
 
+// split partials, and with `done` set their combine into (o, lse) in the same launch
+static int decode_launch(const attn_bf16_t* q, const attn_bf16_t* kcache, const attn_bf16_t* vcache,
+                         const int* kv_lens, int B, int Hq, int Hkv, int d, int max_kv, float scale,
+                         int n_splits, int min_rows_per_split, float* part_o, float* part_lse,
+                         unsigned* done, void* o, float* lse, int o_dtype, attn_stream_t stream) {
+  attn::DecodeArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.q = q; a.kv_lens = kv_lens; a.part_o = part_o; a.part_lse = part_lse;
+  a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.d = d; a.max_kv = max_kv;
+  a.n_splits = n_splits; a.min_rows = min_rows_per_split; a.scale = scale;
+  a.done = done; a.o = o; a.lse = lse; a.o_bf16 = o_dtype == ATTN_BF16 ? 1 : 0;
+  a.err = err_word();
+  if (a.err == nullptr) return ATTN_ERR_CUDA;
+  int rc = encode_bf16_4d(&a.tm_k, kcache, d, Hkv, max_kv, B, attn::kDecodeStageRows);
+  if (rc == ATTN_OK) rc = encode_bf16_4d(&a.tm_v, vcache, d, Hkv, max_kv, B, attn::kDecodeStageRows);
+  if (rc != ATTN_OK) return rc;
+  return from_cuda(attn::launch_decode_split(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int attn_decode_split(const attn_bf16_t* q, const attn_bf16_t* kcache, const attn_bf16_t* vcache,
                       const int* kv_lens, int B, int Hq, int Hkv, int d, int max_kv, float scale,
                       int n_splits, int min_rows_per_split, float* part_o, float* part_lse,
@@ -359,17 +381,21 @@ int attn_decode_split(const attn_bf16_t* q, const attn_bf16_t* kcache, const att
   const int rc0 = attn::check_decode_split_args(q, kcache, vcache, kv_lens, B, Hq, Hkv, d, max_kv, scale,
                                                 n_splits, min_rows_per_split, part_o, part_lse, true);
   if (rc0 != ATTN_OK || B == 0) return rc0;
-  attn::DecodeArgs a;
-  std::memset(&a, 0, sizeof(a));
-  a.q = q; a.kv_lens = kv_lens; a.part_o = part_o; a.part_lse = part_lse;
-  a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.d = d; a.max_kv = max_kv;
-  a.n_splits = n_splits; a.min_rows = min_rows_per_split; a.scale = scale;
-  a.err = err_word();
-  if (a.err == nullptr) return ATTN_ERR_CUDA;
-  int rc = encode_bf16_4d(&a.tm_k, kcache, d, Hkv, max_kv, B, attn::kDecodeStageRows);
-  if (rc == ATTN_OK) rc = encode_bf16_4d(&a.tm_v, vcache, d, Hkv, max_kv, B, attn::kDecodeStageRows);
-  if (rc != ATTN_OK) return rc;
-  return from_cuda(attn::launch_decode_split(a, reinterpret_cast<cudaStream_t>(stream)));
+  return decode_launch(q, kcache, vcache, kv_lens, B, Hq, Hkv, d, max_kv, scale, n_splits,
+                       min_rows_per_split, part_o, part_lse, nullptr, nullptr, nullptr, ATTN_F32, stream);
+}
+
+int attn_decode(const attn_bf16_t* q, const attn_bf16_t* kcache, const attn_bf16_t* vcache,
+                const int* kv_lens, int B, int Hq, int Hkv, int d, int max_kv, float scale,
+                int n_splits, int min_rows_per_split, float* part_o, float* part_lse, void* o,
+                float* lse, int o_dtype, unsigned int* counters, attn_stream_t stream) {
+  int rc = attn::check_decode_split_args(q, kcache, vcache, kv_lens, B, Hq, Hkv, d, max_kv, scale,
+                                         n_splits, min_rows_per_split, part_o, part_lse, true);
+  if (rc == ATTN_OK) rc = attn::check_merge_args(part_o, part_lse, o, lse, B, Hq, n_splits, d, o_dtype, true);
+  if (rc != ATTN_OK || B == 0) return rc;
+  if (!counters || (reinterpret_cast<uintptr_t>(counters) & 3u)) return ATTN_ERR_INVALID_ARG;
+  return decode_launch(q, kcache, vcache, kv_lens, B, Hq, Hkv, d, max_kv, scale, n_splits,
+                       min_rows_per_split, part_o, part_lse, counters, o, lse, o_dtype, stream);
 }
 
 int attn_merge(const float* part_o, const float* part_lse, void* o, float* lse, int B, int Hq,
@@ -395,6 +421,20 @@ int attn_sync_check(attn_stream_t stream) {
     return h == attn::kErrBadShape ? ATTN_ERR_DEVICE_INPUT : ATTN_ERR_DEVICE_TIMEOUT;
   }
   return ATTN_OK;
+}
+
+int attn_prefill_schedule(int BH, int Sq, int Skv, int causal, int grid, int* offsets, int* units,
+                          int max_units) {
+  if (BH < 1 || Sq < 0 || Skv < 0 || grid < 1 || max_units < 0 || !offsets || (max_units > 0 && !units))
+    return ATTN_ERR_INVALID_ARG;
+  std::vector<int> sched;
+  const int n = attn::build_prefill_schedule(BH, Sq, Skv, causal ? 1 : 0, grid, sched);
+  if (n < 0) return ATTN_ERR_INVALID_ARG;
+  if (n == 0) return 0;
+  if (n > max_units) return ATTN_ERR_INVALID_ARG;
+  std::memcpy(offsets, sched.data(), sizeof(int) * ((size_t)grid + 1));
+  std::memcpy(units, sched.data() + grid + 1, sizeof(int) * (size_t)n);
+  return n;
 }
 
 int attn_debug_wait_timeout(unsigned long long limit_ns, attn_stream_t stream) {

@@ -205,6 +205,121 @@ __device__ __forceinline__ void consumer_bar_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
 }
 
+// Non-empty splits whose partial rows a merge warp loads at once: eight covers
+// the common split counts in one round trip (four took two on eight splits).
+constexpr int kMergeBatch = 8;
+
+// The LSE-weighted combine of the n_splits partials of one (sequence, query
+// head) row, by one warp: lane = DPL consecutive dims.  The partials are read
+// through L2 (ld.global.cg): in the fused decode other CTAs of the same launch
+// wrote them, and this SM's L1 may not see those writes.
+template <int D>
+__device__ __noinline__ void merge_row(const float* __restrict__ part_o,
+                                          const float* __restrict__ part_lse, void* o,
+                                          float* __restrict__ lse, size_t row, int n_splits,
+                                          int o_bf16, int lane) {
+  constexpr int DPL = D / 32;
+  const float* pl = part_lse + row * n_splits;
+  const float* po = part_o + row * n_splits * D + lane * DPL;
+  float M = -INFINITY;
+  for (int s = lane; s < n_splits; s += 32) M = fmaxf(M, __ldcg(pl + s));
+  M = warp_max(M);
+  float acc[DPL];
+#pragma unroll
+  for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
+  float wsum = 0.f;
+  if (M != -INFINITY) {
+    for (int s0 = 0; s0 < n_splits; s0 += 32) {
+      // lane j holds the weight of split s0 + j (0 for empty or missing splits)
+      const int s = s0 + lane;
+      const float ls = s < n_splits ? __ldcg(pl + s) : -INFINITY;
+      const float w = ls == -INFINITY ? 0.f : ex2_approx((ls - M) * kLog2e);
+      wsum += w;
+      uint32_t live = __ballot_sync(0xFFFFFFFFu, w > 0.f);  // empty splits are never read
+      while (live) {
+        // up to kMergeBatch non-empty splits per round: their loads are issued together
+        int idx[kMergeBatch];
+        float wk[kMergeBatch];
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u) {
+          idx[u] = live ? __ffs(live) - 1 : -1;
+          if (live) live &= live - 1;
+          wk[u] = __shfl_sync(0xFFFFFFFFu, w, idx[u] < 0 ? 0 : idx[u]);
+        }
+        float x[kMergeBatch][DPL];
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u) {
+          if (idx[u] >= 0) {
+            const float* src = po + (size_t)(s0 + idx[u]) * D;
+#pragma unroll
+            for (int e = 0; e < DPL; e += 2) {
+              const float2 v2 = __ldcg(reinterpret_cast<const float2*>(src + e));
+              x[u][e] = v2.x;
+              x[u][e + 1] = v2.y;
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u) {
+          if (idx[u] >= 0) {
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) acc[e] = fmaf(wk[u], x[u][e], acc[e]);
+          }
+        }
+      }
+    }
+    wsum = warp_sum(wsum);
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  if (o_bf16) {
+    uint16_t* dst = reinterpret_cast<uint16_t*>(o) + row * D + lane * DPL;
+#pragma unroll
+    for (int e = 0; e < DPL; e += 2) {
+      *reinterpret_cast<uint32_t*>(dst + e) = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
+    }
+  } else {
+    float* dst = reinterpret_cast<float*>(o) + row * D + lane * DPL;
+#pragma unroll
+    for (int e = 0; e < DPL; e += 2) {
+      *reinterpret_cast<float2*>(dst + e) = make_float2(acc[e] * inv, acc[e + 1] * inv);
+    }
+  }
+  if (lane == 0) lse[row] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
+}
+
+// The combine fused into the split launch ("66 . D2: explicit K+V register
+// staging", section 5.2, without a launch of its own).  The n_splits CTAs that
+// hold the same query heads of a sequence form a group with one completion
+// counter, indexed by the group's first (sequence, query head) row.  Each CTA,
+// once its partials are written, fences them and counts
+// itself; the CTA that takes the count to n_splits merges the group's rows
+// into o and lse and puts the counter back to zero, so the counters are zero
+// again when the launch ends.  Called by the first NWARPS warps of the CTA
+// together; `sync` is their barrier.
+template <int D, int NWARPS, class Sync>
+__device__ __forceinline__ void combine_if_last(unsigned* done, int n_splits,
+                                                const float* part_o, const float* part_lse,
+                                                void* o, float* lse, size_t row0, int G,
+                                                int o_bf16, Sync sync) {
+  __shared__ int last_sh;
+  __threadfence();  // this thread's partials are visible device-wide before the count
+  sync();
+  if (threadIdx.x == 0) {
+    const unsigned prev = atomicAdd(done, 1u);
+    const int last = prev + 1u == (unsigned)n_splits;
+    if (last) {
+      __threadfence();      // the other CTAs' partials are read after their counts
+      atomicExch(done, 0u);  // ready for the next launch
+    }
+    last_sh = last;
+  }
+  sync();
+  if (!last_sh) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int g = warp; g < G; g += NWARPS)
+    merge_row<D>(part_o, part_lse, o, lse, row0 + g, n_splits, o_bf16, lane);
+}
+
 // One CTA per split unit (batch b, KV head hk, split s).  Consumer warp w owns
 // ring stage w and takes tiles w, w+4, w+8, ... of the unit, for all G query
 // heads of the group.  A stage has a K half and a V half with their own
@@ -218,7 +333,8 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<D, GMAX>::kMinBlocks
                         const int* __restrict__ kv_lens, float* __restrict__ part_o,
                         float* __restrict__ part_lse, int Hq, int Hkv, int max_kv, int n_splits,
                         int min_rows, float scale, int heads_per_cta, int ordered, int B,
-                        uint32_t* err) {
+                        uint32_t* err, unsigned* __restrict__ done, void* o,
+                        float* __restrict__ lse, int o_bf16) {
   using C = DecodeCfg<D, GMAX>;
   constexpr int DPL = D / 32;   // output dims per lane in the P.V phase
   constexpr int DP2 = DPL / 2;  // ... as fp32 pairs
@@ -275,6 +391,11 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<D, GMAX>::kMinBlocks
       const int g = i / D, t = i % D;
       part_o[(row_base + (size_t)g * n_splits) * D + t] = 0.f;
       if (t == 0) part_lse[row_base + (size_t)g * n_splits] = -INFINITY;
+    }
+    if (done) {
+      const size_t orow0 = (size_t)b * Hq + (size_t)hk * Gall + g0;
+      combine_if_last<D, kDecodeThreads / 32>(done + orow0, n_splits, part_o, part_lse, o, lse, orow0,
+                                              G, o_bf16, [] { __syncthreads(); });
     }
     return;
   }
@@ -487,105 +608,41 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<D, GMAX>::kMinBlocks
       }
     }
   }
-  consumer_bar_sync();
-  if (!ok || *abort_flag) return;
-  for (int idx = threadIdx.x; idx < G * D; idx += kConsumerWarps * 32) {
-    const int g = idx / D, t = idx % D;
-    float M = -INFINITY;
+  // the four warps agree on whether every wait of the CTA succeeded
+  const bool good = bar_sync_and(1, kConsumerWarps * 32, ok && *abort_flag == 0);
+  if (good) {
+    for (int idx = threadIdx.x; idx < G * D; idx += kConsumerWarps * 32) {
+      const int g = idx / D, t = idx % D;
+      float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, comb[(w * GMAX + g) * (D + 2) + D]);
-    float Lsum = 0.f, acc = 0.f;
+      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, comb[(w * GMAX + g) * (D + 2) + D]);
+      float Lsum = 0.f, acc = 0.f;
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) {
-      const float* cw = comb + (w * GMAX + g) * (D + 2);
-      const float f = ex2_approx(cw[D] - M);  // warps without tiles: m = -inf -> 0
-      Lsum = fmaf(cw[D + 1], f, Lsum);
-      acc = fmaf(cw[t], f, acc);
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        const float* cw = comb + (w * GMAX + g) * (D + 2);
+        const float f = ex2_approx(cw[D] - M);  // warps without tiles: m = -inf -> 0
+        Lsum = fmaf(cw[D + 1], f, Lsum);
+        acc = fmaf(cw[t], f, acc);
+      }
+      const size_t row = row_base + (size_t)g * n_splits;
+      part_o[row * D + t] = acc / Lsum;
+      if (t == 0) part_lse[row] = (M + log2f(Lsum)) * kLn2;
     }
-    const size_t row = row_base + (size_t)g * n_splits;
-    part_o[row * D + t] = acc / Lsum;
-    if (t == 0) part_lse[row] = (M + log2f(Lsum)) * kLn2;
+  }
+  if (done) {  // counted even after a timeout (which the error word reports), so the count stays whole
+    const size_t orow0 = (row_base - s_idx) / n_splits;  // (sequence, first query head) row
+    combine_if_last<D, kConsumerWarps>(done + orow0, n_splits, part_o, part_lse, o, lse, orow0, G,
+                                       o_bf16, [] { consumer_bar_sync(); });
   }
 }
-
-// Non-empty splits whose partial rows a merge warp loads at once: eight covers
-// the common split counts in one round trip (four took two on eight splits).
-constexpr int kMergeBatch = 8;
 
 template <int D>
 __global__ void __launch_bounds__(128)
     merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse, void* o,
                  float* __restrict__ lse, int rows, int n_splits, int o_bf16) {
-  constexpr int DPL = D / 32;
   const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
   if (row >= rows) return;
-  const float* pl = part_lse + (size_t)row * n_splits;
-  const float* po = part_o + (size_t)row * n_splits * D + lane * DPL;
-  float M = -INFINITY;
-  for (int s = lane; s < n_splits; s += 32) M = fmaxf(M, pl[s]);
-  M = warp_max(M);
-  float acc[DPL];
-#pragma unroll
-  for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
-  float wsum = 0.f;
-  if (M != -INFINITY) {
-    for (int s0 = 0; s0 < n_splits; s0 += 32) {
-      // lane j holds the weight of split s0 + j (0 for empty or missing splits)
-      const int s = s0 + lane;
-      const float ls = s < n_splits ? pl[s] : -INFINITY;
-      const float w = ls == -INFINITY ? 0.f : ex2_approx((ls - M) * kLog2e);
-      wsum += w;
-      uint32_t live = __ballot_sync(0xFFFFFFFFu, w > 0.f);  // empty splits are never read
-      while (live) {
-        // up to kMergeBatch non-empty splits per round: their loads are issued together
-        int idx[kMergeBatch];
-        float wk[kMergeBatch];
-#pragma unroll
-        for (int u = 0; u < kMergeBatch; ++u) {
-          idx[u] = live ? __ffs(live) - 1 : -1;
-          if (live) live &= live - 1;
-          wk[u] = __shfl_sync(0xFFFFFFFFu, w, idx[u] < 0 ? 0 : idx[u]);
-        }
-        float x[kMergeBatch][DPL];
-#pragma unroll
-        for (int u = 0; u < kMergeBatch; ++u) {
-          if (idx[u] >= 0) {
-            const float* src = po + (size_t)(s0 + idx[u]) * D;
-#pragma unroll
-            for (int e = 0; e < DPL; e += 2) {
-              const float2 v2 = *reinterpret_cast<const float2*>(src + e);
-              x[u][e] = v2.x;
-              x[u][e + 1] = v2.y;
-            }
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < kMergeBatch; ++u) {
-          if (idx[u] >= 0) {
-#pragma unroll
-            for (int e = 0; e < DPL; ++e) acc[e] = fmaf(wk[u], x[u][e], acc[e]);
-          }
-        }
-      }
-    }
-    wsum = warp_sum(wsum);
-  }
-  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-  if (o_bf16) {
-    uint16_t* dst = reinterpret_cast<uint16_t*>(o) + (size_t)row * D + lane * DPL;
-#pragma unroll
-    for (int e = 0; e < DPL; e += 2) {
-      *reinterpret_cast<uint32_t*>(dst + e) = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
-    }
-  } else {
-    float* dst = reinterpret_cast<float*>(o) + (size_t)row * D + lane * DPL;
-#pragma unroll
-    for (int e = 0; e < DPL; e += 2) {
-      *reinterpret_cast<float2*>(dst + e) = make_float2(acc[e] * inv, acc[e + 1] * inv);
-    }
-  }
-  if (lane == 0) lse[row] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
+  merge_row<D>(part_o, part_lse, o, lse, (size_t)row, n_splits, o_bf16, threadIdx.x & 31);
 }
 
 template <int D, int GMAX, bool SPLIT_HEADS>
@@ -602,13 +659,16 @@ cudaError_t launch_decode_t(const DecodeArgs& a, int heads_per_cta, cudaStream_t
   const int ordered = a.B <= kOrderMaxBatch ? 1 : 0;
   kern<<<(unsigned)ctas, kDecodeThreads, C::kSmemBytes, stream>>>(
       a.tm_k, a.tm_v, a.q, a.kv_lens, a.part_o, a.part_lse, a.Hq, a.Hkv, a.max_kv, a.n_splits,
-      a.min_rows, a.scale, heads_per_cta, ordered, a.B, a.err);
+      a.min_rows, a.scale, heads_per_cta, ordered, a.B, a.err, a.done, a.o, a.lse, a.o_bf16);
   return cudaGetLastError();
 }
 
 // Query heads per CTA.  A launch with fewer than kSmallUnits (batch, KV head,
 // split) units is latency-bound (one sequence of 1641 keys in 8 splits is 32
-// CTAs on 152 SMs), so its head groups are spread over more CTAs.
+// CTAs on 152 SMs), so its head groups are spread over more CTAs.  A CTA holds
+// at most kMaxHeadsPerCta heads (the register budget of the consumer warps);
+// larger groups are always spread, their CTAs reading the same K/V rows (the
+// CTAs of one unit are adjacent, so the re-reads are L2 hits).
 constexpr int kSmallUnits = 128;
 
 template <int D>
@@ -619,6 +679,10 @@ cudaError_t launch_decode_g(const DecodeArgs& a, cudaStream_t stream) {
   if (units < kSmallUnits && G > 1) {
     const int want = (int)((kSmallUnits + units - 1) / units);  // head groups wanted
     const int n_hg = want < G ? want : G;
+    hpc = (G + n_hg - 1) / n_hg;
+  }
+  if (hpc > kMaxHeadsPerCta) {
+    const int n_hg = (G + kMaxHeadsPerCta - 1) / kMaxHeadsPerCta;
     hpc = (G + n_hg - 1) / n_hg;
   }
   if (hpc < G) {

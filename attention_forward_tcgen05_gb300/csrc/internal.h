@@ -2,6 +2,7 @@
 // kernel translation units.  Not part of the public ABI.
 #pragma once
 #include <cstdint>
+#include <vector>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -120,6 +121,13 @@ struct DecodeArgs {
   int B, Hq, Hkv, d, max_kv, n_splits, min_rows;
   float scale;
   uint32_t* err;
+  // fused combine (all null for partials only): completion counters [B * Hq],
+  // one per group at its first (sequence, query head) row, zero on entry and
+  // zero again on exit; and the merged outputs
+  unsigned* done;
+  void* o;       // [B][Hq][d], fp32 or bf16 (o_bf16)
+  float* lse;    // [B][Hq]
+  int o_bf16;
 };
 
 struct MergeArgs {
@@ -133,6 +141,10 @@ struct MergeArgs {
 // Rows of a K / V stage loaded by one TMA box in the decode kernel (two
 // consumer warps share a stage, 32 rows each).
 constexpr int kDecodeStageRows = 64;
+// Query heads one decode CTA computes; a larger GQA group is spread over
+// ceil(G / kMaxHeadsPerCta) CTAs.  kMaxDecodeGroup bounds G = Hq / Hkv.
+constexpr int kMaxHeadsPerCta = 16;
+constexpr int kMaxDecodeGroup = 128;
 // Rows of a Q tile in the prefill kernel, and of one TMA-loaded K / V stage
 // (the kernel may compute on sub-tiles of a stage).
 constexpr int kPrefillTileM = 128;
@@ -163,6 +175,10 @@ cudaError_t launch_prefill_persistent(const PrefillArgs& a, cudaStream_t stream)
 cudaError_t launch_prefill_d512(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill_empty_kv(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_decode_split(const DecodeArgs& a, cudaStream_t stream);
+// The persistent prefill's unit schedule for BH = B * Hq heads over `grid` CTAs:
+// sched = offsets[grid + 1] followed by each CTA's units; returns the unit count,
+// 0 when the launch keeps the wave deal (sched left empty), -1 on bad arguments.
+int build_prefill_schedule(int BH, int Sq, int Skv, int causal, int grid, std::vector<int>& sched);
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);
 cudaError_t launch_wait_timeout_probe(uint64_t limit_ns, uint32_t* err, cudaStream_t stream);
 

@@ -26,7 +26,14 @@
 // Measured on the causal GQA workload (S = 3314, 28 heads): 86.7 -> 82.6 us against
 // one CTA per unit.  Non-causal launches stay on prefill.cu, whose last wave runs as
 // key halves (faster there: 193 against 209 us at d = 64, 222 against 236 at 128).
+#include <algorithm>
+#include <climits>
 #include <cmath>
+#include <map>
+#include <mutex>
+#include <set>
+#include <tuple>
+#include <vector>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -79,7 +86,7 @@ struct PUnit {
   int hq, hk, b;
 };
 
-__device__ __forceinline__ PUnit punit(int u, int Hq, int Hkv, int B, int Sq, int Skv, int causal) {
+__host__ __device__ __forceinline__ PUnit punit(int u, int Hq, int Hkv, int B, int Sq, int Skv, int causal) {
   const int n_blocks_q = (Sq + 2 * kPrefillTileM - 1) / (2 * kPrefillTileM);
   const int HB = Hq * B;
   // causal: heaviest query blocks first; non-causal: the query blocks of one head are
@@ -102,7 +109,8 @@ __device__ __forceinline__ PUnit punit(int u, int Hq, int Hkv, int B, int Sq, in
     }
     int kv_hi = Skv, kv_lo = Skv;
     if (causal) {
-      const long long hi = (long long)(min(Sq, q0 + kPrefillTileM) - 1) + off + 1, lo = (long long)q0 + off + 1;
+      const int q_end = q0 + kPrefillTileM < Sq ? q0 + kPrefillTileM : Sq;
+      const long long hi = (long long)(q_end - 1) + off + 1, lo = (long long)q0 + off + 1;
       kv_hi = (int)(hi < 0 ? 0 : (hi > Skv ? Skv : hi));
       kv_lo = (int)(lo < 0 ? 0 : (lo > Skv ? Skv : lo));
     }
@@ -112,9 +120,15 @@ __device__ __forceinline__ PUnit punit(int u, int Hq, int Hkv, int B, int Sq, in
   return p;
 }
 
-// The k-th unit of CTA c out of `units`, dealt in waves of `grid` units, every other
-// wave in reverse CTA order; -1 once the CTA has none left.
-__device__ __forceinline__ int unit_of(int k, int c, int grid, int units) {
+// The k-th unit of CTA c, or -1 once the CTA has none left.  With a schedule
+// (sched = offsets[grid + 1] followed by the unit lists) CTA c runs
+// sched[grid + 1 + offsets[c] ...]; without one the units are dealt in waves of
+// `grid`, every other wave in reverse CTA order.
+__device__ __forceinline__ int unit_of(int k, int c, int grid, int units, const int* __restrict__ sched) {
+  if (sched != nullptr) {
+    const int i = __ldg(sched + c) + k;
+    return i < __ldg(sched + c + 1) ? __ldg(sched + grid + 1 + i) : -1;
+  }
   const long long u = (long long)k * grid + ((k & 1) ? grid - 1 - c : c);
   return u < units ? (int)u : -1;
 }
@@ -125,7 +139,7 @@ __global__ void __launch_bounds__(PersistCfg<D>::kThreads, 1)
                            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                            int o_tma, void* __restrict__ o_ptr, float* __restrict__ lse_ptr, int B, int Hq,
                            int Hkv, int Sq, int Skv, int causal, int o_bf16, float scale, int units,
-                           uint32_t* err) {
+                           const int* __restrict__ sched, uint32_t* err) {
   using C = PersistCfg<D>;
   constexpr int BN = C::BN;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -191,7 +205,7 @@ __global__ void __launch_bounds__(PersistCfg<D>::kThreads, 1)
       if (lane == 0) tma_prefetch_desc(&tm_q);
       bool ok = true;
       for (int k = 0; ok; ++k) {
-        const int u = unit_of(k, cta, grid, units);
+        const int u = unit_of(k, cta, grid, units, sched);
         if (u < 0) break;
         const PUnit p = punit(u, Hq, Hkv, B, Sq, Skv, causal);
 #pragma unroll
@@ -222,7 +236,7 @@ __global__ void __launch_bounds__(PersistCfg<D>::kThreads, 1)
       int g = 0;  // ring items issued
       bool ok = true;
       for (int k = 0; ok; ++k) {
-        const int u = unit_of(k, cta, grid, units);
+        const int u = unit_of(k, cta, grid, units, sched);
         if (u < 0) break;
         const PUnit p = punit(u, Hq, Hkv, B, Sq, Skv, causal);
         const int n = max(p.n[0], p.n[1]);
@@ -276,7 +290,7 @@ __global__ void __launch_bounds__(PersistCfg<D>::kThreads, 1)
         return true;
       };
       for (int k = 0; ok; ++k) {
-        const int u = unit_of(k, cta, grid, units);
+        const int u = unit_of(k, cta, grid, units, sched);
         if (u < 0) break;
         const PUnit p = punit(u, Hq, Hkv, B, Sq, Skv, causal);
         const int n = max(p.n[0], p.n[1]);
@@ -352,7 +366,7 @@ __global__ void __launch_bounds__(PersistCfg<D>::kThreads, 1)
     int F = 0;  // this tile's units with keys so far (final barrier phases)
     bool ok = true;
     for (int k = 0; ok; ++k) {
-      const int u = unit_of(k, cta, grid, units);
+      const int u = unit_of(k, cta, grid, units, sched);
       if (u < 0) break;
       const PUnit p = punit(u, Hq, Hkv, B, Sq, Skv, causal);
       const int n_t = p.n[t];
@@ -552,6 +566,132 @@ int n_sms() {
   return n;
 }
 
+// ---- the launch's unit schedule (host) ----
+// A unit costs the KV steps of its longer query tile plus kUnitOverheadSteps for
+// what surrounds it (Q load, the lone last step of the shorter tile's partner,
+// the epilogue).  Dealt in waves, the causal units leave the CTAs unequal: their
+// sizes come in a few coarse values (2, 4, ..., 26 steps for 3314 rows), and on
+// the 28-head workload the most loaded of 152 CTAs carries 44 step-equivalents
+// against a mean of 38.3 (at 2 steps of overhead per unit).  Best-fit decreasing
+// -- each unit, largest first, goes to the fullest CTA it still fits into under a
+// capacity, and the capacity is the smallest one for which every unit fits
+// (bisection between the mean and the wave deal's maximum) -- packs them into 40.
+// Each CTA then runs its units largest first.  Measured there (one GB300): wave
+// deal 82.7-84.6 us; packed with an assumed overhead of 0, 1 and 2 steps per
+// unit: 109.2, 88.7-89.8 and 78.5 us.  A fit of those times puts the real
+// overhead near 2 steps; the packing assumes 3, which leaves the 28-head
+// schedule's maximum at 40 if it is 2 and at 42 if it is 3.
+constexpr long long kUnitOverheadSteps = 3;
+// Launches with more units than this per CTA keep the wave deal: the imbalance it
+// leaves is a small part of each CTA's share, and the packing's cost grows.
+constexpr long long kMaxScheduledUnitsPerCta = 64;
+
+bool pack_units(const std::vector<std::pair<long long, int>>& items, int grid, long long cap,
+                std::vector<int>& cta_of) {
+  std::set<std::pair<long long, int>> load;  // (load, CTA)
+  for (int c = 0; c < grid; ++c) load.insert({0, c});
+  for (const auto& it : items) {
+    auto f = load.upper_bound({cap - it.first, INT_MAX});  // first CTA that would overflow
+    if (f == load.begin()) return false;
+    --f;  // the fullest CTA it fits into
+    const std::pair<long long, int> b = *f;
+    load.erase(f);
+    load.insert({b.first + it.first, b.second});
+    cta_of[it.second] = b.second;
+  }
+  return true;
+}
+
+}  // namespace
+
+int build_prefill_schedule(int BH, int Sq, int Skv, int causal, int grid, std::vector<int>& sched) {
+  sched.clear();
+  const long long n_blocks_q = ((long long)Sq + 2 * kPrefillTileM - 1) / (2 * kPrefillTileM);
+  const long long units = n_blocks_q * BH;
+  if (BH < 1 || Sq < 0 || Skv < 0 || grid < 1 || units > 0x7FFFFFFFLL) return -1;
+  if (units > kMaxScheduledUnitsPerCta * grid) return 0;
+  std::vector<std::pair<long long, int>> items((size_t)units);  // (cost, unit)
+  long long total = 0, biggest = 0;
+  for (int u = 0; u < (int)units; ++u) {
+    const PUnit p = punit(u, BH, BH, 1, Sq, Skv, causal);
+    const long long w = (p.n[0] > p.n[1] ? p.n[0] : p.n[1]) + kUnitOverheadSteps;
+    items[u] = {w, u};
+    total += w;
+    biggest = w > biggest ? w : biggest;
+  }
+  // the wave deal's most loaded CTA bounds the capacity from above
+  std::vector<long long> wave(grid, 0);
+  for (int c = 0; c < grid; ++c)
+    for (int k = 0;; ++k) {
+      const long long u = (long long)k * grid + ((k & 1) ? grid - 1 - c : c);
+      if (u >= units) break;
+      wave[c] += items[u].first;
+    }
+  long long hi = *std::max_element(wave.begin(), wave.end());
+  long long lo = std::max((total + grid - 1) / grid, biggest);
+  std::sort(items.begin(), items.end(), [](const auto& a, const auto& b) {
+    return a.first != b.first ? a.first > b.first : a.second < b.second;
+  });
+  std::vector<int> cta_of((size_t)units, -1), best;
+  if (!pack_units(items, grid, hi, cta_of)) return 0;  // keep the wave deal
+  best = cta_of;
+  while (lo < hi) {
+    const long long mid = (lo + hi) / 2;
+    if (pack_units(items, grid, mid, cta_of)) {
+      best = cta_of;
+      hi = mid;
+    } else {
+      lo = mid + 1;
+    }
+  }
+  // offsets, then each CTA's units largest first (items are sorted that way)
+  sched.assign((size_t)grid + 1 + (size_t)units, 0);
+  for (int u = 0; u < (int)units; ++u) sched[best[u] + 1]++;
+  for (int c = 0; c < grid; ++c) sched[c + 1] += sched[c];
+  std::vector<int> fill(sched.begin(), sched.begin() + grid);
+  for (const auto& it : items) sched[grid + 1 + fill[best[it.second]]++] = it.second;
+  return (int)units;
+}
+
+namespace {
+
+// Device copies of the schedules, one per (device, launch shape); built at a
+// shape's first launch and kept until exit.  A launch that is being captured into
+// a graph does not build one (the upload would break the capture): it takes the
+// wave deal unless its shape was launched before.
+struct SchedKey {
+  int dev, BH, Sq, Skv, causal, grid;
+  bool operator<(const SchedKey& o) const {
+    return std::tie(dev, BH, Sq, Skv, causal, grid) < std::tie(o.dev, o.BH, o.Sq, o.Skv, o.causal, o.grid);
+  }
+};
+constexpr size_t kMaxCachedSchedules = 256;
+
+const int* device_schedule(const PrefillArgs& a, int grid, cudaStream_t stream) {
+  static std::mutex mu;
+  static std::map<SchedKey, int*> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  const SchedKey key{dev, a.B * a.Hq, a.Sq, a.Skv, a.causal, grid};
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) return nullptr;
+  if (cache.size() >= kMaxCachedSchedules) return nullptr;
+  std::vector<int> h;
+  int* d = nullptr;
+  if (build_prefill_schedule(key.BH, a.Sq, a.Skv, a.causal, grid, h) > 0) {
+    if (cudaMalloc(&d, h.size() * sizeof(int)) != cudaSuccess) return nullptr;
+    if (cudaMemcpy(d, h.data(), h.size() * sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) {
+      cudaFree(d);
+      return nullptr;
+    }
+  }
+  cache[key] = d;  // nullptr: this shape keeps the wave deal
+  return d;
+}
+
 template <int D>
 cudaError_t launch_persist_t(const PrefillArgs& a, cudaStream_t stream) {
   using C = PersistCfg<D>;
@@ -570,9 +710,10 @@ cudaError_t launch_persist_t(const PrefillArgs& a, cudaStream_t stream) {
   const long long sms = n_sms();
   if (sms <= 0) return cudaErrorInvalidValue;
   const long long grid = units < sms ? units : sms;
+  const int* sched = device_schedule(a, (int)grid, stream);
   kern<<<(unsigned)grid, C::kThreads, C::kSmemBytes, stream>>>(
       a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.o_tma, a.o, a.lse, a.B, a.Hq, a.Hkv, a.Sq, a.Skv, a.causal, a.o_bf16,
-      a.scale, (int)units, a.err);
+      a.scale, (int)units, sched, a.err);
   return cudaGetLastError();
 }
 

@@ -3,13 +3,15 @@
 
 One step = one pass of the whole hot path over one batch of synthetic input:
   1. prefill FMHA on gqa_prefill_3314  (B=1, Hq=28, Hkv=4, S=3314, d=128, causal, O bf16)
-  2. split-KV decode + merge on gqa_decode_1641 (B=1, Hq=28, Hkv=4, KV 1641, 8 splits)
-  3. split-KV decode + merge on ragged_gqa_decode_b64 (B=64, Hq=32, Hkv=8, KV ~ U[512,8192])
+  2. split-KV decode with its merge on gqa_decode_1641 (B=1, Hq=28, Hkv=4, KV 1641,
+     8 splits), one launch: the last split of each query-head group merges
+  3. the same on ragged_gqa_decode_b64 (B=64, Hq=32, Hkv=8, KV ~ U[512,8192])
 Beside the step, each further workload is timed alone and reported on its own
 line object: chunked (varlen) prefill, the sliding window with sinks, the
 128-head multi-query decode and the non-causal head-dim sweep (B=2, H=16,
 S=4096, d = 64, 128, 256, and 512).
-L2 is flushed (a 256 MiB device write) before every step, outside the kernel
+L2 is flushed (a 256 MiB device write, then a 256 MiB read so that no dirty lines
+are left behind) before every step, outside the kernel
 events.  `value` is the prefill throughput in TFLOP/s (algorithmic FLOPs:
 4*d per admissible (query, key) pair); the decode throughput (algorithmic K+V
 bytes, every cached row of every KV head read once) is reported beside it.
@@ -111,6 +113,24 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------- ours
+class L2Flush:
+    """Empties L2 of the timed kernels' data between timed launches: a write of a
+    buffer larger than L2 (256 MiB), then a read of a second one, so that L2 holds
+    clean lines of the second buffer rather than dirty lines of the first (which
+    the next kernel's reads would otherwise have to write back to HBM first)."""
+
+    def __init__(self, dev):
+        import torch
+        self.w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.s = torch.empty((), dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        import torch
+        self.w.zero_()
+        torch.sum(self.r, dim=0, out=self.s)
+
+
 def max_over_ranks(values, world):
     """Element-wise maximum of per-rank timings over all ranks (the slowest replica
     sets the job's time); the identity with one process."""
@@ -134,7 +154,7 @@ def run_line(args):
     torch.cuda.set_device(dev)
     attn.load()
     peaks, peak_src = load_peaks()
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream()
     if args.line.startswith("sweep"):
         return time_sweep(args, attn, W, dev, stream, flush, peaks, peak_src, int(args.line[5:]))
@@ -169,8 +189,10 @@ def run_ours(args, rank, world, local_rank):
                   torch.empty((sh.B, sh.Hq, sh.n_splits), dtype=torch.float32, device=dev)),
             out=(torch.empty((sh.B, sh.Hq, sh.d), dtype=torch.bfloat16, device=dev),
                  torch.empty((sh.B, sh.Hq), dtype=torch.float32, device=dev)),
+            # completion counters of the combine fused into the split launch (zero between calls)
+            counters=torch.zeros(sh.B * sh.Hq, dtype=torch.int32, device=dev),
             kv_bytes=W.decode_kv_bytes(lens, sh.Hkv, sh.d))
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
     flops = W.prefill_flops(P.B, P.Hq, P.Sq, P.Skv, P.d, P.causal)
     stream = torch.cuda.current_stream()
 
@@ -178,7 +200,7 @@ def run_ours(args, rank, world, local_rank):
     do_decode = args.only in (None, "decode")
 
     def step(ev=None):
-        flush.zero_()  # evict L2 (outside the kernel events)
+        flush()  # evict L2 (outside the kernel events)
         if ev is not None:
             ev[0].record(stream)
         if do_prefill:
@@ -190,14 +212,12 @@ def run_ours(args, rank, world, local_rank):
             dd = dec[name]
             sh = dd["shape"]
             qd, kc, vc, lens = dd["dev"]
-            attn.decode_split(qd, kc, vc, lens, sh.n_splits, sh.min_rows_per_split, sh.scale,
-                              out=dd["part"])
+            # split partials and their combine in one launch (attn_decode)
+            attn.decode(qd, kc, vc, lens, sh.n_splits, sh.min_rows_per_split, sh.scale,
+                        torch.bfloat16, out=dd["out"], parts=dd["part"], counters=dd["counters"])
             if ev is not None:
                 ev[i].record(stream)
-            attn.merge(dd["part"][0], dd["part"][1], torch.bfloat16, out=dd["out"])
-            if ev is not None:
-                ev[i + 1].record(stream)
-            i += 2
+            i += 1
         if not do_decode and ev is not None:
             for e in ev[2:]:
                 e.record(stream)
@@ -212,7 +232,7 @@ def run_ours(args, rank, world, local_rank):
             import torch.distributed as dist
             dist.barrier()
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     with ClockSampler(local_rank) as sampler:
@@ -232,15 +252,13 @@ def run_ours(args, rank, world, local_rank):
         return sum(evs[s][a].elapsed_time(evs[s][b]) for s in range(args.steps)) / args.steps
 
     t_prefill = avg(0, 1)
-    t_split3 = avg(1, 2)
-    t_merge3 = avg(2, 3)
-    t_split5 = avg(3, 4)
-    t_merge5 = avg(4, 5)
-    ms_step = t_prefill + t_split3 + t_merge3 + t_split5 + t_merge5
+    t_dec3 = avg(1, 2)
+    t_dec5 = avg(2, 3)
+    ms_step = t_prefill + t_dec3 + t_dec5
     wall_ms = t_start.elapsed_time(t_end)
 
     ms_step, t_prefill_max, t_dec5_max, wall_ms = max_over_ranks(
-        [ms_step, t_prefill, t_split5 + t_merge5, wall_ms], world)
+        [ms_step, t_prefill, t_dec5, wall_ms], world)
 
     # ---- packed variable-length prefill (chunked prefill against a KV cache) ----
     varlen = None if args.only else time_varlen(args, attn, W, dev, stream, flush, peaks, peak_src)
@@ -261,13 +279,13 @@ def run_ours(args, rank, world, local_rank):
     kv5 = dec[D5.name]["kv_bytes"]
     kv3 = dec[D3.name]["kv_bytes"]
     dec_gbs = world * kv5 / (max(t_dec5_max, 1e-9) * 1e-3) / 1e9
-    split_gbs = kv5 / (max(t_split5, 1e-9) * 1e-3) / 1e9
+    split_gbs = kv5 / (max(t_dec5, 1e-9) * 1e-3) / 1e9
     peak_tc = float(peaks["bf16_tflops"])
     peak_hbm = float(peaks["hbm_gbs"])
     traffic = load_traffic()
     # one roofline per hot kernel; the top-level one is the kernel that takes the
     # largest share of the step's device time
-    pkern = prefill_kernel_name(P.d)
+    pkern = prefill_kernel_name(P.d, P.causal)
     prefill_roof = {"bound": "tensor", "kernel": pkern, "workload": P.name,
                     "achieved": round(prefill_tflops / world, 2), "peak": peak_tc,
                     "unit": "TFLOP/s", "frac": round(prefill_tflops / world / peak_tc, 4),
@@ -278,16 +296,16 @@ def run_ours(args, rank, world, local_rank):
                    "achieved": round(split_gbs, 1), "peak": peak_hbm, "unit": "GB/s",
                    "frac": round(split_gbs / peak_hbm, 4),
                    # keyed by split policy too: a capture holds for the grid it was taken on
-                   "traffic": traffic.get(f"decode_split_kernel<128,4> {D5.name} "
+                   "traffic": traffic.get(f"decode_split_kernel<128,4> fused {D5.name} "
                                           f"{D5.n_splits}x{D5.min_rows_per_split}"),
-                   "step_share": round(t_split5 / ms_step, 4),
+                   "step_share": round(t_dec5 / ms_step, 4),
                    "peak_source": f"hbm_gbs of {peak_src}"}
     if not do_decode:
         dominant_roof = prefill_roof
     elif not do_prefill:
         dominant_roof = decode_roof
     else:
-        dominant_roof = prefill_roof if t_prefill >= t_split5 else decode_roof
+        dominant_roof = prefill_roof if t_prefill >= t_dec5 else decode_roof
     line = {
         "metric": METRIC,
         "value": round(prefill_tflops, 2),
@@ -309,21 +327,22 @@ def run_ours(args, rank, world, local_rank):
                    "decode_ragged": {"B": D5.B, "Hq": D5.Hq, "Hkv": D5.Hkv, "d": D5.d,
                                      "kv_len_range": list(D5.len_range), "n_splits": D5.n_splits,
                                      "min_rows_per_split": D5.min_rows_per_split},
-                   "l2": "flushed before every step (256 MiB device write)",
+                   "l2": "flushed before every step (256 MiB device write, then a 256 MiB read)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": dominant_roof,
         "rooflines": {"prefill": prefill_roof, "decode_split": decode_roof},
         "decode": {"value": round(dec_gbs, 1), "unit": "GB/s", "workload": D5.name,
-                   "kv_bytes": kv5, "split_us": round(t_split5 * 1e3, 2),
-                   "merge_us": round(t_merge5 * 1e3, 2),
+                   "kv_bytes": kv5, "decode_us": round(t_dec5 * 1e3, 2),
+                   "launches": "one: split partials and their combine (attn_decode)",
                    "roofline": decode_roof,
-                   "gqa_decode_1641": {"split_us": round(t_split3 * 1e3, 2),
-                                       "merge_us": round(t_merge3 * 1e3, 2),
+                   "gqa_decode_1641": {"decode_us": round(t_dec3 * 1e3, 2),
                                        "kv_bytes": kv3,
-                                       "GB_per_s": round(kv3 / (max(t_split3 + t_merge3, 1e-9) * 1e-3) / 1e9, 1)}},
+                                       "traffic": traffic.get(f"decode_split_kernel<128,4> fused {D3.name} "
+                                                              f"{D3.n_splits}x{D3.min_rows_per_split}"),
+                                       "GB_per_s": round(kv3 / (max(t_dec3, 1e-9) * 1e-3) / 1e9, 1)}},
         "prefill_us": round(t_prefill * 1e3, 2),
         "wall_ms_timed_region": round(wall_ms, 3),
-        "gpu_launches": (int(do_prefill) + 4 * int(do_decode)) * args.steps,
+        "gpu_launches": (int(do_prefill) + 2 * int(do_decode)) * args.steps,
         "e2e": e2e,
         "prefill_varlen": varlen,
         "prefill_window": window,
@@ -355,7 +374,7 @@ def time_varlen(args, attn, W, dev, stream, flush, peaks, peak_src):
     n = max(1, min(args.steps, 50))
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
     for a, b in evs:
-        flush.zero_()
+        flush()
         a.record(stream)
         call()
         b.record(stream)
@@ -394,7 +413,7 @@ def time_window(args, attn, W, dev, stream, flush, peaks, peak_src):
     n = max(1, min(args.steps, 50))
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
     for a, b in evs:
-        flush.zero_()
+        flush()
         a.record(stream)
         call()
         b.record(stream)
@@ -433,7 +452,7 @@ def time_sweep(args, attn, W, dev, stream, flush, peaks, peak_src, d):
     n = max(1, min(args.steps, 50))
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
     for a, b in evs:
-        flush.zero_()
+        flush()
         a.record(stream)
         call()
         b.record(stream)
@@ -442,7 +461,7 @@ def time_sweep(args, attn, W, dev, stream, flush, peaks, peak_src, d):
     ms = sum(a.elapsed_time(b) for a, b in evs) / n
     tf = flops / (ms * 1e-3) / 1e12
     peak_tc = float(peaks["bf16_tflops"])
-    kern = prefill_kernel_name(P.d)
+    kern = prefill_kernel_name(P.d, P.causal)
     line = {"workload": P.name, "B": P.B, "Hq": P.Hq, "Hkv": P.Hkv, "S": P.Sq, "d": P.d,
             "causal": P.causal, "gflop": round(flops / 1e9, 3), "us": round(ms * 1e3, 2),
             "value": round(tf, 2), "unit": "TFLOP/s", "steps": n,
@@ -458,11 +477,14 @@ def time_sweep(args, attn, W, dev, stream, flush, peaks, peak_src, d):
     return line
 
 
-def prefill_kernel_name(d: int) -> str:
-    """The kernel that runs a fixed-length prefill of head dim d."""
+def prefill_kernel_name(d: int, causal: bool = False) -> str:
+    """The kernel that runs a fixed-length prefill of head dim d (causal launches of
+    head dims 64 and 128 run on the persistent kernel)."""
     if d == 512:
         return "fmha_d512_kernel"
-    return f"fmha_pair_kernel<{d}>" if d == 256 else f"fmha_fwd_kernel<{d}>"
+    if d == 256:
+        return f"fmha_pair_kernel<{d}>"
+    return f"fmha_persistent_kernel<{d}>" if causal else f"fmha_fwd_kernel<{d}>"
 
 
 def time_mqa_decode(args, attn, W, dev, stream, flush, peaks, peak_src):
@@ -487,7 +509,7 @@ def time_mqa_decode(args, attn, W, dev, stream, flush, peaks, peak_src):
     n = max(1, min(args.steps, 50))
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
     for a, b in evs:
-        flush.zero_()
+        flush()
         a.record(stream)
         call()
         b.record(stream)

@@ -151,7 +151,7 @@ int attn_prefill_packed(const attn_bf16_t* q, const attn_bf16_t* k, const attn_b
  * rows of one MMA tile (the FMHA page's D2), so a decode step of G >= 8 heads per
  * KV head runs on tcgen05 instead of CUDA cores; one unit of work per (sequence,
  * KV head) streams that sequence's keys once.  Requires d in {64, 128} and G
- * dividing 128 (any G up to 128, so also MQA groups larger than attn_decode_split's 16).
+ * dividing 128 (any G up to 128).
  *
  * Arguments
  *   q         bf16 [B][Hq][d]
@@ -271,7 +271,7 @@ int attn_prefill_varlen_window(const attn_bf16_t* q, const attn_bf16_t* kcache,
  *   vcache    bf16 [B][max_kv][Hkv][d]    values
  *   kv_lens   int32 [B] (device)          L_b, 0 <= L_b <= max_kv (values are trusted
  *                                         to be in range; they are clamped on the device)
- *   B, Hq, Hkv, d, max_kv                 B >= 0, Hq % Hkv == 0, Hq/Hkv <= 16, d in {64,128,256},
+ *   B, Hq, Hkv, d, max_kv                 B >= 0, Hq % Hkv == 0, Hq/Hkv <= 128, d in {64,128,256},
  *                                         max_kv >= 1
  *   scale                                 softmax scale (finite, > 0)
  *   n_splits                              >= 1 and <= 1024; B * Hkv * n_splits <= 2^31 - 1
@@ -302,6 +302,35 @@ int attn_decode_split(const attn_bf16_t* q, const attn_bf16_t* kcache, const att
  */
 int attn_merge(const float* part_o, const float* part_lse, void* o, float* lse, int B, int Hq,
                int n_splits, int d, int o_dtype, attn_stream_t stream);
+
+/*
+ * attn_decode -- one-token GQA decode: the split-KV partials and their
+ * LSE-weighted combine in a single launch.
+ *
+ * Computes what attn_decode_split followed by attn_merge computes, with the
+ * same arguments, split rule and layouts, and writes the same part_o /
+ * part_lse on the way; o and lse are bit-identical to those two calls.  The
+ * n_splits CTAs that hold the same query heads of a sequence form a group:
+ * each writes its partials, makes them visible device-wide and counts itself
+ * on the group's counter, and the CTA whose count completes the group merges
+ * its rows (the merge of attn_merge) and sets the counter back to zero.  This
+ * is the split-combine step of "66 . D2: explicit K+V register staging",
+ * section 5.2, run by the split kernel itself instead of a second launch.
+ *
+ * Arguments: those of attn_decode_split and of attn_merge (o, lse, o_dtype), plus
+ *   counters  uint32 [B * Hq] (device, 4-byte aligned): completion counters.
+ *             The caller zeroes them once; every call that completes leaves them
+ *             zero, so one buffer serves any number of calls in sequence.  Calls
+ *             that may run at the same time (on streams not ordered with each
+ *             other) need buffers of their own.  After an error reported by
+ *             attn_sync_check their contents are undefined: zero them again.
+ * Returns ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED or ATTN_ERR_CUDA;
+ * device-side errors are reported by attn_sync_check as for attn_decode_split.
+ */
+int attn_decode(const attn_bf16_t* q, const attn_bf16_t* kcache, const attn_bf16_t* vcache,
+                const int* kv_lens, int B, int Hq, int Hkv, int d, int max_kv, float scale,
+                int n_splits, int min_rows_per_split, float* part_o, float* part_lse, void* o,
+                float* lse, int o_dtype, unsigned int* counters, attn_stream_t stream);
 
 /*
  * attn_decode_noalloc -- attn_decode_split followed by attn_merge, for callers
@@ -362,6 +391,23 @@ const char* attn_strerror(int status);
 
 /* Library version, major * 10000 + minor * 100 + patch. */
 int attn_version(void);
+
+/*
+ * attn_prefill_schedule -- the unit schedule the causal fixed-length prefill
+ * runs on (host only: no GPU, no CUDA call).  (The pages have no counterpart:
+ * it is how this library spreads work over SMs.)
+ *
+ * A unit is one 256-row query block of one (sequence, query head); the launch
+ * runs one CTA per SM, each walking a list of units.  For BH = B * Hq heads, Sq
+ * query rows and Skv keys on `grid` CTAs this writes offsets[grid + 1] and
+ * units[n] (CTA c runs units[offsets[c] .. offsets[c+1]), in that order) and
+ * returns n = ceil(Sq / 256) * BH.  Unit u is query block
+ * ceil(Sq / 256) - 1 - u / BH of head u % BH.  Returns 0 (nothing written) when
+ * the launch deals its units in waves instead (more than 64 units per CTA);
+ * ATTN_ERR_INVALID_ARG for bad arguments or max_units < n.
+ */
+int attn_prefill_schedule(int BH, int Sq, int Skv, int causal, int grid, int* offsets, int* units,
+                          int max_units);
 
 /*
  * attn_debug_wait_timeout -- test hook for the bounded-wait machinery.

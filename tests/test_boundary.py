@@ -147,7 +147,7 @@ def test_decode_and_merge_validation(lib):
     f = attn.attn_decode_split
     assert f(P, P, P, P, 1, 28, 4, 96, 10, 0.1, 8, 1, P, P, N) == attn.ATTN_ERR_UNSUPPORTED
     assert f(P, P, P, P, 1, 28, 5, 128, 10, 0.1, 8, 1, P, P, N) == attn.ATTN_ERR_INVALID_ARG
-    assert f(P, P, P, P, 1, 34, 2, 128, 10, 0.1, 8, 1, P, P, N) == attn.ATTN_ERR_INVALID_ARG  # G > 16
+    assert f(P, P, P, P, 1, 258, 2, 128, 10, 0.1, 8, 1, P, P, N) == attn.ATTN_ERR_INVALID_ARG  # G > 128
     assert f(P, P, P, P, 1, 28, 4, 128, 10, 0.1, 0, 1, P, P, N) == attn.ATTN_ERR_INVALID_ARG  # n_splits
     assert f(P, P, P, P, 1, 28, 4, 128, 0, 0.1, 8, 1, P, P, N) == attn.ATTN_ERR_INVALID_ARG  # max_kv
     assert f(P, P, P, N, 1, 28, 4, 128, 10, 0.1, 8, 1, P, P, N) == attn.ATTN_ERR_INVALID_ARG  # lens
@@ -159,6 +159,24 @@ def test_decode_and_merge_validation(lib):
     assert g(P, P, P, P, 1, 4, 0, 128, 1, N) == attn.ATTN_ERR_INVALID_ARG
     assert g(P, P, M, P, 1, 4, 8, 128, 1, N) == attn.ATTN_ERR_INVALID_ARG
     assert g(N, N, N, N, 0, 4, 8, 128, 1, N) == attn.ATTN_OK
+
+
+def test_fused_decode_validation(lib):
+    """attn_decode takes the rules of attn_decode_split and attn_merge, and needs a
+    4-byte aligned counter buffer."""
+    f = attn.attn_decode
+    C = ctypes.c_void_p(20)  # 4-byte aligned counters
+    #      q  kc vc kv B  Hq Hkv d    mkv scale ns mr po pl o  lse dtype ctr stream
+    assert f(P, P, P, P, 1, 28, 4, 128, 10, 0.1, 8, 1, P, P, P, P, 1, N, N) == attn.ATTN_ERR_INVALID_ARG
+    assert f(P, P, P, P, 1, 28, 4, 128, 10, 0.1, 8, 1, P, P, P, P, 1, M, N) == attn.ATTN_ERR_INVALID_ARG
+    assert f(P, P, P, P, 1, 28, 4, 96, 10, 0.1, 8, 1, P, P, P, P, 1, C, N) == attn.ATTN_ERR_UNSUPPORTED
+    assert f(P, P, P, P, 1, 28, 4, 128, 10, 0.1, 8, 1, P, P, P, P, 7, C, N) == attn.ATTN_ERR_UNSUPPORTED
+    assert f(P, P, P, P, 1, 258, 2, 128, 10, 0.1, 8, 1, P, P, P, P, 1, C, N) == attn.ATTN_ERR_INVALID_ARG
+    assert f(P, P, P, P, 1, 28, 4, 128, 10, 0.1, 0, 1, P, P, P, P, 1, C, N) == attn.ATTN_ERR_INVALID_ARG
+    assert f(P, P, P, P, 1, 28, 4, 128, 10, 0.1, 8, 1, N, P, P, P, 1, C, N) == attn.ATTN_ERR_INVALID_ARG
+    assert f(P, P, P, P, 1, 28, 4, 128, 10, 0.1, 8, 1, P, P, M, P, 1, C, N) == attn.ATTN_ERR_INVALID_ARG
+    assert f(P, P, P, P, 1, 28, 4, 128, 10, 0.1, 8, 1, P, P, P, N, 1, C, N) == attn.ATTN_ERR_INVALID_ARG
+    assert f(N, N, N, N, 0, 28, 4, 128, 10, 0.1, 8, 1, N, N, N, N, 1, N, N) == attn.ATTN_OK
 
 
 def test_debug_wait_limits(lib):
@@ -185,7 +203,7 @@ def test_noalloc_validation(lib):
     assert f(P, P, P, P, B, Hq, Hkv, d, 16, 0.1, n_splits, 1, P, N, 1, N) == attn.ATTN_ERR_INVALID_ARG
     assert f(P, P, P, P, B, Hq, Hkv, 96, 16, 0.1, n_splits, 1, P, P, 1, N) == attn.ATTN_ERR_UNSUPPORTED
     assert f(P, P, P, P, B, Hq, Hkv, d, 16, 0.1, n_splits, 1, P, P, 5, N) == attn.ATTN_ERR_UNSUPPORTED
-    assert f(P, P, P, P, B, 34, 2, d, 16, 0.1, n_splits, 1, P, P, 1, N) == attn.ATTN_ERR_INVALID_ARG  # G > 16
+    assert f(P, P, P, P, B, 258, 2, d, 16, 0.1, n_splits, 1, P, P, 1, N) == attn.ATTN_ERR_INVALID_ARG  # G > 128
     assert f(P, P, P, P, B, Hq, Hkv, d, 16, 0.1, 2000, 1, P, P, 1, N) == attn.ATTN_ERR_INVALID_ARG  # n_splits
     # the rules shared with attn_decode_split on a problem that fits
     assert f(P, P, P, N, 2, 8, 2, 64, 16, 0.1, 4, 1, P, P, 1, N) == attn.ATTN_ERR_INVALID_ARG  # null kv_lens
