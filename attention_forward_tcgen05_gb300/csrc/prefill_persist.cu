@@ -21,8 +21,11 @@
 // out first and each CTA gets a mix of long and short ones).
 //
 // Barrier phases run on across units: the K/V rings count items, the S, P and O
-// barriers of a tile count its KV steps, its Q and Q-free barriers count units, its
-// final barrier the units in which it has keys, and the staging barrier the turns.
+// barriers of a tile count its KV steps, its Q, Q-free and final barriers the units
+// in which it has keys, and the staging barrier the turns.  (Counted by unit, the
+// Q-free phases of key-less units were completed by the MMA warp without a wait, so
+// it could run two phases ahead of the Q warp; and a tcgen05.commit issued before
+// the CTA's first MMA was seen not to arrive.)
 // Measured on the causal GQA workload (S = 3314, 28 heads): 86.7 -> 82.6 us against
 // one CTA per unit.  Non-causal launches stay on prefill.cu, whose last wave runs as
 // key halves (faster there: 193 against 209 us at d = 64, 222 against 236 at 128).
@@ -202,26 +205,27 @@ __global__ void __launch_bounds__(PersistCfg<D>::kThreads, 1)
     setmaxnreg_dec<C::kCtlRegs>();
     if (warp == C::kQWarp) {
       // ----------------- Q producer: each unit's two Q tiles -----------------
+      // A tile's Q and Q-free phases count the units in which it has keys (a tile
+      // without rows or keys loads nothing and is not waited for).
       if (lane == 0) tma_prefetch_desc(&tm_q);
       bool ok = true;
+      int m[2] = {0, 0};  // Q tiles loaded so far
       for (int k = 0; ok; ++k) {
         const int u = unit_of(k, cta, grid, units, sched);
         if (u < 0) break;
         const PUnit p = punit(u, Hq, Hkv, B, Sq, Skv, causal);
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-          // the tile's Q buffer is free once its last S MMA of the previous unit is done
-          if (k > 0 && !(ok = mbar_wait_warp(&bar_qfree[t], (uint32_t)(k - 1) & 1u, err, abort_flag))) break;
-          if (p.n[t] > 0) {
-            mbar_arrive_expect_tx_e(&bar_q[t], C::kTileBytes);
+          if (!ok || p.n[t] == 0) continue;
+          // the tile's Q buffer is free once the last S MMA of its previous load is done
+          if (m[t] > 0 && !(ok = mbar_wait_warp(&bar_qfree[t], (uint32_t)(m[t] - 1) & 1u, err, abort_flag)))
+            break;
+          mbar_arrive_expect_tx_e(&bar_q[t], C::kTileBytes);
 #pragma unroll
-            for (int pn = 0; pn < C::kPanels; ++pn)
-              tma_load_5d_e(sQ + t * C::kTileBytes + pn * C::kPanelBytes, &tm_q, &bar_q[t], pn * 64, 0, p.hq,
-                            p.q0[t], p.b);
-          } else {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar_q[t]);  // no rows or no keys: the phase still completes
-          }
+          for (int pn = 0; pn < C::kPanels; ++pn)
+            tma_load_5d_e(sQ + t * C::kTileBytes + pn * C::kPanelBytes, &tm_q, &bar_q[t], pn * 64, 0, p.hq,
+                          p.q0[t], p.b);
+          ++m[t];
         }
       }
     } else if (warp == C::kKWarp || warp == C::kVWarp) {
@@ -265,6 +269,7 @@ __global__ void __launch_bounds__(PersistCfg<D>::kThreads, 1)
       const uint64_t dv0 = smem_desc(smem_u32(sV), C::kPanelBytes, 1024, kSwizzle128B);
       int gk = 0, gv = 0;   // ring items consumed
       int J[2] = {0, 0};    // KV steps of each tile so far (S, P and O barrier phases)
+      int mq[2] = {0, 0};   // units with keys of each tile so far (Q and Q-free phases)
       bool ok = true;
       // S_t = Q_t K(item gk)^T into tile t's S buffer
       auto issue_s = [&](int t) {
@@ -298,7 +303,7 @@ __global__ void __launch_bounds__(PersistCfg<D>::kThreads, 1)
           // this unit's Q tiles and its first K tile
 #pragma unroll
           for (int t = 0; t < 2; ++t)
-            if (ok && p.n[t] > 0) ok = mbar_wait_warp(&bar_q[t], (uint32_t)k & 1u, err, abort_flag);
+            if (ok && p.n[t] > 0) ok = mbar_wait_warp(&bar_q[t], (uint32_t)mq[t] & 1u, err, abort_flag);
           if (ok) ok = mbar_wait_warp(&bar_fullK[gk % C::kStagesK], (uint32_t)(gk / C::kStagesK) & 1u, err, abort_flag);
           tc_fence_after();
           if (!ok) break;
@@ -344,10 +349,8 @@ __global__ void __launch_bounds__(PersistCfg<D>::kThreads, 1)
             ++gv;
           }
         }
-        // a tile with no KV tile in this unit still completes its Q-free phase
 #pragma unroll
-        for (int t = 0; t < 2; ++t)
-          if (p.n[t] == 0) mma_commit_e(&bar_qfree[t]);
+        for (int t = 0; t < 2; ++t) mq[t] += p.n[t] > 0 ? 1 : 0;
         J[0] += p.n[0];
         J[1] += p.n[1];
       }

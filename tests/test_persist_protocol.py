@@ -3,14 +3,14 @@
 One CTA walks a sequence of units; unit k has two query tiles with n0 and n1 KV
 tiles (a causal unit has n1 = n0 + 1; a tile past the end or without keys has 0).
 Roles and barriers, with their phases running on across units:
-  * the Q warp: for each unit and tile, waits until the tile's last S MMA of the
-    previous unit has completed (Qfree), then loads the tile's Q (Q barrier; a
-    tile without keys completes the phase with a plain arrival);
+  * the Q warp: for each unit in which a tile has keys, waits until the tile's
+    last S MMA of its previous such unit has completed (Qfree), then loads the
+    tile's Q (Q barrier): both barriers count the tile's units with keys;
   * the K and V warps: one ring each, items in unit order, max(n0, n1) per unit;
-  * the MMA warp: per unit waits for the Q tiles and the first K item, issues S of
-    both tiles, then per step V, and per tile P.V (after P) and the next S; it
-    commits Qfree after a tile's last S of the unit (at the end of the unit for a
-    tile without keys), and Fin after its last P.V;
+  * the MMA warp: per unit waits for the Q tiles with keys and the first K item,
+    issues S of both tiles, then per step V, and per tile P.V (after P) and the
+    next S; it commits Qfree after a tile's last S of the unit, and Fin after its
+    last P.V;
   * two softmax warpgroups: per unit and step wait S, maybe rescale (waiting for
     the previous P.V on O), publish P with four arrivals; then wait Fin (its phases
     count the tile's units with keys) and take the O staging tile in turn with the
@@ -19,6 +19,14 @@ The model checks every wait for soundness (its barrier has completed exactly the
 phases before the awaited one, or that one too), that the pipeline drains, that
 no S MMA of a unit is issued before its tile's Q has landed and that a tile's O
 is not read before its last P.V completed.
+
+A tcgen05.commit issued before the CTA's first MMA does not arrive (a CTA whose
+first units had no keys timed out on its Q-free barrier): the model's commits
+follow that rule.  The earlier form, Q and Q-free phases counted by unit with
+key-less tiles completing them (a plain arrival on Q, a commit on Q-free), is
+kept as a negative case: it needs that commit, and even with a plain arrival its
+MMA warp can complete Q-free phases of consecutive key-less units two ahead of
+the Q warp's wait.
 """
 import heapq
 import itertools
@@ -29,10 +37,12 @@ import pytest
 from tests.test_prefill_protocol import Bar
 
 
-def simulate(units, SK, SV, seed, fin_by_unit=False):
+def simulate(units, SK, SV, seed, fin_by_unit=False, q_by_unit=None):
     """units: [(n0, n1), ...] of one CTA.  fin_by_unit=True waits for the final
     barrier with the unit index as its phase (wrong when a tile has no keys in
-    some unit): the model must catch it."""
+    some unit).  q_by_unit counts the Q and Q-free phases by unit, key-less tiles
+    completing them with a commit ("commit") or a plain arrival ("arrive") on
+    Q-free: the model must catch all three."""
     rng = random.Random(seed)
     bars = {}
 
@@ -50,21 +60,29 @@ def simulate(units, SK, SV, seed, fin_by_unit=False):
     def at(time, fn):
         heapq.heappush(events, (time, next(seq), fn))
 
+    n_mma = [0]
+
     def mma(dur):
         mma_free[0] = max(now[0], mma_free[0]) + dur
+        n_mma[0] += 1
 
     def commit(b):
-        at(mma_free[0], b.arrive)
+        if n_mma[0] > 0:  # a commit before the first MMA never arrives
+            at(mma_free[0], b.arrive)
 
     def wait(b, parity, use):
         assert b.done in (use, use + 1), f"{b.name}: waiting for phase {use} with {b.done} done"
         return ("wait", b, parity)
 
     def q_warp():
+        m = [0, 0]
         for k, ns in enumerate(units):
             for t in range(2):
-                if k > 0:
-                    yield wait(bar(("qfree", t)), (k - 1) & 1, k - 1)
+                if ns[t] == 0 and not q_by_unit:
+                    continue
+                ph = k if q_by_unit else m[t]
+                if ph > 0:
+                    yield wait(bar(("qfree", t)), (ph - 1) & 1, ph - 1)
                 b = bar(("q", t))
                 if ns[t] > 0:
                     b.expect_tx(1)
@@ -73,6 +91,7 @@ def simulate(units, SK, SV, seed, fin_by_unit=False):
                         q_loaded[(t, k)] = True
                         b.complete_tx(1)
                     at(now[0] + rng.randint(100, 3000), land)
+                    m[t] += 1
                 else:
                     b.arrive()
 
@@ -98,12 +117,14 @@ def simulate(units, SK, SV, seed, fin_by_unit=False):
                 mma(rng.randint(20, 80))
             commit(bar(("S", t)))
 
+        mq = [0, 0]
         for k, ns in enumerate(units):
             n = max(ns)
             if n > 0:
                 for t in range(2):
                     if ns[t] > 0:
-                        yield wait(bar(("q", t)), k & 1, k)
+                        ph = k if q_by_unit else mq[t]
+                        yield wait(bar(("q", t)), ph & 1, ph)
                 s, u = gk % SK, gk // SK
                 yield wait(bar(("fK", s)), u & 1, u)
                 for t in range(2):
@@ -140,8 +161,12 @@ def simulate(units, SK, SV, seed, fin_by_unit=False):
                     commit(bar(("eV", sv)))
                     gv += 1
             for t in range(2):
-                if ns[t] == 0:
+                if ns[t] > 0:
+                    mq[t] += 1
+                elif q_by_unit == "commit":
                     commit(bar(("qfree", t)))
+                elif q_by_unit == "arrive":
+                    bar(("qfree", t)).arrive()
             J[0] += ns[0]
             J[1] += ns[1]
 
@@ -227,6 +252,11 @@ SEQUENCES = {
     "no_keys": [(0, 0), (3, 3), (0, 1), (2, 0), (0, 0)],
     "single": [(1, 1)],
     "ones": [(1, 2), (1, 1), (1, 0), (0, 1)],
+    # units without keys before the CTA's first MMA (a packed schedule gives a CTA
+    # only such units, or puts them first)
+    "keyless_only": [(0, 0), (0, 0), (0, 0), (0, 0)],
+    "keyless_first": [(0, 0), (0, 0), (2, 3), (0, 1)],
+    "one_tile_first": [(0, 1), (1, 0), (0, 0)],
 }
 RINGS = [(2, 2), (4, 4), (1, 1), (3, 2)]
 
@@ -244,3 +274,54 @@ def test_final_barrier_phase_by_unit_is_unsound():
     with pytest.raises(AssertionError):
         for seed in range(40):
             simulate([(0, 2), (3, 3), (2, 2)], 2, 2, seed, fin_by_unit=True)
+
+
+@pytest.mark.parametrize("units", [[(0, 0), (0, 0), (0, 0)], [(0, 0), (2, 3)]])
+def test_commit_before_first_mma_is_caught(units):
+    """Completing a key-less tile's Q-free phase with a commit before any MMA leaves
+    the Q warp waiting forever on a CTA whose first units have no keys."""
+    with pytest.raises(AssertionError):
+        simulate(units, 2, 2, 0, q_by_unit="commit")
+
+
+def test_key_less_units_racing_ahead_is_caught():
+    """Counted by unit, consecutive key-less units let the MMA warp complete Q-free
+    phases without waiting, two ahead of the Q warp's wait, whose parity then
+    aliases."""
+    with pytest.raises(AssertionError):
+        for seed in range(40):
+            simulate([(0, 0), (0, 0), (0, 0), (0, 0)], 2, 2, seed, q_by_unit="arrive")
+
+
+def _unit_tiles(u, BH, Sq, Skv):
+    """(n0, n1) of causal unit u: KV tiles of its two query tiles (0 past the end or
+    without keys), as the kernel derives them."""
+    nb = -(-Sq // 256)
+    qb = nb - 1 - u // BH
+    out = []
+    for t in range(2):
+        q0 = qb * 256 + t * 128
+        if q0 >= Sq:
+            out.append(0)
+            continue
+        hi = max(0, min(Skv, min(Sq, q0 + 128) - 1 + (Skv - Sq) + 1))
+        out.append(-(-hi // 128))
+    return tuple(out)
+
+
+@pytest.mark.parametrize("BH,Sq,Skv", [(16, 2900, 2900), (60, 1000, 1300), (64, 1100, 700), (40, 2048, 2048),
+                                       (28, 3314, 3314)])
+def test_host_schedules_are_sound(BH, Sq, Skv):
+    """The unit lists the host schedule gives 152 CTAs for the persistent-kernel test
+    shapes and the 3314-row workload (CTAs with no units, with key-less units only,
+    or key-less units first among them), each replayed through the model."""
+    import attention_forward_tcgen05_gb300 as attn
+    from attention_forward_tcgen05_gb300 import build as attn_build
+    attn_build.build()
+    attn.load()
+    sched = attn.prefill_schedule(BH, Sq, Skv, True, 152)
+    seqs = {tuple(_unit_tiles(u, BH, Sq, Skv) for u in lst) for lst in sched}
+    for seq in seqs:
+        for seed in range(8):
+            simulate(list(seq), 4, 4, seed)
+            simulate(list(seq), 2, 2, seed)
