@@ -72,6 +72,23 @@ def test_large_scores_force_rescale(d):
     _full_compare(1, 2, 2, 260, 260, d, True, 0.35, 6, torch.float32, amp=3.0)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_causal_scores_growing_every_tile(d):
+    """Key rows scaled up along the sequence, so that every later KV tile raises a
+    row's maximum by more than 2^8: a tile exponentiated against the stale reference
+    overflows the rescale bound and is done again with the new maximum, on every
+    tile (the causal launch runs on the persistent kernel)."""
+    q, k, v = W.prefill_inputs(1, 2, 2, 600, 600, d, 31)
+    ramp = torch.linspace(1.0, 6.0, 600).view(1, 600, 1, 1)
+    q = (q.float() * 2.0).to(torch.bfloat16)
+    k = (k.float().abs() * ramp).to(torch.bfloat16)
+    q = q.float().abs().to(torch.bfloat16)
+    o, lse = _run(q, k, v, True, 0.5, torch.float32)
+    ro, rl = oracle.sdpa(q, k, v, True, 0.5)
+    check_o(o, ro, False)
+    check_lse(lse, rl)
+
+
 def test_deterministic():
     q, k, v = W.prefill_inputs(1, 4, 2, 333, 333, 128, 9)
     a = prefill(q.cuda(), k.cuda(), v.cuda(), causal=True)
