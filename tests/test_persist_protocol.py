@@ -18,7 +18,9 @@ Roles and barriers, with their phases running on across units:
 The model checks every wait for soundness (its barrier has completed exactly the
 phases before the awaited one, or that one too), that the pipeline drains, that
 no S MMA of a unit is issued before its tile's Q has landed and that a tile's O
-is not read before its last P.V completed.
+is not read before its last P.V completed, that no S MMA is issued over a P whose
+P.V has not been issued, and that no unit's first P.V (which starts O afresh) is
+issued before the tile's warpgroup has read out the previous unit's O.
 
 A tcgen05.commit issued before the CTA's first MMA does not arrive (a CTA whose
 first units had no keys timed out on its Q-free barrier): the model's commits
@@ -107,12 +109,20 @@ def simulate(units, SK, SV, seed, fin_by_unit=False, q_by_unit=None):
                 at(now[0] + rng.randint(50, 3000), lambda b=b: b.complete_tx(1))
                 g += 1
 
+    n_s = [0, 0]   # S MMAs issued per tile
+    n_pv = [0, 0]  # P.V MMAs issued per tile
+    o_read = [0, 0]  # units with keys whose O the tile's warpgroup has read out
+
     def mma_warp():
         gk = gv = 0
         J = [0, 0]
+        m_pv = [0, 0]  # units with keys whose first P.V has been issued, per tile
 
         def issue_s(t, k):
             assert q_loaded.get((t, k)), f"S of tile {t} unit {k} issued before its Q landed"
+            # S_t overwrites P_t of the tile's previous step: its P.V must be issued first
+            assert n_pv[t] >= n_s[t], f"S of tile {t} issued over a P its P.V has not read"
+            n_s[t] += 1
             for _ in range(8):
                 mma(rng.randint(20, 80))
             commit(bar(("S", t)))
@@ -142,6 +152,10 @@ def simulate(units, SK, SV, seed, fin_by_unit=False, q_by_unit=None):
                         if j < ns[t]:
                             use = J[t] + j
                             yield wait(bar(("P", t), 4), use & 1, use)
+                            if j == 0:  # this P.V starts O_t afresh: the last unit's O is out
+                                assert o_read[t] >= m_pv[t], f"P.V into O of tile {t} before its O was read"
+                                m_pv[t] += 1
+                            n_pv[t] += 1
                             for _ in range(8):
                                 mma(rng.randint(20, 80))
                             commit(bar(("O", t)))
@@ -191,6 +205,7 @@ def simulate(units, SK, SV, seed, fin_by_unit=False, q_by_unit=None):
                 yield wait(bar(("Fin", t)), fu & 1, fu)
                 # O is read now: every P.V of the tile up to this unit must have completed
                 assert bar(("O", t)).done >= J + ns[t], f"O of tile {t} read before its last P.V completed"
+                o_read[t] += 1
                 F += 1
             e = 2 * k + t
             if e > 0:
