@@ -285,12 +285,14 @@ int attn_prefill_window(const attn_bf16_t* q, const attn_bf16_t* k, const attn_b
   return prefill_impl(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, d, 1, window, n_sink, scale, o_dtype, stream);
 }
 
-// head packing needs the group to tile the 128 rows and the single-CTA kernel
-static bool packable(int Hq, int Hkv, int d) {
+// head packing needs the single-CTA kernel and at most 128 head rows per group; a
+// prefill also needs the group to tile the 128 rows (so that tiles hold whole
+// positions), a one-token decode (one position, in the first tile) does not
+static bool packable(int Hq, int Hkv, int d, bool one_position = false) {
   if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return false;
   const int G = Hq / Hkv;
   return (d == 64 || d == 128) && !attn::prefill_uses_pair(d) && G <= attn::kPrefillTileM &&
-         attn::kPrefillTileM % G == 0;
+         (one_position || attn::kPrefillTileM % G == 0);
 }
 
 int attn_prefill_packed(const attn_bf16_t* q, const attn_bf16_t* k, const attn_bf16_t* v, void* o,
@@ -307,7 +309,7 @@ int attn_decode_packed(const attn_bf16_t* q, const attn_bf16_t* kcache, const at
                        void* o, float* lse, int o_dtype, attn_stream_t stream) {
   if (B < 0 || max_kv < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (!ok_scale(scale)) return ATTN_ERR_INVALID_ARG;
-  if (!packable(Hq, Hkv, d) || (o_dtype != ATTN_F32 && o_dtype != ATTN_BF16)) return ATTN_ERR_UNSUPPORTED;
+  if (!packable(Hq, Hkv, d, true) || (o_dtype != ATTN_F32 && o_dtype != ATTN_BF16)) return ATTN_ERR_UNSUPPORTED;
   if (B == 0) return ATTN_OK;
   if (!kv_lens || (reinterpret_cast<uintptr_t>(kv_lens) & 3)) return ATTN_ERR_INVALID_ARG;
   // one query position per sequence, the last one: causal admits keys [0, kv_lens[b])
@@ -322,7 +324,7 @@ int attn_decode_split_packed(const attn_bf16_t* q, const attn_bf16_t* kcache,
   if (B < 0 || max_kv < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (n_splits < 1 || n_splits > 1024 || min_rows_per_split < 0 || !ok_scale(scale))
     return ATTN_ERR_INVALID_ARG;
-  if (!packable(Hq, Hkv, d)) return ATTN_ERR_UNSUPPORTED;
+  if (!packable(Hq, Hkv, d, true)) return ATTN_ERR_UNSUPPORTED;
   if (B == 0) return ATTN_OK;
   if (!kv_lens || (reinterpret_cast<uintptr_t>(kv_lens) & 3)) return ATTN_ERR_INVALID_ARG;
   if (!part_o || !part_lse || !aligned16(part_o) || !aligned16(part_lse)) return ATTN_ERR_INVALID_ARG;

@@ -314,10 +314,15 @@ __global__ void __launch_bounds__(PrefillCfg<D, HALVES>::kThreads, 1)
         }
       }
       if (is_k) {
+        // a Q box holds 128 / G whole positions of G head rows: all 128 rows of the
+        // tile when G divides 128, else the first G * floor(128 / G) (one-token decode
+        // only, whose single position is in tile 0; the rows below are never read
+        // out)
+        const uint32_t q_box_bytes = (uint32_t)(G * (kPrefillTileM / G)) * 128u * C::kPanels;
         uint32_t qbytes = 0;
 #pragma unroll
         for (int t = 0; t < C::kQTiles; ++t)
-          if (ti[t].n_kv > 0) qbytes += C::kQTileBytes;
+          if (ti[t].n_kv > 0) qbytes += q_box_bytes;
         mbar_arrive_expect_tx_e(bar_q, qbytes);
 #pragma unroll
         for (int t = 0; t < C::kQTiles; ++t) {

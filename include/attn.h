@@ -150,8 +150,9 @@ int attn_prefill_packed(const attn_bf16_t* q, const attn_bf16_t* k, const attn_b
  * launch and without split partials.  The G = Hq/Hkv heads of a KV head form the
  * rows of one MMA tile (the FMHA page's D2), so a decode step of G >= 8 heads per
  * KV head runs on tcgen05 instead of CUDA cores; one unit of work per (sequence,
- * KV head) streams that sequence's keys once.  Requires d in {64, 128} and G
- * dividing 128 (any G up to 128).
+ * KV head) streams that sequence's keys once.  Requires d in {64, 128} and
+ * G <= 128 (a G that does not divide 128 leaves the tile's last 128 mod G rows
+ * unused).
  *
  * Arguments
  *   q         bf16 [B][Hq][d]
@@ -174,8 +175,8 @@ int attn_decode_packed(const attn_bf16_t* q, const attn_bf16_t* kcache, const at
  * Each (sequence, split, KV head) is one unit of work whose G = Hq/Hkv query
  * heads fill the rows of an MMA tile (the FMHA page's D2); splits spread a long
  * sequence's keys over several SMs ("66 . D2: explicit K+V register staging",
- * section 3.2: rows [lo, hi) of one sequence).  Requires d in {64, 128} and G
- * dividing 128; part_o and part_lse 16-byte aligned.  Arguments as for
+ * section 3.2: rows [lo, hi) of one sequence).  Requires d in {64, 128} and
+ * G <= 128; part_o and part_lse 16-byte aligned.  Arguments as for
  * attn_decode_split (n_splits in [1, 1024], min_rows_per_split >= 0).
  * Returns ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED or ATTN_ERR_CUDA.
  */

@@ -124,6 +124,7 @@ def test_packed_validation(lib):
     #      q  kc vc kv  B  Hq Hkv d   mkv scale o  lse dtype stream
     assert g(P, P, P, P, 2, 8, 1, 96, 16, 0.5, P, P, 0, N) == attn.ATTN_ERR_UNSUPPORTED  # d
     assert g(P, P, P, P, 2, 8, 1, 64, 16, 0.5, P, P, 3, N) == attn.ATTN_ERR_UNSUPPORTED  # dtype
+    assert g(P, P, P, P, 2, 256, 1, 64, 16, 0.5, P, P, 0, N) == attn.ATTN_ERR_UNSUPPORTED  # G = 256
     assert g(P, P, P, N, 2, 8, 1, 64, 16, 0.5, P, P, 0, N) == attn.ATTN_ERR_INVALID_ARG  # null kv_lens
     assert g(P, P, P, M, 2, 8, 1, 64, 16, 0.5, P, P, 0, N) == attn.ATTN_ERR_INVALID_ARG  # misaligned kv_lens
     assert g(P, P, P, P, 2, 8, 1, 64, -1, 0.5, P, P, 0, N) == attn.ATTN_ERR_INVALID_ARG  # max_kv
@@ -135,7 +136,7 @@ def test_split_packed_validation(lib):
     f = attn.attn_decode_split_packed
     #      q  kc vc kv  B  Hq Hkv d   mkv scale ns mr po pl stream
     assert f(P, P, P, P, 2, 8, 1, 256, 16, 0.5, 4, 1, P, P, N) == attn.ATTN_ERR_UNSUPPORTED  # d
-    assert f(P, P, P, P, 2, 12, 4, 64, 16, 0.5, 4, 1, P, P, N) == attn.ATTN_ERR_UNSUPPORTED  # G = 3
+    assert f(P, P, P, P, 2, 256, 1, 64, 16, 0.5, 4, 1, P, P, N) == attn.ATTN_ERR_UNSUPPORTED  # G = 256
     assert f(P, P, P, P, 2, 8, 1, 64, 16, 0.5, 0, 1, P, P, N) == attn.ATTN_ERR_INVALID_ARG  # n_splits
     assert f(P, P, P, P, 2, 8, 1, 64, 16, 0.5, 4, -1, P, P, N) == attn.ATTN_ERR_INVALID_ARG  # min rows
     assert f(P, P, P, P, 2, 8, 1, 64, 16, 0.5, 4, 1, N, P, N) == attn.ATTN_ERR_INVALID_ARG  # null part_o

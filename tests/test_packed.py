@@ -63,8 +63,11 @@ def test_packed_prefill_bf16_output(out_dtype):
 
 
 @pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("Hq,Hkv", [(128, 1), (64, 2), (32, 1), (16, 2), (8, 1)])
+@pytest.mark.parametrize("Hq,Hkv", [(128, 1), (64, 2), (32, 1), (16, 2), (8, 1),
+                                    (28, 4), (12, 1), (96, 1), (100, 2), (3, 3)])
 def test_packed_decode(d, Hq, Hkv):
+    """Head groups that divide 128 and groups that do not (7, 12, 96, 50, 1): the
+    one-token decode's single position fills the first G rows of the tile."""
     # one KV tile (the second key half empty), two, odd counts (unequal halves),
     # ragged tails, an empty sequence
     lens = torch.tensor([0, 1, 29, 128, 129, 300, 640, 1000, 2500, 77], dtype=torch.int32)
@@ -90,7 +93,7 @@ def test_packed_decode_cache_rows_past_length_ignored():
 
 
 @pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("Hq,Hkv", [(128, 1), (16, 2)])
+@pytest.mark.parametrize("Hq,Hkv", [(128, 1), (16, 2), (28, 4), (100, 1)])
 @pytest.mark.parametrize("n_splits,min_rows", [(1, 1), (3, 1), (8, 256), (16, 64)])
 def test_packed_decode_split_partials(d, Hq, Hkv, n_splits, min_rows):
     """Partials with the decode split rule (empty splits included) against the
@@ -120,3 +123,17 @@ def test_packed_decode_no_keys_with_splits():
     po, pl = decode_split_packed(q.cuda(), kc.cuda(), vc.cuda(), lens.cuda(), 4, 1, 0.125)
     sync_check()
     assert np.all(po.cpu().numpy() == 0) and np.all(np.isneginf(pl.cpu().numpy()))
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_packed_decode_gqa_1641(out_dtype):
+    """The 1641-key GQA decode (7 query heads per KV head, a group that does not
+    divide 128) on the tensor cores, bf16 O through the TMA store of the first 7
+    rows, against the oracle's decode."""
+    s = W.GQA_DECODE
+    q, kc, vc, lens = W.decode_inputs_for(s)
+    o, lse = decode_packed(q.cuda(), kc.cuda(), vc.cuda(), lens.cuda(), s.scale, out_dtype=out_dtype)
+    sync_check()
+    ro, rl = oracle.decode(q, kc, vc, lens, s.scale)
+    check_o(o.float().cpu().numpy(), ro, out_dtype == torch.bfloat16)
+    check_lse(lse.cpu().numpy(), rl)
