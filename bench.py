@@ -8,8 +8,9 @@ One step = one pass of the whole hot path over one batch of synthetic input:
   3. the same on ragged_gqa_decode_b64 (B=64, Hq=32, Hkv=8, KV ~ U[512,8192])
 Beside the step, each further workload is timed alone and reported on its own
 line object: chunked (varlen) prefill, the sliding window with sinks, the
-128-head multi-query decode and the non-causal head-dim sweep (B=2, H=16,
-S=4096, d = 64, 128, 256, and 512).
+128-head multi-query decode, the non-causal head-dim sweep (B=2, H=16,
+S=4096, d = 64, 128, 256, and 512), and, for context, the 1641-key decode of
+the 28 layers of a model in one CUDA graph.
 L2 is flushed (a 256 MiB device write, then a 256 MiB read so that no dirty lines
 are left behind) before every step, outside the kernel
 events.  `value` is the prefill throughput in TFLOP/s (algorithmic FLOPs:
@@ -266,6 +267,8 @@ def run_ours(args, rank, world, local_rank):
     window = None if args.only else time_window(args, attn, W, dev, stream, flush, peaks, peak_src)
     # ---- multi-query decode on the tensor cores (heads packed into the tile rows) ----
     mqa = None if args.only else time_mqa_decode(args, attn, W, dev, stream, flush, peaks, peak_src)
+    # ---- the 1641-key decode of all 28 layers of a model, in one CUDA graph ----
+    layers28 = None if args.only else time_decode_layers_graph(args, attn, W, dev, stream, flush, peaks, peak_src)
     # ---- non-causal head-dim sweep (B = 2, H = 16, S = 4096; d = 64, 128, 256) ----
     sweep = None if args.only else [time_sweep(args, attn, W, dev, stream, flush, peaks, peak_src, d)
                                     for d in (64, 128, 256, 512)]
@@ -347,6 +350,7 @@ def run_ours(args, rank, world, local_rank):
         "prefill_varlen": varlen,
         "prefill_window": window,
         "decode_packed": mqa,
+        "decode_1641_layers_graph": layers28,
         "prefill_headdim_sweep": sweep,
         "clocks": clocks,
     }
@@ -530,6 +534,67 @@ def time_mqa_decode(args, attn, W, dev, stream, flush, peaks, peak_src):
                              "frac": round(gbs / peak_hbm, 4),
                              "traffic": load_traffic().get(f"fmha_fwd_kernel<{S.d}> packed {S.name}"),
                              "peak_source": f"hbm_gbs of {peak_src}"}}
+
+
+def time_decode_layers_graph(args, attn, W, dev, stream, flush, peaks, peak_src, layers=28):
+    """Context for the latency-bound 1641-key GQA decode: one decode per layer of a
+    28-layer model (each layer its own KV cache, the same shape), the 28 calls (split
+    and merge in one launch each) captured in one CUDA graph and replayed, L2 flushed
+    before each replay.  Reports the time per layer, with the graph and with plain
+    launches, and the K/V bandwidth over the whole replay."""
+    import torch
+
+    S = W.GQA_DECODE
+    lens = torch.full((S.B,), S.fixed_len, dtype=torch.int32)
+    caches = []
+    for layer in range(layers):
+        q, kc, vc = W.decode_inputs(S.B, S.Hq, S.Hkv, S.d, lens, S.seed + 100 + layer)
+        caches.append([t.to(dev) for t in (q, kc, vc, lens)])
+    kvb = W.decode_kv_bytes(lens, S.Hkv, S.d) * layers
+    o = torch.empty((layers, S.B, S.Hq, S.d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((layers, S.B, S.Hq), dtype=torch.float32, device=dev)
+    # the layers run one after another on one stream: they can share the partials
+    # and the completion counters
+    po = torch.empty((S.B, S.Hq, S.n_splits, S.d), dtype=torch.float32, device=dev)
+    pl = torch.empty((S.B, S.Hq, S.n_splits), dtype=torch.float32, device=dev)
+    ctr = torch.zeros(S.B * S.Hq, dtype=torch.int32, device=dev)
+
+    def run():
+        for layer, (q, kc, vc, ln) in enumerate(caches):
+            attn.decode(q, kc, vc, ln, S.n_splits, S.min_rows_per_split, S.scale, torch.bfloat16,
+                        out=(o[layer], lse[layer]), parts=(po, pl), counters=ctr)
+
+    run()
+    torch.cuda.synchronize()
+    attn.sync_check()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        run()
+    n = max(1, min(args.steps, 50))
+
+    def timed(fn):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for a, b in evs:
+            flush()
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        attn.sync_check()
+        return sum(a.elapsed_time(b) for a, b in evs) / n
+
+    ms_graph = timed(graph.replay)
+    ms_plain = timed(run)
+    return {"workload": f"{S.name} x {layers} layers", "layers": layers, "B": S.B, "Hq": S.Hq, "Hkv": S.Hkv,
+            "d": S.d, "kv_len": S.fixed_len, "n_splits": S.n_splits,
+            "us_per_layer_graph": round(ms_graph * 1e3 / layers, 2),
+            "us_per_layer_launches": round(ms_plain * 1e3 / layers, 2),
+            "gbs_graph": round(kvb / (ms_graph * 1e-3) / 1e9, 1),
+            "gpu_launches_per_replay": layers, "steps": n,
+            "note": "context line: the 28 layers' decodes run in sequence, as in a model's decode step; "
+                    "L2 flushed before each replay, not between the layers"}
 
 
 def run_e2e(args, attn, W, dev, stream, P, dec, flops):
