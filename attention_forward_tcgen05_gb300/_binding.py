@@ -373,7 +373,10 @@ _counters = {}  # (device type, index) -> the shared zeroed completion counters 
 
 def decode_counters(n: int, device):
     """The shared completion-counter buffer of decode() on `device`: int32, at least n
-    entries, zero between calls.  Calls that use it must be ordered on one stream."""
+    entries, zero between calls.  Calls that use it must be ordered on one stream.
+    It is allocated (and the device synchronised) when it first has to hold n
+    entries: a call captured into a CUDA graph passes counters of its own, or
+    follows a call of at least its size."""
     torch = _torch()
     key = (device.type, device.index)
     with _lock:

@@ -10,9 +10,15 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  *  - Pointers are DEVICE pointers owned by the caller (e.g. torch tensors'
- *    data_ptr()).  The library allocates nothing per call and never frees a
- *    caller's buffer.  It keeps one small static device word per device for
- *    error reporting.
+ *    data_ptr()).  The library never frees a caller's buffer.  Per device it
+ *    keeps a small word for error reporting (allocated at the first call) and,
+ *    for the causal fixed-length prefill, the unit schedule of each launch
+ *    shape (a few KB, uploaded at that shape's first launch, at most 256
+ *    shapes; a launch that is being captured into a CUDA graph uploads nothing
+ *    and takes the schedule of an earlier launch of its shape, else a simpler
+ *    one).  Both are held until the process exits; a cudaDeviceReset()
+ *    invalidates them: do not call the library on a device again in the same
+ *    process after resetting it.
  *  - bf16 buffers hold raw bfloat16 bits (attn_bf16_t).  Every tensor is
  *    dense, row-major, contiguous in the layout stated for it, and 16-byte
  *    aligned (the TMA engine reads whole 16-byte units).
