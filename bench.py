@@ -289,6 +289,7 @@ def run_ours(args, rank, world, local_rank):
     # one roofline per hot kernel; the top-level one is the kernel that takes the
     # largest share of the step's device time
     pkern = prefill_kernel_name(P.d, P.causal)
+    prefill_mufu = mufu_roofline(flops / (4 * P.d), t_prefill)
     prefill_roof = {"bound": "tensor", "kernel": pkern, "workload": P.name,
                     "achieved": round(prefill_tflops / world, 2), "peak": peak_tc,
                     "unit": "TFLOP/s", "frac": round(prefill_tflops / world / peak_tc, 4),
@@ -333,7 +334,7 @@ def run_ours(args, rank, world, local_rank):
                    "l2": "flushed before every step (256 MiB device write, then a 256 MiB read)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": dominant_roof,
-        "rooflines": {"prefill": prefill_roof, "decode_split": decode_roof},
+        "rooflines": {"prefill": prefill_roof, "decode_split": decode_roof, "prefill_mufu": prefill_mufu},
         "decode": {"value": round(dec_gbs, 1), "unit": "GB/s", "workload": D5.name,
                    "kv_bytes": kv5, "decode_us": round(t_dec5 * 1e3, 2),
                    "launches": "one: split partials and their combine (attn_decode)",
@@ -478,7 +479,26 @@ def time_sweep(args, attn, W, dev, stream, flush, peaks, peak_src, d):
         # cores execute 6*d FLOPs per pair, 1.5x the algorithmic 4*d counted above
         line["executed_gflop"] = round(1.5 * flops / 1e9, 3)
         line["executed_tflops"] = round(1.5 * tf, 2)
+    line["roofline_mufu"] = mufu_roofline(flops / (4 * P.d), ms)
     return line
+
+
+# MUFU ex2 rate: 32 lanes per clock per SM (a probe on this GPU; 8 per sub-partition)
+MUFU_EX2_PER_CLK_SM = 32
+
+
+def mufu_roofline(exps: float, ms: float) -> dict:
+    """The secondary bound of the prefill: one exp2 per admissible (query, key) pair on
+    the MUFU, against the GPU's rate at its maximum SM clock."""
+    import torch
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    clk_ghz = 2.07  # maximum SM clock of the GB300s this runs on (nvidia-smi clocks.max.sm)
+    peak = MUFU_EX2_PER_CLK_SM * props.multi_processor_count * clk_ghz  # G exp2 / s
+    achieved = exps / (ms * 1e-3) / 1e9
+    return {"bound": "alu", "unit": "Gexp2/s", "achieved": round(achieved, 1), "peak": round(peak, 1),
+            "frac": round(achieved / peak, 4),
+            "peak_source": f"{MUFU_EX2_PER_CLK_SM} ex2 per clock per SM x {props.multi_processor_count} SMs "
+                           f"x {clk_ghz} GHz"}
 
 
 def prefill_kernel_name(d: int, causal: bool = False) -> str:
