@@ -171,8 +171,13 @@ cudaError_t launch_prefill_pair(const PrefillArgs& a, cudaStream_t stream);
 // per tile (pack = 1), no window, key splits or kv_lens; d in {64, 128}.
 cudaError_t launch_prefill_persistent(const PrefillArgs& a, cudaStream_t stream);
 // Head dimension 512 (prefill_d512.cu): fixed-length batches, causal or not; O in
-// two column halves (S recomputed for the second).
+// two column halves (S recomputed for the second).  The single-CTA kernel takes
+// 128-row query tiles (maps: Q 5-D, K and V boxes of 128 rows); the CTA-pair
+// kernel 256-row query blocks (maps: Q 4-D with 128-row boxes, K boxes of 64
+// rows, V boxes of 128 rows).  d512_uses_pair picks one by the query length.
 cudaError_t launch_prefill_d512(const PrefillArgs& a, cudaStream_t stream);
+cudaError_t launch_prefill_d512_pair(const PrefillArgs& a, cudaStream_t stream);
+constexpr bool d512_uses_pair(int Sq) { return Sq > kPrefillTileM; }
 cudaError_t launch_prefill_empty_kv(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_decode_split(const DecodeArgs& a, cudaStream_t stream);
 // The persistent prefill's unit schedule for BH = B * Hq heads over `grid` CTAs:

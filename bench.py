@@ -288,7 +288,7 @@ def run_ours(args, rank, world, local_rank):
     traffic = load_traffic()
     # one roofline per hot kernel; the top-level one is the kernel that takes the
     # largest share of the step's device time
-    pkern = prefill_kernel_name(P.d, P.causal)
+    pkern = prefill_kernel_name(P.d, P.causal, P.Sq)
     prefill_mufu = mufu_roofline(flops / (4 * P.d), t_prefill)
     prefill_roof = {"bound": "tensor", "kernel": pkern, "workload": P.name,
                     "achieved": round(prefill_tflops / world, 2), "peak": peak_tc,
@@ -427,7 +427,7 @@ def time_window(args, attn, W, dev, stream, flush, peaks, peak_src):
     ms = sum(a.elapsed_time(b) for a, b in evs) / n
     tf = flops / (ms * 1e-3) / 1e12
     peak_tc = float(peaks["bf16_tflops"])
-    kern = prefill_kernel_name(P.d)
+    kern = prefill_kernel_name(P.d, False, P.Sq)
     return {"workload": S.name, "B": P.B, "Hq": P.Hq, "Hkv": P.Hkv, "S": P.Sq, "d": P.d,
             "window": S.window, "n_sink": S.n_sink, "gflop": round(flops / 1e9, 3),
             "us": round(ms * 1e3, 2), "value": round(tf, 2), "unit": "TFLOP/s", "steps": n,
@@ -466,7 +466,7 @@ def time_sweep(args, attn, W, dev, stream, flush, peaks, peak_src, d):
     ms = sum(a.elapsed_time(b) for a, b in evs) / n
     tf = flops / (ms * 1e-3) / 1e12
     peak_tc = float(peaks["bf16_tflops"])
-    kern = prefill_kernel_name(P.d, P.causal)
+    kern = prefill_kernel_name(P.d, P.causal, P.Sq)
     line = {"workload": P.name, "B": P.B, "Hq": P.Hq, "Hkv": P.Hkv, "S": P.Sq, "d": P.d,
             "causal": P.causal, "gflop": round(flops / 1e9, 3), "us": round(ms * 1e3, 2),
             "value": round(tf, 2), "unit": "TFLOP/s", "steps": n,
@@ -501,11 +501,12 @@ def mufu_roofline(exps: float, ms: float) -> dict:
                            f"x {clk_ghz} GHz"}
 
 
-def prefill_kernel_name(d: int, causal: bool = False) -> str:
+def prefill_kernel_name(d: int, causal: bool = False, Sq: int = 4096) -> str:
     """The kernel that runs a fixed-length prefill of head dim d (causal launches of
-    head dims 64 and 128 run on the persistent kernel)."""
+    head dims 64 and 128 run on the persistent kernel; head dim 512 runs on CTA pairs
+    once the queries span more than one 128-row tile)."""
     if d == 512:
-        return "fmha_d512_kernel"
+        return "fmha_d512_pair_kernel" if Sq > 128 else "fmha_d512_kernel"
     if d == 256:
         return f"fmha_pair_kernel<{d}>"
     return f"fmha_persistent_kernel<{d}>" if causal else f"fmha_fwd_kernel<{d}>"

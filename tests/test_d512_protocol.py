@@ -216,3 +216,251 @@ def test_d512_final_barrier_waited_with_phase_zero_twice_is_unsound():
     with pytest.raises(AssertionError):
         for seed in range(50):
             simulate(3, 6, seed, fin_parity_by_phase=False)
+
+
+# ---------------------------------------------------------------------------
+# The CTA-pair form of the same kernel: a cluster of two CTAs takes 256 query
+# rows; rank 0's MMA warp issues every MMA for both (M = 256).  Each CTA's ring
+# holds its own share of every item -- K: 64 of the tile's 128 keys, two
+# 64-column panels per item (4 items per tile); V: one 64-column panel of the
+# phase's half per item (2 items per tile) -- and both CTAs' copies of an item
+# complete on rank 0's full barrier, which rank 0's producer arms for both.
+# MMA completions are multicast to the S, O, final and empty barriers of both
+# CTAs; the softmax warps of rank 1 publish P with remote arrivals on rank 0's
+# P barrier (eight arrivals: four warps per CTA).  Signals that cross the pair
+# are delivered late, by a random delay of their own.
+
+PAIR_K_ITEMS, PAIR_V_ITEMS = 4, 2
+
+
+class PairBar(Bar):
+    """An mbarrier whose transaction count may go below zero for a while: the
+    peer CTA's bytes can land before the owner arms the barrier for them."""
+
+    def complete_tx(self, n):
+        self.tx -= n
+        self._check()
+
+
+def simulate_pair(n_kv, slots, seed, p_count=8, arm_both=True, wait_own_empty=True, o_bars=2):
+    """One randomised run of the pair schedule; AssertionError on an unsound wait,
+    an early overwrite of O or a deadlock.  p_count: arrivals the P barriers
+    expect; arm_both=False arms the full barrier for rank 0's bytes only;
+    wait_own_empty=False lets rank 1's producer refill a slot without waiting;
+    o_bars=1 completes every P.V on one O barrier instead of alternating two."""
+    rng = random.Random(seed)
+    bars = {}
+
+    def bar(name, count=1):
+        if name not in bars:
+            bars[name] = PairBar(name, count)
+        return bars[name]
+
+    T = 2 * n_kv
+    now = [0]
+    events = []
+    seq = itertools.count()
+    mma_free = [0]
+    epilogue_done = [[False, False], [False, False]]  # [phase][rank]
+    pv_completed = [0]  # P.V groups the tensor core has finished (not their barrier arrivals)
+
+    def at(time, fn):
+        heapq.heappush(events, (time, next(seq), fn))
+
+    def mma(dur):
+        mma_free[0] = max(now[0], mma_free[0]) + dur
+
+    def cross():  # latency of a signal that crosses to the other SM of the pair
+        return rng.randint(0, 2500)
+
+    def commit_both(name):  # multicast: arrives on the barrier of each CTA
+        for r in range(2):
+            b = bar((name, r) if isinstance(name, str) else name + (r,))
+            at(mma_free[0] + (cross() if r == 1 else 0), b.arrive)
+
+    def wait(b, parity, use):
+        assert b.done in (use, use + 1), f"{b.name}: waiting for phase {use} with {b.done} done"
+        return ("wait", b, parity)
+
+    def items():
+        seq_ = [("K", 0)] * PAIR_K_ITEMS + [("K", 1)] * PAIR_K_ITEMS
+        for jj in range(T):
+            seq_ += [("V", jj)] * PAIR_V_ITEMS
+            if jj + 2 < T:
+                seq_ += [("K", jj + 2)] * PAIR_K_ITEMS
+        return seq_
+
+    def land(b, use, delay):
+        def fn():
+            # bytes of item use land while the barrier still collects that item
+            assert b.done == use, f"{b.name}: bytes of use {use} landed with {b.done} phases done"
+            b.complete_tx(1)
+        at(now[0] + delay, fn)
+
+    def producer(r):
+        q = bar("q")
+        if r == 0:
+            q.expect_tx(2)
+        land(q, 0, rng.randint(50, 3000) + (cross() if r == 1 else 0))
+        for g, _ in enumerate(items()):
+            s, u = g % slots, g // slots
+            if u > 0 and (wait_own_empty or r == 0):
+                yield wait(bar(("empty", s, r)), (u & 1) ^ 1, u - 1)
+            full = bar(("full", s))
+            if r == 0:
+                full.expect_tx(2 if arm_both else 1)
+            land(full, u, rng.randint(50, 3000) + (cross() if r == 1 else 0))
+            yield ("sleep", rng.randint(0, 30))
+
+    def mma_warp():
+        yield wait(bar("q"), 0, 0)
+        g = [0]
+
+        def take():
+            s, u = g[0] % slots, g[0] // slots
+            yield wait(bar(("full", s)), u & 1, u)
+            return s
+
+        def issue_s(jj):
+            for _ in range(PAIR_K_ITEMS):
+                s = yield from take()
+                for _ in range(8):
+                    mma(rng.randint(20, 80))
+                commit_both(("empty", s))
+                g[0] += 1
+            commit_both(("S", jj & 1))
+
+        def issue_pv(jj):
+            u = jj >> 1
+            yield wait(bar(("P", jj & 1), p_count), u & 1, u)
+            if jj == n_kv:  # first P.V of phase 1 overwrites the O half of phase 0
+                assert all(epilogue_done[0]), "O half of phase 0 overwritten before both CTAs read it"
+            for _ in range(PAIR_V_ITEMS):
+                s = yield from take()
+                for _ in range(8):
+                    mma(rng.randint(20, 80))
+                commit_both(("empty", s))
+                g[0] += 1
+            commit_both(("O", jj % o_bars))
+            at(mma_free[0], lambda: pv_completed.__setitem__(0, pv_completed[0] + 1))
+            if jj % n_kv == n_kv - 1:
+                commit_both("Fin")
+
+        yield from issue_s(0)
+        yield from issue_s(1)
+        for jj in range(T):
+            yield from issue_pv(jj)
+            if jj + 2 < T:
+                yield from issue_s(jj + 2)
+
+    def softmax(r):
+        for jj in range(T):
+            ph, j = divmod(jj, n_kv)
+            u = jj >> 1
+            yield wait(bar(("S", jj & 1, r)), u & 1, u)
+            yield ("sleep", rng.randint(20, 400))
+            if ph == 0 and j > 0 and rng.random() < 0.3:
+                uo = (jj - 1) // o_bars
+                yield wait(bar(("O", (jj - 1) % o_bars, r)), uo & 1, uo)
+                yield ("sleep", rng.randint(20, 200))
+            p = bar(("P", jj & 1), p_count)
+            for _ in range(4):
+                if r == 0:
+                    p.arrive()
+                else:
+                    at(now[0] + cross(), p.arrive)
+            if j == n_kv - 1:
+                yield wait(bar(("Fin", r)), ph & 1, ph)
+                # the final commit tracks every MMA issued before it; its arrival may
+                # overtake the O barrier's, which the epilogue does not read
+                assert pv_completed[0] >= (ph + 1) * n_kv, "O half read before its last P.V completed"
+                yield ("sleep", rng.randint(1000, 8000))
+                epilogue_done[ph][r] = True
+            elif rng.random() < 0.2:
+                yield ("sleep", rng.randint(100, 4000))
+
+    procs = [producer(0), producer(1), softmax(0), softmax(1), mma_warp()]
+    blocked = {}
+    finished = set()
+    advanced = [0]
+
+    def step(i):
+        while True:
+            if i in blocked:
+                _, b, parity = blocked[i]
+                if not b.ready(parity):
+                    return
+                del blocked[i]
+            advanced[0] += 1
+            try:
+                req = next(procs[i])
+            except StopIteration:
+                finished.add(i)
+                return
+            if req[0] == "wait":
+                blocked[i] = req
+            elif req[0] == "sleep":
+                at(now[0] + req[1], lambda i=i: step(i))
+                return
+
+    for i in range(len(procs)):
+        step(i)
+    for _ in range(2000000):
+        while True:
+            before = advanced[0]
+            for i in list(blocked):
+                step(i)
+            if advanced[0] == before:
+                break
+        if len(finished) == len(procs) and not events:
+            break
+        if not events:
+            raise AssertionError(f"deadlock: blocked on {[blocked[i][1].name for i in blocked]}")
+        now[0], _, fn = heapq.heappop(events)
+        fn()
+    assert len(finished) == len(procs), "pipeline did not drain"
+    for b in bars.values():  # every phase that was armed completed
+        assert b.pending == b.count and b.tx == 0, f"{b.name}: left mid-phase"
+
+
+@pytest.mark.parametrize("n_kv", [1, 2, 3, 8, 17])
+@pytest.mark.parametrize("slots", [6, 1, 4])
+def test_d512_pair_protocol_is_sound(n_kv, slots):
+    for seed in range(40):
+        simulate_pair(n_kv, slots, seed)
+
+
+def test_d512_pair_p_barrier_counting_one_cta_is_unsound():
+    """P barriers expecting four arrivals (one CTA's warps): P.V can start before
+    the peer CTA has written its P.  The model must catch it."""
+    with pytest.raises(AssertionError):
+        for seed in range(50):
+            simulate_pair(3, 6, seed, p_count=4)
+
+
+def test_d512_pair_full_barrier_armed_for_one_cta_is_unsound():
+    """A full barrier armed for rank 0's bytes only completes without the peer's
+    copy, whose bytes then land in a later phase.  The model must catch it."""
+    with pytest.raises(AssertionError):
+        for seed in range(50):
+            simulate_pair(3, 6, seed, arm_both=False)
+
+
+def test_d512_pair_one_o_barrier_is_unsound_without_ordered_delivery():
+    """Every P.V completing on one O barrier: the peer's copy of an O arrival can be
+    overtaken by a later S arrival, and the softmax's rescale wait then tests a
+    parity two phases ahead.  With two O barriers taken in turn the previous use of
+    the awaited barrier lies a whole P.V and S group earlier.  The model must catch
+    the one-barrier form."""
+    with pytest.raises(AssertionError):
+        for seed in range(200):
+            for n_kv in (8, 17):
+                simulate_pair(n_kv, 6, seed, o_bars=1)
+
+
+def test_d512_pair_peer_refilling_without_its_empty_wait_is_unsound():
+    """Rank 1's producer refilling a slot without waiting for its own empty
+    barrier: its bytes land while the slot's previous item is still collected."""
+    with pytest.raises(AssertionError):
+        for seed in range(50):
+            simulate_pair(3, 2, seed, wait_own_empty=False)
