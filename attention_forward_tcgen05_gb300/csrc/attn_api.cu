@@ -187,15 +187,11 @@ static int prefill_impl(const attn_bf16_t* q, const attn_bf16_t* k, const attn_b
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (Skv == 0) return from_cuda(attn::launch_prefill_empty_kv(a, s));
   if (d512) {
-    const bool pair = attn::d512_uses_pair(Sq);
-    int rc = pair ? encode_bf16_4d(&a.tm_q, q, d, Hq, Sq, B, attn::kPrefillTileM)
-                  : encode_bf16_q5d(&a.tm_q, q, d, 1, Hq, Sq, B);
-    if (rc == ATTN_OK)
-      rc = encode_bf16_4d(&a.tm_k, k, d, Hkv, Skv, B,
-                          pair ? attn::kPrefillKVStageRows / 2 : attn::kPrefillKVStageRows);
-    if (rc == ATTN_OK) rc = encode_bf16_4d(&a.tm_v, v, d, Hkv, Skv, B, attn::kPrefillKVStageRows);
+    int rc = encode_bf16_4d(&a.tm_q, q, d, Hq, Sq, B, attn::kPrefillTileM);
+    if (rc == ATTN_OK) rc = encode_bf16_4d(&a.tm_k, k, d, Hkv, Skv, B, attn::kPrefillKVStageRows / 2);
+    if (rc == ATTN_OK) rc = encode_bf16_4d(&a.tm_v, v, d, Hkv, Skv, B, attn::kD512PairVBoxRows);
     if (rc != ATTN_OK) return rc;
-    return from_cuda(pair ? attn::launch_prefill_d512_pair(a, s) : attn::launch_prefill_d512(a, s));
+    return from_cuda(attn::launch_prefill_d512(a, s));
   }
   const bool pair = attn::prefill_uses_pair(d);
   if (pair && pack != 1) return ATTN_ERR_UNSUPPORTED;

@@ -171,13 +171,17 @@ cudaError_t launch_prefill_pair(const PrefillArgs& a, cudaStream_t stream);
 // per tile (pack = 1), no window, key splits or kv_lens; d in {64, 128}.
 cudaError_t launch_prefill_persistent(const PrefillArgs& a, cudaStream_t stream);
 // Head dimension 512 (prefill_d512.cu): fixed-length batches, causal or not; O in
-// two column halves (S recomputed for the second).  The single-CTA kernel takes
-// 128-row query tiles (maps: Q 5-D, K and V boxes of 128 rows); the CTA-pair
-// kernel 256-row query blocks (maps: Q 4-D with 128-row boxes, K boxes of 64
-// rows, V boxes of 128 rows).  d512_uses_pair picks one by the query length.
+// two column halves (S recomputed for the second), on CTA pairs of 256 query rows.
+// Maps: Q 4-D with 128-row boxes, K boxes of 64 rows, V boxes of
+// kD512PairVBoxRows rows.
 cudaError_t launch_prefill_d512(const PrefillArgs& a, cudaStream_t stream);
-cudaError_t launch_prefill_d512_pair(const PrefillArgs& a, cudaStream_t stream);
-constexpr bool d512_uses_pair(int Sq) { return Sq > kPrefillTileM; }
+// The CTA-pair kernel's ring: kD512PairRingBytes of shared memory in slots of
+// kD512PairSlotBytes (three of 32 KB: measured against six of 16 KB and twelve of
+// 8 KB, every ring item costs a cross-SM round trip, so fewer, larger items win);
+// a V panel of an item holds kD512PairVBoxRows keys (the V map's box height).
+constexpr int kD512PairRingBytes = 6 * 16384;
+constexpr int kD512PairSlotBytes = 32768;
+constexpr int kD512PairVBoxRows = kD512PairSlotBytes >= 16384 ? 128 : kD512PairSlotBytes / 128;
 cudaError_t launch_prefill_empty_kv(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_decode_split(const DecodeArgs& a, cudaStream_t stream);
 // The persistent prefill's unit schedule for BH = B * Hq heads over `grid` CTAs:

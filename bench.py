@@ -506,7 +506,7 @@ def prefill_kernel_name(d: int, causal: bool = False, Sq: int = 4096) -> str:
     head dims 64 and 128 run on the persistent kernel; head dim 512 runs on CTA pairs
     once the queries span more than one 128-row tile)."""
     if d == 512:
-        return "fmha_d512_pair_kernel" if Sq > 128 else "fmha_d512_kernel"
+        return "fmha_d512_pair_kernel"
     if d == 256:
         return f"fmha_pair_kernel<{d}>"
     return f"fmha_persistent_kernel<{d}>" if causal else f"fmha_fwd_kernel<{d}>"

@@ -1,21 +1,30 @@
 """The head-dimension-512 prefill kernel's mbarrier protocol, modelled on the CPU.
 
-The d = 512 kernel computes O in two column halves one after the other (S is
-recomputed for the second), so its T = 2 n_kv tiles form one sequence: tile jj
-belongs to phase jj // n_kv and key tile jj % n_kv.  A TMA producer warp fills
-a ring of single-panel slots in the order K(0) K(1) { V(jj) K(jj + 2) } (8 K
-panels, 4 V panels per tile), the MMA warp consumes them in that order issuing
-S(0) S(1) { P(jj).V(jj) S(jj + 2) } (two S buffers, S(jj) in buffer jj % 2,
-each with its own S and P barrier), and one softmax warpgroup waits for S(jj),
-optionally rescales O in phase 0 (waiting for P(jj-1).V(jj-1) on the O
-barrier), publishes P(jj), and at the end of each phase waits for that phase's
-last P.V on the final barrier (its phase-th phase) before reading the O half.
+The d = 512 kernel runs on CTA pairs: a cluster of two CTAs takes 256 query
+rows of one head, and rank 0's MMA warp issues every MMA for both (M = 256).
+O is computed in two column halves one after the other (S is recomputed for
+the second), so the T = 2 n_kv tiles form one sequence: tile jj belongs to
+phase jj // n_kv and key tile jj % n_kv.  Each CTA's TMA producer fills a ring
+of slots with its own share of every item, in the order K(0) K(1) { V(jj)
+K(jj + 2) }; both CTAs' copies of an item complete on rank 0's full barrier,
+which rank 0's producer arms for both.  The MMA warp consumes the items in that
+order, issuing S(0) S(1) { P(jj).V(jj) S(jj + 2) } (two S buffers, S(jj) in
+buffer jj % 2, each with its own S and P barrier).  MMA completions are
+multicast to the S, O, final and empty barriers of both CTAs; P.V(jj) completes
+on O barrier jj % 2.  Each CTA's softmax warpgroup waits for S(jj), may rescale
+O in phase 0 (waiting for P(jj-1).V(jj-1)), publishes P(jj) -- rank 1's warps
+with remote arrivals on rank 0's P barrier, eight arrivals in all -- and at the
+end of each phase waits for that phase's last P.V on the final barrier (its
+phase-th phase) before reading the O half.  Signals that cross the pair arrive
+late, each by a random delay of its own.
 
 A wait tests a phase parity, so it is sound only if its barrier has completed
 exactly the phases before the awaited one or that phase too.  The model runs
-the schedule against exact mbarrier semantics with random TMA, MMA and softmax
-latencies, checks every wait for soundness and that the pipeline drains, and
-must catch the unsound variants kept as negative cases.
+the schedule against exact mbarrier semantics with random TMA, MMA, softmax and
+cross-SM latencies, checks every wait for soundness, that every copy lands in
+the phase it was armed for, that no O half is read or overwritten early and
+that the pipeline drains, and must catch the unsound variants kept as negative
+cases.
 """
 import heapq
 import itertools
@@ -25,212 +34,10 @@ import pytest
 
 from tests.test_prefill_protocol import Bar
 
-K_PANELS, V_PANELS = 8, 4
-
-
-def simulate(n_kv, slots, seed, s_per_buffer=True, fin_parity_by_phase=True):
-    """Run one randomised schedule; raises AssertionError on an unsound wait or a
-    deadlock.  s_per_buffer=False keys the S and P barriers by nothing (one of each
-    for both buffers); fin_parity_by_phase=False waits for the final barrier's
-    phase 0 at the end of both phases."""
-    rng = random.Random(seed)
-    bars = {}
-
-    def bar(name, count=1):
-        if name not in bars:
-            bars[name] = Bar(name, count)
-        return bars[name]
-
-    def s_bar(buf):
-        return bar(("S", buf if s_per_buffer else 0))
-
-    def p_bar(buf):
-        return bar(("P", buf if s_per_buffer else 0), 4)
-
-    def buf_use(jj):  # index of the awaited phase of tile jj's S / P barrier
-        return jj >> 1 if s_per_buffer else jj
-
-    T = 2 * n_kv
-    now = [0]
-    events = []
-    seq = itertools.count()
-    mma_free = [0]
-
-    def at(time, fn):
-        heapq.heappush(events, (time, next(seq), fn))
-
-    def mma(dur):
-        mma_free[0] = max(now[0], mma_free[0]) + dur
-
-    def commit(b):
-        at(mma_free[0], b.arrive)
-
-    def wait(b, parity, use):
-        assert b.done in (use, use + 1), f"{b.name}: waiting for phase {use} with {b.done} done"
-        return ("wait", b, parity)
-
-    def items():  # the ring's item order, shared by producer and MMA warp
-        seq_ = [("K", 0)] * K_PANELS + [("K", 1)] * K_PANELS
-        for jj in range(T):
-            seq_ += [("V", jj)] * V_PANELS
-            if jj + 2 < T:
-                seq_ += [("K", jj + 2)] * K_PANELS
-        return seq_
-
-    def producer():
-        bar("q").expect_tx(1)
-        at(now[0] + rng.randint(50, 3000), lambda: bar("q").complete_tx(1))
-        for g, _ in enumerate(items()):
-            s, u = g % slots, g // slots
-            if u > 0:
-                yield wait(bar(("empty", s)), (u & 1) ^ 1, u - 1)
-            b = bar(("full", s))
-            b.expect_tx(1)
-            at(now[0] + rng.randint(50, 3000), lambda b=b: b.complete_tx(1))
-
-    def mma_warp():
-        yield wait(bar("q"), 0, 0)
-        g = [0]
-
-        def take():
-            s, u = g[0] % slots, g[0] // slots
-            yield wait(bar(("full", s)), u & 1, u)
-            return s
-
-        def issue_s(jj):
-            for _ in range(K_PANELS):
-                s = yield from take()
-                for _ in range(4):
-                    mma(rng.randint(20, 80))
-                commit(bar(("empty", s)))
-                g[0] += 1
-            commit(s_bar(jj & 1))
-
-        def issue_pv(jj):
-            u = buf_use(jj)
-            yield wait(p_bar(jj & 1), u & 1, u)
-            for _ in range(V_PANELS):
-                s = yield from take()
-                for _ in range(8):
-                    mma(rng.randint(10, 40))
-                commit(bar(("empty", s)))
-                g[0] += 1
-            commit(bar("O"))
-            if jj % n_kv == n_kv - 1:
-                commit(bar("Fin"))
-
-        yield from issue_s(0)
-        yield from issue_s(1)
-        for jj in range(T):
-            yield from issue_pv(jj)
-            if jj + 2 < T:
-                yield from issue_s(jj + 2)
-
-    def softmax():
-        for jj in range(T):
-            ph, j = divmod(jj, n_kv)
-            u = buf_use(jj)
-            yield wait(s_bar(jj & 1), u & 1, u)
-            yield ("sleep", rng.randint(20, 400))
-            if ph == 0 and j > 0 and rng.random() < 0.3:  # O rescale needs P(jj-1).V(jj-1) done
-                yield wait(bar("O"), (jj - 1) & 1, jj - 1)
-                yield ("sleep", rng.randint(20, 200))
-            for _ in range(4):  # one arrival per softmax warp
-                p_bar(jj & 1).arrive()
-            if j == n_kv - 1:  # end of the phase: its O half is complete
-                fu = ph if fin_parity_by_phase else 0
-                yield wait(bar("Fin"), fu & 1, fu)
-                # the O half is read now: every P.V of the phase must have completed
-                assert bar("O").done >= (ph + 1) * n_kv, "O half read before its last P.V completed"
-                yield ("sleep", rng.randint(1000, 8000))  # the O half's epilogue
-            elif rng.random() < 0.2:
-                yield ("sleep", rng.randint(100, 4000))  # the warps fall behind the MMAs
-
-    procs = [producer(), softmax(), mma_warp()]
-    blocked = {}
-    finished = set()
-    advanced = [0]  # process steps taken
-
-    def step(i):
-        while True:
-            if i in blocked:
-                _, b, parity = blocked[i]
-                if not b.ready(parity):
-                    return
-                del blocked[i]
-            advanced[0] += 1
-            try:
-                req = next(procs[i])
-            except StopIteration:
-                finished.add(i)
-                return
-            if req[0] == "wait":
-                blocked[i] = req
-            elif req[0] == "sleep":
-                at(now[0] + req[1], lambda i=i: step(i))
-                return
-
-    for i in range(len(procs)):
-        step(i)
-    for _ in range(400000):
-        # step the blocked processes until none makes progress (an arrival made by
-        # one of them can release another that was stepped before it)
-        while True:
-            before = advanced[0]
-            for i in list(blocked):
-                step(i)
-            if advanced[0] == before:
-                break
-        if len(finished) == len(procs):
-            break
-        if not events:
-            raise AssertionError(f"deadlock: blocked on {[blocked[i][1].name for i in blocked]}")
-        now[0], _, fn = heapq.heappop(events)
-        fn()
-    assert len(finished) == len(procs), "pipeline did not drain"
-
-
-@pytest.mark.parametrize("n_kv", [1, 2, 3, 8, 17])
-@pytest.mark.parametrize("slots", [6, 1, 4])
-def test_d512_protocol_is_sound(n_kv, slots):
-    for seed in range(60):
-        simulate(n_kv, slots, seed)
-
-
-def test_d512_one_s_barrier_for_both_buffers_is_unsound():
-    """One S barrier and one P barrier for both S buffers: S(jj+1) can complete
-    before the softmax waits for S(jj), two phases ahead.  The model must catch it."""
-    failures = 0
-    for seed in range(100):
-        try:
-            simulate(5, 6, seed, s_per_buffer=False)
-        except AssertionError:
-            failures += 1
-    assert failures > 0
-
-
-def test_d512_final_barrier_waited_with_phase_zero_twice_is_unsound():
-    """Waiting for the final barrier's phase 0 at the end of phase 1 too: the wait
-    passes at once and the second O half would be read before its last P.V
-    completed.  The model must catch it."""
-    with pytest.raises(AssertionError):
-        for seed in range(50):
-            simulate(3, 6, seed, fin_parity_by_phase=False)
-
-
-# ---------------------------------------------------------------------------
-# The CTA-pair form of the same kernel: a cluster of two CTAs takes 256 query
-# rows; rank 0's MMA warp issues every MMA for both (M = 256).  Each CTA's ring
-# holds its own share of every item -- K: 64 of the tile's 128 keys, two
-# 64-column panels per item (4 items per tile); V: one 64-column panel of the
-# phase's half per item (2 items per tile) -- and both CTAs' copies of an item
-# complete on rank 0's full barrier, which rank 0's producer arms for both.
-# MMA completions are multicast to the S, O, final and empty barriers of both
-# CTAs; the softmax warps of rank 1 publish P with remote arrivals on rank 0's
-# P barrier (eight arrivals: four warps per CTA).  Signals that cross the pair
-# are delivered late, by a random delay of their own.
-
-PAIR_K_ITEMS, PAIR_V_ITEMS = 4, 2
+# ring items as built: 32 KB slots; a K item holds four 64-column panels of the
+# CTA's 64 keys (two items per tile), a V item both 128-column chunks' panels
+# (one item per tile and phase)
+SLOTS, K_ITEMS, V_ITEMS = 3, 2, 1
 
 
 class PairBar(Bar):
@@ -242,12 +49,16 @@ class PairBar(Bar):
         self._check()
 
 
-def simulate_pair(n_kv, slots, seed, p_count=8, arm_both=True, wait_own_empty=True, o_bars=2):
+def simulate(n_kv, slots, seed, k_items=K_ITEMS, v_items=V_ITEMS, p_count=8, arm_both=True,
+             wait_own_empty=True, o_bars=2, s_per_buffer=True, fin_parity_by_phase=True):
     """One randomised run of the pair schedule; AssertionError on an unsound wait,
     an early overwrite of O or a deadlock.  p_count: arrivals the P barriers
     expect; arm_both=False arms the full barrier for rank 0's bytes only;
     wait_own_empty=False lets rank 1's producer refill a slot without waiting;
-    o_bars=1 completes every P.V on one O barrier instead of alternating two."""
+    o_bars=1 completes every P.V on one O barrier instead of alternating two;
+    s_per_buffer=False keys the S and P barriers by nothing (one of each for both
+    S buffers); fin_parity_by_phase=False waits for the final barrier's phase 0 at
+    the end of both phases."""
     rng = random.Random(seed)
     bars = {}
 
@@ -282,12 +93,15 @@ def simulate_pair(n_kv, slots, seed, p_count=8, arm_both=True, wait_own_empty=Tr
         assert b.done in (use, use + 1), f"{b.name}: waiting for phase {use} with {b.done} done"
         return ("wait", b, parity)
 
+    def sbuf(jj):  # key of tile jj's S and P barriers, and the index of its awaited phase
+        return (jj & 1, jj >> 1) if s_per_buffer else (0, jj)
+
     def items():
-        seq_ = [("K", 0)] * PAIR_K_ITEMS + [("K", 1)] * PAIR_K_ITEMS
+        seq_ = [("K", 0)] * k_items + [("K", 1)] * k_items
         for jj in range(T):
-            seq_ += [("V", jj)] * PAIR_V_ITEMS
+            seq_ += [("V", jj)] * v_items
             if jj + 2 < T:
-                seq_ += [("K", jj + 2)] * PAIR_K_ITEMS
+                seq_ += [("K", jj + 2)] * k_items
         return seq_
 
     def land(b, use, delay):
@@ -322,20 +136,20 @@ def simulate_pair(n_kv, slots, seed, p_count=8, arm_both=True, wait_own_empty=Tr
             return s
 
         def issue_s(jj):
-            for _ in range(PAIR_K_ITEMS):
+            for _ in range(k_items):
                 s = yield from take()
                 for _ in range(8):
                     mma(rng.randint(20, 80))
                 commit_both(("empty", s))
                 g[0] += 1
-            commit_both(("S", jj & 1))
+            commit_both(("S", sbuf(jj)[0]))
 
         def issue_pv(jj):
-            u = jj >> 1
-            yield wait(bar(("P", jj & 1), p_count), u & 1, u)
+            key, u = sbuf(jj)
+            yield wait(bar(("P", key), p_count), u & 1, u)
             if jj == n_kv:  # first P.V of phase 1 overwrites the O half of phase 0
                 assert all(epilogue_done[0]), "O half of phase 0 overwritten before both CTAs read it"
-            for _ in range(PAIR_V_ITEMS):
+            for _ in range(v_items):
                 s = yield from take()
                 for _ in range(8):
                     mma(rng.randint(20, 80))
@@ -356,21 +170,22 @@ def simulate_pair(n_kv, slots, seed, p_count=8, arm_both=True, wait_own_empty=Tr
     def softmax(r):
         for jj in range(T):
             ph, j = divmod(jj, n_kv)
-            u = jj >> 1
-            yield wait(bar(("S", jj & 1, r)), u & 1, u)
+            key, u = sbuf(jj)
+            yield wait(bar(("S", key, r)), u & 1, u)
             yield ("sleep", rng.randint(20, 400))
             if ph == 0 and j > 0 and rng.random() < 0.3:
                 uo = (jj - 1) // o_bars
                 yield wait(bar(("O", (jj - 1) % o_bars, r)), uo & 1, uo)
                 yield ("sleep", rng.randint(20, 200))
-            p = bar(("P", jj & 1), p_count)
+            p = bar(("P", key), p_count)
             for _ in range(4):
                 if r == 0:
                     p.arrive()
                 else:
                     at(now[0] + cross(), p.arrive)
             if j == n_kv - 1:
-                yield wait(bar(("Fin", r)), ph & 1, ph)
+                fu = ph if fin_parity_by_phase else 0
+                yield wait(bar(("Fin", r)), fu & 1, fu)
                 # the final commit tracks every MMA issued before it; its arrival may
                 # overtake the O barrier's, which the epilogue does not read
                 assert pv_completed[0] >= (ph + 1) * n_kv, "O half read before its last P.V completed"
@@ -423,30 +238,58 @@ def simulate_pair(n_kv, slots, seed, p_count=8, arm_both=True, wait_own_empty=Tr
         assert b.pending == b.count and b.tx == 0, f"{b.name}: left mid-phase"
 
 
+# (slots, K items per tile, V items per tile and phase): 32 KB slots as built,
+# 16 KB slots (two K panels or one V panel per item), 8 KB slots (one K panel or
+# 64 keys of a V panel), shallower rings
+RINGS = [(SLOTS, K_ITEMS, V_ITEMS), (6, 4, 2), (12, 8, 4), (2, 2, 1), (1, 4, 2), (4, 4, 2), (5, 8, 4)]
+
+
 @pytest.mark.parametrize("n_kv", [1, 2, 3, 8, 17])
-@pytest.mark.parametrize("slots", [6, 1, 4])
-def test_d512_pair_protocol_is_sound(n_kv, slots):
+@pytest.mark.parametrize("ring", RINGS, ids=lambda r: "x".join(map(str, r)))
+def test_d512_protocol_is_sound(n_kv, ring):
+    slots, k_items, v_items = ring
     for seed in range(40):
-        simulate_pair(n_kv, slots, seed)
+        simulate(n_kv, slots, seed, k_items, v_items)
 
 
-def test_d512_pair_p_barrier_counting_one_cta_is_unsound():
+def test_d512_one_s_barrier_for_both_buffers_is_unsound():
+    """One S barrier and one P barrier for both S buffers: S(jj+1) can complete
+    before the softmax waits for S(jj), two phases ahead.  The model must catch it."""
+    failures = 0
+    for seed in range(100):
+        try:
+            simulate(5, SLOTS, seed, s_per_buffer=False)
+        except AssertionError:
+            failures += 1
+    assert failures > 0
+
+
+def test_d512_final_barrier_waited_with_phase_zero_twice_is_unsound():
+    """Waiting for the final barrier's phase 0 at the end of phase 1 too: the wait
+    passes at once and the second O half would be read before its last P.V
+    completed.  The model must catch it."""
+    with pytest.raises(AssertionError):
+        for seed in range(50):
+            simulate(3, SLOTS, seed, fin_parity_by_phase=False)
+
+
+def test_d512_p_barrier_counting_one_cta_is_unsound():
     """P barriers expecting four arrivals (one CTA's warps): P.V can start before
     the peer CTA has written its P.  The model must catch it."""
     with pytest.raises(AssertionError):
         for seed in range(50):
-            simulate_pair(3, 6, seed, p_count=4)
+            simulate(3, SLOTS, seed, p_count=4)
 
 
-def test_d512_pair_full_barrier_armed_for_one_cta_is_unsound():
+def test_d512_full_barrier_armed_for_one_cta_is_unsound():
     """A full barrier armed for rank 0's bytes only completes without the peer's
     copy, whose bytes then land in a later phase.  The model must catch it."""
     with pytest.raises(AssertionError):
         for seed in range(50):
-            simulate_pair(3, 6, seed, arm_both=False)
+            simulate(3, SLOTS, seed, arm_both=False)
 
 
-def test_d512_pair_one_o_barrier_is_unsound_without_ordered_delivery():
+def test_d512_one_o_barrier_is_unsound_without_ordered_delivery():
     """Every P.V completing on one O barrier: the peer's copy of an O arrival can be
     overtaken by a later S arrival, and the softmax's rescale wait then tests a
     parity two phases ahead.  With two O barriers taken in turn the previous use of
@@ -455,12 +298,12 @@ def test_d512_pair_one_o_barrier_is_unsound_without_ordered_delivery():
     with pytest.raises(AssertionError):
         for seed in range(200):
             for n_kv in (8, 17):
-                simulate_pair(n_kv, 6, seed, o_bars=1)
+                simulate(n_kv, 6, seed, 4, 2, o_bars=1)
 
 
-def test_d512_pair_peer_refilling_without_its_empty_wait_is_unsound():
+def test_d512_peer_refilling_without_its_empty_wait_is_unsound():
     """Rank 1's producer refilling a slot without waiting for its own empty
     barrier: its bytes land while the slot's previous item is still collected."""
     with pytest.raises(AssertionError):
         for seed in range(50):
-            simulate_pair(3, 2, seed, wait_own_empty=False)
+            simulate(3, 2, seed, 2, 1, wait_own_empty=False)
