@@ -176,9 +176,9 @@ static int prefill_impl(const attn_bf16_t* q, const attn_bf16_t* k, const attn_b
   a.pack = pack;
   a.n_splits = n_splits;
   a.split_min = split_min;
-  // a one-token decode (one position, kv_lens, no splits): its head rows fill one
-  // query tile, so the second tile takes the second half of each sequence's keys
-  a.halves = (kv_lens != nullptr && Sq == 1 && n_splits <= 1 && window == 0 &&
+  // a one-token decode (one position, kv_lens): its head rows fill one query tile,
+  // so the second tile takes the second half of each sequence's (or key split's) keys
+  a.halves = (kv_lens != nullptr && Sq == 1 && window == 0 &&
               (long long)pack <= attn::kPrefillTileM && !attn::prefill_uses_pair(d)) ? 1 : 0;
   a.part_o = part_o;
   a.part_lse = part_lse;

@@ -173,7 +173,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, HALVES>::kThreads, 1)
   using C = PrefillCfg<D, HALVES>;
   constexpr int NQ = C::NQ, NS = C::NS, BN = C::BN;
   static_assert(C::kSub == 1, "a KV stage is one tile (the sliding-window tile list maps tiles, not stages)");
-  static_assert(!HALVES || (NQ == 2 && NS == 1 && !WIN && !SPLIT), "key halves: two query tiles, plain keys");
+  static_assert(!HALVES || (NQ == 2 && NS == 1 && !WIN), "key halves: two query tiles, no window");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // ---- work unit ----
@@ -245,8 +245,9 @@ __global__ void __launch_bounds__(PrefillCfg<D, HALVES>::kThreads, 1)
 #pragma unroll
   for (int t = 0; t < NQ; ++t) ti[t].n_kv = klo < khi ? tile_list_len(tl, ti[t].n_kv) : 0;
   n_kv = klo < khi ? tile_list_len(tl, n_kv) : 0;
-  // key halves: tile 0 takes key tiles [0, n0), tile 1 (the same rows) [n0, n);
-  // the K/V rings run over items i = (step i / 2, tile i % 2)
+  // key halves: tile 0 takes list entries [0, n0), tile 1 (the same rows) [n0, n)
+  // (with a key split, of the split's tiles); the K/V rings run over items
+  // i = (step i / 2, tile i % 2)
   int n_items = n_kv, n0 = n_kv;
   if constexpr (HALVES) {
     const int n = ti[0].n_kv;
@@ -259,7 +260,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, HALVES>::kThreads, 1)
   }
   // key tile of ring item i (the TMA order) and of list entry j of query tile t
   auto item_key = [&](int i) -> int {
-    if constexpr (HALVES) return (i & 1) ? n0 + (i >> 1) : (i >> 1);
+    if constexpr (HALVES) return tile_list_key(tl, (i & 1) ? n0 + (i >> 1) : (i >> 1));
     return tile_list_key(tl, i);
   };
 
@@ -565,7 +566,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, HALVES>::kThreads, 1)
       tmem_wait_ld();
       // mask: keys at or past row_bound (causal bound or Skv), and with a window the
       // keys below the row's window that are not sinks
-      const int key0 = (HALVES ? (t == 1 ? n0 + j : j) : tile_list_key(tl, j)) * BN;
+      const int key0 = tile_list_key(tl, HALVES ? (t == 1 ? n0 + j : j) : j) * BN;
       if (key0 + BN > my.kv_lo || (SPLIT && key0 < klo)) {
         const int lim = row_bound - key0, low = klo - key0;  // and keys below the split
 #pragma unroll
@@ -822,7 +823,7 @@ cudaError_t launch_prefill_grid(const PrefillArgs& a, cudaStream_t stream, long 
   using C = PrefillCfg<D, H>;
   auto kern = fmha_fwd_kernel<D, false, false, false>;
   if constexpr (H) {
-    kern = fmha_fwd_kernel<D, false, false, true>;
+    kern = a.n_splits > 1 ? fmha_fwd_kernel<D, false, true, true> : fmha_fwd_kernel<D, false, false, true>;
   } else {
     if (a.window > 0) kern = fmha_fwd_kernel<D, true, false, false>;
     else if (a.n_splits > 1) kern = fmha_fwd_kernel<D, false, true, false>;

@@ -544,16 +544,17 @@ def time_mqa_decode(args, attn, W, dev, stream, flush, peaks, peak_src):
     tf = flops / (ms * 1e-3) / 1e12
     gbs = kvb / (ms * 1e-3) / 1e9
     peak_tc, peak_hbm = float(peaks["bf16_tflops"]), float(peaks["hbm_gbs"])
+    kern = f"fmha_fwd_kernel<{S.d}>"
+    traffic = load_traffic().get(f"{kern} packed {S.name}")  # DRAM bytes of the launch, both rooflines
     return {"workload": S.name, "B": S.B, "Hq": S.Hq, "Hkv": S.Hkv, "d": S.d,
             "kv_tokens": int(lens.sum()), "gflop": round(flops / 1e9, 3), "kv_mb": round(kvb / 1e6, 1),
             "us": round(ms * 1e3, 2), "value": round(tf, 2), "unit": "TFLOP/s", "gbs": round(gbs, 1),
             "steps": n,
-            "roofline": {"bound": "tensor", "kernel": f"fmha_fwd_kernel<{S.d}>", "achieved": round(tf, 2),
-                         "peak": peak_tc, "unit": "TFLOP/s", "frac": round(tf / peak_tc, 4),
+            "roofline": {"bound": "tensor", "kernel": kern, "achieved": round(tf, 2),
+                         "peak": peak_tc, "unit": "TFLOP/s", "frac": round(tf / peak_tc, 4), "traffic": traffic,
                          "peak_source": f"bf16_tflops (burst) of {peak_src}"},
-            "roofline_hbm": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak_hbm, "unit": "GB/s",
-                             "frac": round(gbs / peak_hbm, 4),
-                             "traffic": load_traffic().get(f"fmha_fwd_kernel<{S.d}> packed {S.name}"),
+            "roofline_hbm": {"bound": "hbm", "kernel": kern, "achieved": round(gbs, 1), "peak": peak_hbm,
+                             "unit": "GB/s", "frac": round(gbs / peak_hbm, 4), "traffic": traffic,
                              "peak_source": f"hbm_gbs of {peak_src}"}}
 
 
