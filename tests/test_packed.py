@@ -116,6 +116,29 @@ def test_packed_decode_split_partials(d, Hq, Hkv, n_splits, min_rows):
     check_lse(lse.cpu().numpy(), fl)
 
 
+def test_packed_decode_split_halves_with_different_maxima():
+    """A split's two key halves see score maxima far apart (the second half's keys
+    scaled up), so the merge of the halves inside each split unit rescales one of
+    them by a large factor before the split's partial is written; the partials and
+    their merge against the oracle."""
+    from attention_forward_tcgen05_gb300 import decode_split_packed, merge
+    lens = torch.tensor([1000, 777, 2049], dtype=torch.int32)
+    q, kc, vc = W.decode_inputs(len(lens), 64, 1, 128, lens, 731)
+    ramp = torch.linspace(0.2, 3.0, kc.shape[1]).view(1, -1, 1, 1)
+    kc = (kc.float() * ramp).to(torch.bfloat16)
+    q = (q.float() * 2.0).to(torch.bfloat16)
+    scale = 0.25
+    po, pl = decode_split_packed(q.cuda(), kc.cuda(), vc.cuda(), lens.cuda(), 3, 128, scale)
+    o, lse = merge(po, pl, torch.float32)
+    sync_check()
+    ro, rl = oracle.decode_split(q, kc, vc, lens, scale, 3, 128)
+    check_o(po.cpu().numpy(), ro, False)
+    check_lse(pl.cpu().numpy(), rl)
+    fo, fl = oracle.decode(q, kc, vc, lens, scale)
+    check_o(o.cpu().numpy(), fo, False)
+    check_lse(lse.cpu().numpy(), fl)
+
+
 def test_packed_decode_no_keys_with_splits():
     from attention_forward_tcgen05_gb300 import decode_split_packed
     lens = torch.zeros(3, dtype=torch.int32)
