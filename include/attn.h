@@ -87,8 +87,9 @@ typedef struct CUstream_st* attn_stream_t; /* == cudaStream_t */
  *                         Sq, Skv < 2^31; every tensor < 2^31 rows of d elements
  *   d                     head dim: 64, 128, 256 or 512.  At 512 the fp32 O of a
  *                         128-row tile fills all of tensor memory, so O is computed
- *                         in two column halves by one CTA, S = Q K^T once per half
- *                         (1.5x the tensor work of the other head dims); the pages'
+ *                         in two column halves one after the other (on CTA pairs of
+ *                         256 query rows), S = Q K^T once per half (1.5x the tensor
+ *                         work of the other head dims); the pages'
  *                         D1.4 of "STAGE_D.md -- FMHA Kernel Development" meets this
  *                         head dim as a shared-memory limit and splits the head
  *                         dimension, which the kernel does for Q, K, V and O.  Head
