@@ -52,6 +52,31 @@ def test_mixed_batch(d, causal, out_dtype):
     check_lse(lse, rl)
 
 
+def test_uneven_cached_prefixes():
+    """Twenty sequences whose query chunks (1-599 rows) sit behind cached prefixes of
+    up to 2,500 keys: a short chunk's one query block can outweigh every block of a
+    long chunk with no history.  Every row against the oracle."""
+    rng = np.random.default_rng(81)
+    seqs = [(int(rng.integers(1, 600)), 0) for _ in range(20)]
+    seqs = [(a, a + int(rng.integers(0, 2500))) for a, _ in seqs]
+    q, kc, vc, cu, kv = _case(seqs, 4, 1, 64, 82)
+    o, lse = _run(q, kc, vc, cu, kv, True, 0.125, torch.float32)
+    ro, rl = oracle.sdpa_varlen(q, kc, vc, cu, kv, True, 0.125)
+    check_o(o, ro, False)
+    check_lse(lse, rl)
+
+
+def test_many_short_sequences():
+    """301 sequences, 300 of them a few rows long and one of 900 rows: 1,204
+    (sequence, query block) units, most of them past their sequence's rows."""
+    seqs = [(int(3 + (i * 7) % 20), int(3 + (i * 7) % 20 + (i * 13) % 90)) for i in range(300)] + [(900, 1000)]
+    q, kc, vc, cu, kv = _case(seqs, 2, 1, 64, 83)
+    o, lse = _run(q, kc, vc, cu, kv, True, 0.125, torch.float32)
+    ro, rl = oracle.sdpa_varlen(q, kc, vc, cu, kv, True, 0.125)
+    check_o(o, ro, False)
+    check_lse(lse, rl)
+
+
 def test_one_sequence_equals_prefill():
     """One sequence whose keys are exactly its rows is the fixed-length prefill."""
     from attention_forward_tcgen05_gb300 import prefill
