@@ -661,6 +661,25 @@ def _pipelined_ms(n, h2d, compute, d2h, dev):
     return start.elapsed_time(end) / n
 
 
+def _staged(specs, dev):
+    """One flat byte buffer (pinned host memory when dev is None) and a contiguous
+    view of it for each (shape, dtype) in specs, every view 256-byte aligned."""
+    import torch
+
+    offs, n = [], 0
+    for shape, dtype in specs:
+        offs.append(n)
+        nbytes = torch.Size(shape).numel() * torch.empty((), dtype=dtype).element_size()
+        n += (nbytes + 255) // 256 * 256
+    buf = torch.empty(n, dtype=torch.uint8, device=dev) if dev is not None else \
+        torch.empty(n, dtype=torch.uint8).pin_memory()
+    views = []
+    for (shape, dtype), o in zip(specs, offs):
+        nbytes = torch.Size(shape).numel() * torch.empty((), dtype=dtype).element_size()
+        views.append(buf[o:o + nbytes].view(dtype).view(shape))
+    return buf, views
+
+
 def run_e2e(args, attn, W, dev, stream, P, dec, flops):
     """The step's work through the public API from pinned host buffers: every step
     copies its inputs host-to-device, runs the kernels and copies O and LSE back,
@@ -670,23 +689,30 @@ def run_e2e(args, attn, W, dev, stream, P, dec, flops):
     same work done one step at a time on one stream is reported as the latency."""
     import torch
 
-    qh, kh, vh = [t.pin_memory() for t in W.prefill_inputs_for(P)]
-    qd, kd, vd = ([torch.empty_like(t, device=dev) for _ in range(2)] for t in (qh, kh, vh))
-    od = [torch.empty((P.B, P.Sq, P.Hq, P.d), dtype=torch.bfloat16, device=dev) for _ in range(2)]
-    ld = [torch.empty((P.B, P.Hq, P.Sq), dtype=torch.float32, device=dev) for _ in range(2)]
-    oh = torch.empty((P.B, P.Sq, P.Hq, P.d), dtype=torch.bfloat16).pin_memory()
-    lh = torch.empty((P.B, P.Hq, P.Sq), dtype=torch.float32).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
-    d2h = oh.numel() * 2 + lh.numel() * 4
+    # a step's inputs sit in one pinned staging buffer and its outputs in one device
+    # buffer, so that each direction is one copy per step (three input copies and
+    # two output copies measured slower: each copy has a cost of its own)
+    q0, k0, v0 = W.prefill_inputs_for(P)
+    o_shape, l_shape = (P.B, P.Sq, P.Hq, P.d), (P.B, P.Hq, P.Sq)
+    hin, (qh, kh, vh) = _staged([(q0.shape, q0.dtype), (k0.shape, k0.dtype), (v0.shape, v0.dtype)], None)
+    for h, t in zip((qh, kh, vh), (q0, k0, v0)):
+        h.copy_(t)
+    hout, (oh, lh) = _staged([(o_shape, torch.bfloat16), (l_shape, torch.float32)], None)
+    din, dq = zip(*(_staged([(q0.shape, q0.dtype), (k0.shape, k0.dtype), (v0.shape, v0.dtype)], dev)
+                    for _ in range(2)))
+    dout, dol = zip(*(_staged([(o_shape, torch.bfloat16), (l_shape, torch.float32)], dev) for _ in range(2)))
+    h2d = hin.numel()
+    d2h = hout.numel()
 
-    def pre_in(b):  # (device, host) pairs of buffer b's inputs
-        return list(zip((qd[b], kd[b], vd[b]), (qh, kh, vh)))
+    def pre_in(b):  # (device, host) pairs of buffer b's inputs: one copy
+        return [(din[b], hin)]
 
     def pre_run(b, st):
-        attn.prefill(qd[b], kd[b], vd[b], causal=P.causal, scale=P.scale, out=(od[b], ld[b]), stream=st)
+        q_, k_, v_ = dq[b]
+        attn.prefill(q_, k_, v_, causal=P.causal, scale=P.scale, out=dol[b], stream=st)
 
-    def pre_out(b):  # (host, device) pairs of buffer b's outputs
-        return [(oh, od[b]), (lh, ld[b])]
+    def pre_out(b):  # (host, device) pairs of buffer b's outputs: one copy
+        return [(hout, dout[b])]
 
     # the ragged decode (the step's second workload) the same way
     name = list(dec)[1]
@@ -745,7 +771,7 @@ def run_e2e(args, attn, W, dev, stream, P, dec, flops):
     t_dec = _pipelined_ms(nd, dec_in, dec_run, dec_out, dev)
     attn.sync_check()
     # the pipelined steps computed what the kernels compute: compare the last copy-out
-    o_ref, l_ref = attn.prefill(qd[0], kd[0], vd[0], causal=P.causal, scale=P.scale)
+    o_ref, l_ref = attn.prefill(*dq[0], causal=P.causal, scale=P.scale)
     torch.cuda.synchronize()
     assert torch.equal(oh, o_ref.cpu()) and torch.equal(lh, l_ref.cpu()), "pipelined e2e output differs"
     kv = dd["kv_bytes"]
